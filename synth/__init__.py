@@ -1,0 +1,321 @@
+"""Seeded synthetic decode workloads, shared by the tests, the benchmark and
+the oracle checks.
+
+This module draws random numbers and lays out buffers; it holds none of the
+decode path's arithmetic (no Q quantization, no attention, no plan). It does
+act as the KV-cache WRITER for its synthetic caches — the step that comes
+before the decode path (a cache write at ``slot_mapping``) — so it rounds
+N(0,1) values to the stored code format:
+
+* e4m3 KV: ``torch``'s own ``float8_e4m3fn`` conversion of ``X / s`` with
+  ``s = amax/448`` per tensor or per KV head;
+* e2m3 KV: nearest of the 64 e2m3 values (ties to the even code) of
+  ``X / s_c`` with static per-(KV head, channel) scales ``s_c = amax/7.5``,
+  packed 4 codes per 3 bytes as a little-endian bitstream.
+
+Unused pool pages and the tail slots of each request's last page are
+poisoned (e4m3 NaN ``0x7F``; e2m3 has no NaN, so its largest code ``0x1F``),
+and unused block-table entries are ``-1``: a decode path that reads past a
+request's last valid key shows up as NaN or as a wrong result.
+
+Every array is host (numpy) memory; callers move it to the device.
+The named workloads follow the shapes of the pages' target model
+(Qwen3-8B: 32 query heads, 8 KV heads, head size 128) at the sizes of the
+five benchmark configurations; :func:`make_case` builds any smaller case.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+E4M3_NAN = 0x7F
+E2M3_POISON = 0x1F
+
+
+def _rng(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), int(stream)])))
+
+
+# sub-stream ids
+_S_Q, _S_K, _S_V, _S_LENS, _S_PAGES, _S_OUTLIER_K, _S_OUTLIER_V = range(7)
+
+
+@dataclass
+class Workload:
+    name: str
+    num_seqs: int  # requests, real + trailing padding
+    q_len: int
+    h_q: int
+    h_k: int
+    d: int
+    page_size: int
+    kv_format: str  # "fp8" | "e2m3"
+    layout: str  # "HND" | "NHD"
+    causal: bool
+    seq_lens: np.ndarray  # int32 [B]; padding requests 0
+    block_table: np.ndarray  # int32 [B, max_blocks]; unused entries -1
+    num_pages: int
+    q_bits: np.ndarray  # uint16 [B*q_len, h_q, d], bf16 bit patterns
+    q_f32: np.ndarray  # float32 [B*q_len, h_q, d], the same values
+    k_cache: np.ndarray  # uint8 physical buffer
+    v_cache: np.ndarray
+    kv_strides: tuple  # (page, token, head) byte strides of k_cache/v_cache
+    row_bytes: int
+    k_scale: np.ndarray  # float32: (1,) per tensor, (h_k,) per head
+    v_scale: np.ndarray
+    q_mul: np.ndarray | None = None  # float32 [h_q, d] (e2m3: K channel scales)
+    o_mul: np.ndarray | None = None  # float32 [h_q, d] (e2m3: V channel scales)
+    softmax_scale: float = 0.0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def h_r(self) -> int:
+        return self.h_q // self.h_k
+
+    @property
+    def n_q(self) -> int:
+        return self.q_len * self.h_r
+
+    def logical(self, which: str) -> np.ndarray:
+        """``[num_pages, page_size, h_k, row_bytes]`` view of the K or V buffer."""
+        buf = self.k_cache if which == "k" else self.v_cache
+        if self.layout == "HND":
+            return buf.transpose(0, 2, 1, 3)
+        return buf
+
+
+# ----------------------------------------------------------------------------
+# synthetic cache writer
+# ----------------------------------------------------------------------------
+def _e4m3_codes(x: np.ndarray) -> np.ndarray:
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def _e2m3_grid():
+    """The 32 non-negative e2m3 magnitudes in code order (codes 0..31)."""
+    vals = []
+    for code in range(32):
+        e, m = code >> 3, code & 7
+        vals.append(m / 8.0 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 1))
+    return np.array(vals)
+
+
+_E2M3_GRID = _e2m3_grid()
+
+
+def _e2m3_codes(x: np.ndarray) -> np.ndarray:
+    a = np.abs(x.astype(np.float64))
+    i = np.clip(np.searchsorted(_E2M3_GRID, a, side="right") - 1, 0, 31)
+    j = np.minimum(i + 1, 31)
+    lo, hi = _E2M3_GRID[i], _E2M3_GRID[j]
+    up = (2 * a > lo + hi) | ((2 * a == lo + hi) & (i % 2 == 1))
+    c = np.where(up, j, i)
+    c = np.where(a >= 7.5, 31, c)
+    return (c | np.where(np.signbit(x), 0x20, 0)).astype(np.uint8)
+
+
+def pack_e2m3(codes: np.ndarray) -> np.ndarray:
+    """``[..., 4k]`` 6-bit codes -> ``[..., 3k]`` bytes, little-endian bitstream."""
+    c = codes.astype(np.uint32).reshape(codes.shape[:-1] + (-1, 4))
+    c0, c1, c2, c3 = c[..., 0], c[..., 1], c[..., 2], c[..., 3]
+    b0 = (c0 | (c1 << 6)) & 0xFF
+    b1 = ((c1 >> 2) | (c2 << 4)) & 0xFF
+    b2 = ((c2 >> 4) | (c3 << 2)) & 0xFF
+    out = np.stack([b0, b1, b2], axis=-1).astype(np.uint8)
+    return out.reshape(codes.shape[:-1] + (-1,))
+
+
+# ----------------------------------------------------------------------------
+# builder
+# ----------------------------------------------------------------------------
+def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_lens, layout="HND",
+              kv_format="fp8", scale_mode="head", causal=True, pool_pages=None, seed=0,
+              outlier_channels=0, outlier_gain=10.0, extra_block_cols=0) -> Workload:
+    """Build a seeded workload.
+
+    ``seq_lens``: lengths of all ``num_seqs`` requests (0 = padding request).
+    ``pool_pages``: pool size; default exactly the pages the requests use.
+    Pages are drawn without replacement from the pool in a seeded random
+    order. ``scale_mode``: "tensor" | "head" (e4m3) — e2m3 always uses
+    per-(KV head, channel) scales folded into ``q_mul`` / ``o_mul``.
+    """
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    assert seq_lens.shape == (num_seqs,)
+    h_r = h_q // h_k
+    pages_per = [math.ceil(int(L) / page_size) for L in seq_lens]
+    need = sum(pages_per)
+    pool = need if pool_pages is None else int(pool_pages)
+    assert pool >= need
+    pool = max(pool, 1)
+    max_blocks = max([1] + pages_per) + extra_block_cols
+
+    order = _rng(seed, _S_PAGES).permutation(pool)[:need].astype(np.int32)
+    block_table = np.full((num_seqs, max_blocks), -1, dtype=np.int32)
+    off = 0
+    for b, n in enumerate(pages_per):
+        block_table[b, :n] = order[off:off + n]
+        off += n
+
+    # (page, slot) of every valid token, request-major
+    tok_pages, tok_slots = [], []
+    for b, L in enumerate(seq_lens):
+        j = np.arange(int(L))
+        tok_pages.append(block_table[b, j // page_size])
+        tok_slots.append(j % page_size)
+    tok_pages = np.concatenate(tok_pages) if tok_pages else np.zeros(0, np.int32)
+    tok_slots = np.concatenate(tok_slots) if tok_slots else np.zeros(0, np.int64)
+    n_tok = len(tok_pages)
+
+    row_bytes = d if kv_format == "fp8" else d * 6 // 8
+    if layout == "HND":
+        shape = (pool, h_k, page_size, row_bytes)
+        strides = (h_k * page_size * row_bytes, row_bytes, page_size * row_bytes)
+    elif layout == "NHD":
+        shape = (pool, page_size, h_k, row_bytes)
+        strides = (page_size * h_k * row_bytes, h_k * row_bytes, row_bytes)
+    else:
+        raise ValueError(layout)
+
+    if kv_format == "fp8":
+        poison_row = np.full(row_bytes, E4M3_NAN, dtype=np.uint8)
+    else:
+        poison_row = pack_e2m3(np.full(d, E2M3_POISON, dtype=np.uint8))
+
+    meta = {}
+    caches, scales, chans = {}, {}, {}
+    for which, stream, ostream in (("k", _S_K, _S_OUTLIER_K), ("v", _S_V, _S_OUTLIER_V)):
+        buf = np.empty(shape, dtype=np.uint8)
+        buf[...] = poison_row
+        rng = _rng(seed, stream)
+        orng = _rng(seed, ostream)
+        per_head_scale = np.zeros(h_k, dtype=np.float32)
+        ch_scale = np.zeros((h_k, d), dtype=np.float32)
+        tensor_scale = np.float32(1.0)
+        xs = []
+        for g in range(h_k):
+            x = rng.standard_normal((n_tok, d), dtype=np.float32)
+            if outlier_channels:
+                ch = orng.choice(d, size=outlier_channels, replace=False)
+                x[:, ch] *= np.float32(outlier_gain)
+                meta.setdefault(f"{which}_outlier_channels", []).append(sorted(int(c) for c in ch))
+            xs.append(x)
+        if kv_format == "fp8" and scale_mode == "tensor":
+            amax = max([float(np.abs(x).max()) if x.size else 0.0 for x in xs] + [1e-30])
+            tensor_scale = np.float32(amax / 448.0)
+        for g in range(h_k):
+            x = xs[g]
+            if kv_format == "fp8":
+                if scale_mode == "tensor":
+                    s = tensor_scale
+                else:
+                    s = np.float32((float(np.abs(x).max()) if x.size else 1.0) / 448.0)
+                    per_head_scale[g] = s
+                codes = _e4m3_codes(x / s)
+            else:
+                s_c = (np.abs(x).max(axis=0) if x.size else np.ones(d)).astype(np.float32) / np.float32(7.5)
+                s_c = np.maximum(s_c, np.float32(1e-30))
+                ch_scale[g] = s_c
+                codes = pack_e2m3(_e2m3_codes(x / s_c[None, :]))
+            if layout == "HND":
+                buf[tok_pages, g, tok_slots, :] = codes
+            else:
+                buf[tok_pages, tok_slots, g, :] = codes
+            xs[g] = None
+        caches[which] = buf
+        if kv_format == "fp8":
+            scales[which] = (np.array([tensor_scale], dtype=np.float32) if scale_mode == "tensor"
+                             else per_head_scale)
+        else:
+            scales[which] = np.ones(1, dtype=np.float32)
+            chans[which] = ch_scale
+
+    qrng = _rng(seed, _S_Q)
+    q = qrng.standard_normal((num_seqs * q_len, h_q, d), dtype=np.float32)
+    import torch
+
+    qb = torch.from_numpy(q).to(torch.bfloat16)
+    q_bits = qb.view(torch.int16).numpy().view(np.uint16).copy()
+    q_f32 = qb.to(torch.float32).numpy().copy()
+
+    q_mul = o_mul = None
+    if kv_format == "e2m3":
+        q_mul = np.repeat(chans["k"], h_r, axis=0).astype(np.float32)
+        o_mul = np.repeat(chans["v"], h_r, axis=0).astype(np.float32)
+
+    return Workload(name=name, num_seqs=num_seqs, q_len=q_len, h_q=h_q, h_k=h_k, d=d,
+                    page_size=page_size, kv_format=kv_format, layout=layout, causal=causal,
+                    seq_lens=seq_lens, block_table=block_table, num_pages=pool, q_bits=q_bits,
+                    q_f32=q_f32, k_cache=caches["k"], v_cache=caches["v"], kv_strides=strides,
+                    row_bytes=row_bytes, k_scale=scales["k"], v_scale=scales["v"], q_mul=q_mul,
+                    o_mul=o_mul, softmax_scale=1.0 / math.sqrt(d), meta=meta)
+
+
+# ----------------------------------------------------------------------------
+# the five benchmark configurations
+# ----------------------------------------------------------------------------
+def _uniform_lens(seed, n, lo, hi):
+    return _rng(seed, _S_LENS).integers(lo, hi + 1, size=n).astype(np.int32)
+
+
+def tiny(seed: int = 1001) -> Workload:
+    """B=2, q_len=1, 8/2 heads, D=128, page 16, lens {37, 100}, e4m3 KV with one
+    per-tensor scale each for K and V, HND, 10 pages in a seeded permutation."""
+    return make_case(name="tiny", num_seqs=2, q_len=1, h_q=8, h_k=2, page_size=16,
+                     seq_lens=[37, 100], layout="HND", scale_mode="tensor", seed=seed)
+
+
+def qwen3_8b_decode(seed: int = 1002) -> Workload:
+    """B=64, q_len=1, 32/8 heads, page 16, every length 4096, per-KV-head e4m3
+    scales, HND, 16384 distinct pages drawn from a 20000-page pool."""
+    return make_case(name="qwen3_8b_decode", num_seqs=64, q_len=1, h_q=32, h_k=8, page_size=16,
+                     seq_lens=[4096] * 64, layout="HND", scale_mode="head", pool_pages=20000,
+                     seed=seed)
+
+
+def long_split(seed: int = 1003) -> Workload:
+    """B=8, q_len=1, 32/8 heads, page 64, lengths uniform in [32768, 131072],
+    per-KV-head e4m3 scales, NHD."""
+    return make_case(name="long_split", num_seqs=8, q_len=1, h_q=32, h_k=8, page_size=64,
+                     seq_lens=_uniform_lens(seed, 8, 32768, 131072), layout="NHD",
+                     scale_mode="head", seed=seed)
+
+
+def long_single(seed: int = 1013) -> Workload:
+    """B=1, a single 131072-token sequence, otherwise as :func:`long_split`."""
+    return make_case(name="long_single", num_seqs=1, q_len=1, h_q=32, h_k=8, page_size=64,
+                     seq_lens=[131072], layout="NHD", scale_mode="head", seed=seed)
+
+
+def spec_verify(causal: bool = True, seed: int = 1004) -> Workload:
+    """B = 32 real + 8 trailing zero-token padding requests, q_len=4, page 32,
+    lengths uniform in [1024, 16384], one per-tensor e4m3 scale, HND."""
+    lens = np.concatenate([_uniform_lens(seed, 32, 1024, 16384), np.zeros(8, np.int32)])
+    return make_case(name="spec_verify" + ("" if causal else "_noncausal"), num_seqs=40, q_len=4,
+                     h_q=32, h_k=8, page_size=32, seq_lens=lens, layout="HND",
+                     scale_mode="tensor", causal=causal, seed=seed)
+
+
+def fp6_decode(seed: int = 1005) -> Workload:
+    """B=128, q_len=1, 64/8 heads (GQA 8), page 128, every length 8192, packed
+    e2m3 KV with 4 seeded x10 outlier channels per KV head (independently for
+    K and V) and per-(KV head, channel) scales = amax/7.5, HND."""
+    return make_case(name="fp6_decode", num_seqs=128, q_len=1, h_q=64, h_k=8, page_size=128,
+                     seq_lens=[8192] * 128, layout="HND", kv_format="e2m3", outlier_channels=4,
+                     seed=seed)
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "qwen3_8b_decode": qwen3_8b_decode,
+    "long_split": long_split,
+    "long_single": long_single,
+    "spec_verify": spec_verify,
+    "spec_verify_noncausal": lambda seed=1004: spec_verify(False, seed),
+    "fp6_decode": fp6_decode,
+}

@@ -1,0 +1,190 @@
+"""Pins of the oracle's exact paged decode attention and of the LSE merge."""
+
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+
+import synth
+from oracle import attention as A
+from oracle import formats as F
+from oracle.qquant import quantize_q
+
+
+def _run(w, units=None, causal=None):
+    codes, desc = quantize_q(w.q_f32, w.num_seqs, w.q_len, w.h_q, w.h_k, w.d, w.q_mul)
+    out, lse = A.decode_attention(
+        codes, desc, w.logical("k"), w.logical("v"), w.k_scale, w.v_scale, w.block_table,
+        w.seq_lens, num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
+        page_size=w.page_size, kv_format=w.kv_format, softmax_scale=w.softmax_scale,
+        causal=w.causal if causal is None else causal, o_mul=w.o_mul, units=units)
+    return codes, desc, out, lse
+
+
+def _small(**kw):
+    base = dict(num_seqs=3, q_len=1, h_q=4, h_k=2, d=128, page_size=16, seq_lens=[5, 33, 17],
+                layout="HND", seed=11)
+    base.update(kw)
+    return synth.make_case(**base)
+
+
+@pytest.mark.parametrize("kv_format,q_len,causal", [("fp8", 1, True), ("fp8", 3, True),
+                                                    ("fp8", 3, False), ("e2m3", 2, True)])
+def test_matches_brute_force(kv_format, q_len, causal):
+    w = _small(kv_format=kv_format, q_len=q_len, causal=causal, seq_lens=[5, 21, 9],
+               outlier_channels=2 if kv_format == "e2m3" else 0)
+    codes, desc, out, _ = _run(w)
+    for b in range(w.num_seqs):
+        for g in range(w.h_k):
+            bf = A.brute_force_unit(codes[b, g], float(desc[b, g]), w.logical("k"), w.logical("v"),
+                                    A.descale_at(w.k_scale, b, g), A.descale_at(w.v_scale, b, g),
+                                    w.block_table, b, g, int(w.seq_lens[b]), w.page_size, w.kv_format,
+                                    w.softmax_scale, w.q_len, w.h_r, causal)
+            for row in range(w.n_q):
+                t, r = divmod(row, w.h_r)
+                o = out[b * w.q_len + t, g * w.h_r + r]
+                want = bf[row] * (w.o_mul[g * w.h_r + r] if w.o_mul is not None else 1.0)
+                np.testing.assert_allclose(o, want, rtol=1e-10, atol=1e-12)
+
+
+def test_paged_equals_contiguous_and_page_permutation():
+    """The same tokens scattered over random pages of a larger pool, or laid
+    out contiguously from page 0, give the same result."""
+    w1 = _small(pool_pages=40, seed=5)
+    w2 = _small(pool_pages=40, seed=5)
+    bt = np.full_like(w2.block_table, -1)
+    kc = np.zeros_like(w2.k_cache)
+    vc = np.zeros_like(w2.v_cache)
+    nxt = 0
+    for b in range(w2.num_seqs):
+        for j, p in enumerate(w2.block_table[b]):
+            if p < 0:
+                continue
+            bt[b, j] = nxt
+            kc[nxt] = w2.k_cache[p]
+            vc[nxt] = w2.v_cache[p]
+            nxt += 1
+    w2.block_table, w2.k_cache, w2.v_cache = bt, kc, vc
+    _, _, o1, l1 = _run(w1)
+    _, _, o2, l2 = _run(w2)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_hnd_and_nhd_views_agree():
+    w1 = _small(layout="HND", seed=9)
+    w2 = _small(layout="NHD", seed=9)
+    np.testing.assert_array_equal(w1.logical("k"), w2.logical("k"))
+    _, _, o1, _ = _run(w1)
+    _, _, o2, _ = _run(w2)
+    np.testing.assert_array_equal(o1, o2)
+
+
+def test_constant_v_returns_v():
+    w = _small()
+    w.v_cache[...] = F.e4m3_encode(1.5)
+    _, _, out, _ = _run(w)
+    for b in range(w.num_seqs):
+        for g in range(w.h_k):
+            v = 1.5 * A.descale_at(w.v_scale, b, g)
+            np.testing.assert_allclose(out[b, g * w.h_r:(g + 1) * w.h_r], v, rtol=1e-13)
+
+
+def test_single_key_returns_its_v_row():
+    w = _small(seq_lens=[1, 1, 1])
+    _, _, out, _ = _run(w)
+    for b in range(w.num_seqs):
+        for g in range(w.h_k):
+            p = w.block_table[b, 0]
+            v = F.e4m3_decode(w.logical("v")[p, 0, g]) * A.descale_at(w.v_scale, b, g)
+            for r in range(w.h_r):
+                np.testing.assert_allclose(out[b, g * w.h_r + r], v, rtol=1e-13)
+
+
+def test_one_row_is_scipy_softmax_times_v():
+    w = _small()
+    codes, desc, out, lse = _run(w)
+    b, g = 1, 1
+    L = int(w.seq_lens[b])
+    kc, vc = A.gather_unit(w.logical("k"), w.logical("v"), w.block_table, b, g, L, w.page_size)
+    q = F.e4m3_decode(codes[b, g, 0]) * float(desc[b, g])
+    k = F.e4m3_decode(kc) * A.descale_at(w.k_scale, b, g)
+    v = F.e4m3_decode(vc) * A.descale_at(w.v_scale, b, g)
+    s = w.softmax_scale * (k @ q)
+    np.testing.assert_allclose(out[b, g * w.h_r], scipy.special.softmax(s) @ v, rtol=1e-12)
+    assert math.isclose(lse[b, g, 0], scipy.special.logsumexp(s), rel_tol=1e-12)
+
+
+def test_causal_last_row_equals_noncausal_and_prefix_rule():
+    w = _small(q_len=4, seq_lens=[9, 40, 23])
+    _, _, oc, _ = _run(w, causal=True)
+    _, _, on, _ = _run(w, causal=False)
+    ql = w.q_len
+    for b in range(w.num_seqs):
+        np.testing.assert_array_equal(oc[b * ql + ql - 1], on[b * ql + ql - 1])
+        assert not np.allclose(oc[b * ql], on[b * ql])
+    # causal row t == non-causal result over the prefix L - q_len + t + 1
+    codes, desc = quantize_q(w.q_f32, w.num_seqs, ql, w.h_q, w.h_k, w.d)
+    for b in range(w.num_seqs):
+        L = int(w.seq_lens[b])
+        for t in range(ql):
+            pre = L - ql + t + 1
+            lens = np.array([pre if i == b else 0 for i in range(w.num_seqs)])
+            o2, _ = A.decode_attention(codes, desc, w.logical("k"), w.logical("v"), w.k_scale,
+                                       w.v_scale, w.block_table, lens, num_seqs=w.num_seqs,
+                                       q_len=ql, h_q=w.h_q, h_k=w.h_k, d=w.d,
+                                       page_size=w.page_size, kv_format="fp8",
+                                       softmax_scale=w.softmax_scale, causal=False)
+            np.testing.assert_allclose(oc[b * ql + t], o2[b * ql + t], rtol=1e-12, atol=1e-15)
+
+
+def test_gqa_heads_with_equal_q_give_equal_o():
+    w = _small()
+    h_r = w.h_r
+    for g in range(w.h_k):
+        for r in range(1, h_r):
+            w.q_f32[:, g * h_r + r] = w.q_f32[:, g * h_r]
+    _, _, out, _ = _run(w)
+    for g in range(w.h_k):
+        for r in range(1, h_r):
+            np.testing.assert_array_equal(out[:, g * h_r + r], out[:, g * h_r])
+
+
+def test_padding_requests_write_nothing():
+    w = _small(seq_lens=[7, 0, 0])
+    _, _, out, lse = _run(w)
+    assert np.all(np.isfinite(out[0]))
+    assert np.all(np.isnan(out[1:])) and np.all(np.isnan(lse[1:]))
+
+
+def test_split_merge_equals_unsplit():
+    rng = np.random.default_rng(4)
+    for trial in range(20):
+        L = int(rng.integers(1, 300))
+        n_q, d = int(rng.integers(1, 9)), 16
+        s = rng.standard_normal((n_q, L)) * rng.uniform(0.1, 8)
+        v = rng.standard_normal((L, d))
+        vis = np.ones((n_q, L), bool)
+        if trial % 3 == 0:
+            vis = np.arange(L)[None, :] <= (L - n_q + np.arange(n_q))[:, None]
+            vis[:, 0] = True
+        m, l, o = A.chunk_partial(s, vis, v, 0, L)
+        cuts = np.sort(rng.integers(0, L + 1, size=int(rng.integers(0, 6))))
+        bounds = [0] + list(cuts) + [L, L]  # includes empty chunks
+        parts = [A.chunk_partial(s, vis, v, a, e) for a, e in zip(bounds[:-1], bounds[1:])]
+        om, lse = A.merge_partials([p[0] for p in parts], [p[1] for p in parts], [p[2] for p in parts])
+        np.testing.assert_allclose(om, o, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse, m + np.log(l), rtol=1e-12)
+
+
+def test_bf16_rounding():
+    assert A.to_bf16(1.0) == 1.0
+    assert A.to_bf16(1.0 + 2 ** -9) == 1.0  # tie -> even
+    assert A.to_bf16(1.0 + 3 * 2 ** -9) == 1.0 + 2 ** -7  # tie -> even (up)
+    assert A.to_bf16(1.0 + 2 ** -8 + 2 ** -20) == 1.0 + 2 ** -7
+    assert A.to_bf16(-3.0) == -3.0
+    import torch
+    x = np.random.default_rng(0).standard_normal(10000).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(A.to_bf16(x.astype(np.float64)), ref)

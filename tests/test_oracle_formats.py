@@ -1,0 +1,128 @@
+"""Pins of the oracle's number formats (e4m3, e2m3, fp6 packing)."""
+
+import math
+
+import numpy as np
+import torch
+
+from oracle import formats as F
+
+
+def _parse_value(s):
+    return float("nan") if s == "nan" else float(s)
+
+
+def test_e4m3_golden_values(golden):
+    for row in golden("e4m3_codes.txt"):
+        code_s, val_s = row.split()[:2]
+        code, want = int(code_s, 16), _parse_value(val_s)
+        got = F.e4m3_value(code)
+        if math.isnan(want):
+            assert math.isnan(got), code_s
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), code_s
+
+
+def test_e2m3_golden_values(golden):
+    for row in golden("e2m3_codes.txt"):
+        code_s, val_s = row.split()[:2]
+        code, want = int(code_s, 16), _parse_value(val_s)
+        got = F.e2m3_value(code)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want), code_s
+
+
+def test_e4m3_table_shape_and_order():
+    t = F.E4M3_TABLE
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert np.sum(np.isnan(t)) == 2
+    pos = t[:0x7F]
+    assert np.all(np.diff(pos) > 0)  # strictly increasing with the code
+    assert np.array_equal(t[0x80:0xFF], -pos)  # sign symmetry
+    assert pos[-1] == 448.0 and pos[1] == 2.0 ** -9
+
+
+def test_e4m3_roundtrip_all_codes():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = F.e4m3_decode(codes)
+    back = F.e4m3_encode(vals)
+    assert np.array_equal(back, codes)
+
+
+def test_e4m3_midpoints_go_to_even():
+    pos = F.E4M3_TABLE[:0x7F]
+    for c in range(0x7E):
+        mid = (pos[c] + pos[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert F.e4m3_encode(mid) == even, hex(c)
+        assert F.e4m3_encode(-mid) == (even | 0x80), hex(c)
+        # just off the midpoint goes to the nearer neighbour
+        eps = (pos[c + 1] - pos[c]) * 1e-6
+        assert F.e4m3_encode(mid - eps) == c
+        assert F.e4m3_encode(mid + eps) == c + 1
+
+
+def test_e4m3_saturation_and_nan():
+    assert F.e4m3_encode(448.0) == 0x7E
+    assert F.e4m3_encode(460.0) == 0x7E
+    assert F.e4m3_encode(1e9) == 0x7E
+    assert F.e4m3_encode(-1e9) == 0xFE
+    assert F.e4m3_encode(float("nan")) == 0x7F
+    assert F.e4m3_encode(-0.0) == 0x80
+    assert F.e4m3_encode(0.0) == 0x00
+    assert F.e4m3_encode(2.0 ** -11) == 0x00  # below half the smallest subnormal
+    assert F.e4m3_encode(2.0 ** -10) == 0x00  # exact half: tie to even (0)
+    assert F.e4m3_encode(3 * 2.0 ** -11) == 0x01  # 0.75 * 2^-9 rounds up to 2^-9
+
+
+def test_e4m3_matches_torch_conversion():
+    """torch's float8_e4m3fn conversion is round-to-nearest-even; on the
+    range the Q path produces (|x| <= 448) it must agree bit for bit."""
+    rng = np.random.default_rng(7)
+    xs = [
+        rng.uniform(-448, 448, 200000),
+        rng.standard_normal(200000) * 3,
+        rng.uniform(-0.05, 0.05, 200000),  # subnormal neighbourhood
+        np.ldexp(rng.uniform(1, 2, 50000), rng.integers(-12, 9, 50000)) * rng.choice([-1, 1], 50000),
+    ]
+    x = np.concatenate(xs).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ours = F.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e2m3_every_value_is_an_e4m3_value():
+    """Each e2m3 value is exactly representable in e4m3 (2 exponent bits and
+    3 mantissa bits fit inside 4 and 3): a property of the two formats."""
+    for c in range(64):
+        v = F.e2m3_value(c)
+        code = F.e4m3_encode(v)
+        assert F.e4m3_value(int(code)) == v
+
+
+def test_e2m3_range():
+    t = F.E2M3_TABLE
+    assert t.max() == 7.5 and t.min() == -7.5
+    assert np.all(np.diff(t[:32]) > 0)
+    assert np.array_equal(t[32:], -t[:32])
+
+
+def test_fp6_unpack_golden(golden):
+    for row in golden("fp6_packing.txt"):
+        codes_s, bytes_s = row.split("|")
+        codes = [int(x) for x in codes_s.split()]
+        raw = np.array([int(x, 16) for x in bytes_s.split()], dtype=np.uint8)
+        got = F.fp6_unpack_rows(raw[None, :])[0]
+        assert list(got) == codes, row
+
+
+def test_fp6_unpack_matches_independent_packer():
+    """The synthetic cache writer packs with shifts; the oracle unpacks bit
+    by bit: two independent statements of the same bitstream reading."""
+    from synth import pack_e2m3
+
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 64, size=(50, 128)).astype(np.uint8)
+    packed = pack_e2m3(codes)
+    assert packed.shape == (50, 96)
+    assert np.array_equal(F.fp6_unpack_rows(packed), codes)

@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode-attention step on GB300.
+
+A step is the whole hot path over one batch: the split-KV plan (host) and
+its upload, ``mj_quantize_q``, ``mj_decode_attention`` and ``mj_merge_lse``.
+Default workload: the Qwen3-8B-shaped decode batch (B=64, q_len=1, 32/8
+heads, D=128, page 16, every length 4096, per-KV-head e4m3 scales, HND,
+16384 pages drawn from a 20000-page pool). Prints ONE JSON line.
+
+* ``value``: effective KV GB/s = sum(seq_len) * h_k * 2 * row_bytes per step
+  / device step time (CUDA events on the launching stream), inputs resident in
+  HBM. The KV read per step (537 MB) is larger than the 129 MB L2, so no
+  flush is needed between steps.
+* ``e2e``: the same metric end to end through the C ABI from pinned host
+  buffers: each step plans on the host, copies Q, seq_lens, the block table
+  and the plan to the device, runs the three kernels and copies O back.
+* ``roofline``: the decode kernel alone, algorithmic KV bytes per launch /
+  its average CUDA-event duration, against the measured HBM copy bandwidth.
+* ``cpu_baseline``: the CPU oracle timed on a bounded sample in a
+  single-threaded subprocess.
+
+``--impl reference`` times the CPU oracle itself, one (request, KV head)
+unit per step. Under torchrun every rank runs an independent replica
+(weak scaling); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn effective KV GB/s (% of HBM peak) and decode tokens/s per step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# knobs per workload: (ctas_per_sm, max_splits, kv_stages)
+DEFAULT_KNOBS = {
+    "qwen3_8b_decode": (4, 64, 0),
+    "long_split": (2, 64, 0),
+    "long_single": (2, 64, 0),
+    "spec_verify": (2, 64, 0),
+    "spec_verify_noncausal": (2, 64, 0),
+    "fp6_decode": (2, 64, 0),
+    "tiny": (2, 16, 0),
+}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001 - absent on a box that had no measurement
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "paged_fp8_decode_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(f"{kernel_file}:{workload}")
+    except Exception:  # noqa: BLE001
+        return None
+    if not rec or rec.get("source_sha") != _kernel_source_hash(kernel_file):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        time.sleep(0.05)
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+            out = ""
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def summary(self):
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle legs
+# ----------------------------------------------------------------------------
+def _oracle_unit_seconds(w, units):
+    """Time the oracle on the given (request, KV head) units: Q quantization
+    of the whole batch + exact attention of each unit."""
+    from oracle import attention as OA
+    from oracle.qquant import quantize_q
+
+    t0 = time.perf_counter()
+    codes, desc = quantize_q(w.q_f32, w.num_seqs, w.q_len, w.h_q, w.h_k, w.d, w.q_mul)
+    OA.decode_attention(codes, desc, w.logical("k"), w.logical("v"), w.k_scale, w.v_scale, w.block_table,
+                        w.seq_lens, num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
+                        page_size=w.page_size, kv_format=w.kv_format, softmax_scale=w.softmax_scale,
+                        causal=w.causal, o_mul=w.o_mul, units=units)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_child(workload: str, budget_s: float):
+    """Run in a single-threaded subprocess: oracle KV GB/s on a time-bounded
+    sample of the workload's units."""
+    import synth
+
+    w = synth.WORKLOADS[workload]()
+    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    units = [(b, g) for b in range(w.num_seqs) for g in range(w.h_k) if w.seq_lens[b] > 0]
+    done, nbytes, t = 0, 0, 0.0
+    while t < budget_s and done < len(units):
+        batch = units[done:done + 8]
+        t += _oracle_unit_seconds(w, batch)
+        nbytes += sum(int(w.seq_lens[b]) for b, _ in batch) * 2 * row
+        done += len(batch)
+    print(json.dumps({"value": nbytes / t / 1e9, "units": done, "total_units": len(units), "seconds": t,
+                      "bytes": nbytes}))
+
+
+def run_cpu_baseline(workload: str, budget_s: float = 12.0):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", workload,
+                        "--budget", str(budget_s)], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
+    j = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(j["value"], 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{j['units']} of {j['total_units']} (request, KV head) units of {workload}: Q "
+                      f"quantization of the batch + exact fp64 attention, {j['seconds']:.1f} s single-threaded"}
+
+
+def reference_arm(args):
+    """--impl reference: the CPU oracle, one (request, KV head) unit per step."""
+    import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]()
+    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    units = [(b, g) for b in range(w.num_seqs) for g in range(w.h_k) if w.seq_lens[b] > 0]
+    for i in range(args.warmup):
+        _oracle_unit_seconds(w, [units[i % len(units)]])
+    t, nbytes, toks = 0.0, 0, 0
+    for i in range(args.steps):
+        b, g = units[(args.warmup + i) % len(units)]
+        t += _oracle_unit_seconds(w, [(b, g)])
+        nbytes += int(w.seq_lens[b]) * 2 * row
+    value = nbytes / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "unit_per_step": "one (request, KV head)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} (request, KV head) units of {args.workload}, one per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def main_ours(args):
+    import numpy as np
+    import torch
+
+    import synth
+    from paged_fp8_decode_gb300 import (DecodeStep, mj_decode_attention, mj_merge_lse, mj_quantize_q,
+                                        mj_workspace_status)
+    from paged_fp8_decode_gb300.build import build
+    from paged_fp8_decode_gb300.step import paged_kv_from_workload, q_from_workload
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_base = run_cpu_baseline(args.workload)
+
+    build()
+    w = synth.WORKLOADS[args.workload](seed=1002 + 17 * rank) if args.workload == "qwen3_8b_decode" else \
+        synth.WORKLOADS[args.workload]()
+    cps, msplit, stages = DEFAULT_KNOBS.get(args.workload, (2, 64, 0))
+    cps = args.ctas_per_sm or cps
+    msplit = args.max_splits or msplit
+    stages = args.kv_stages if args.kv_stages is not None else stages
+    impl = {"auto": 0, "simt": 1, "tcgen05": 2}[args.variant]
+
+    torch.cuda.set_device(dev)
+    kv = paged_kv_from_workload(w, dev)
+    q = q_from_workload(w, dev)
+    out = torch.empty(w.num_seqs * w.q_len, w.h_q, w.d, dtype=torch.bfloat16, device=dev)
+    step = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d, ctas_per_sm=cps,
+                      max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    info = step.plan(w.seq_lens, w.num_seqs, stream)
+    a = step.args(kv, out, w.num_seqs, w.softmax_scale)
+    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.h_k * 2 * row
+    tokens = int((w.seq_lens > 0).sum()) * w.q_len
+    launches_per_step = 2 + (1 if info["with_reduction"] else 0)
+
+    def device_step(ev=None):
+        mj_quantize_q(q, w.num_seqs, w.q_len, w.h_k, step.q_codes, step.q_descale, q_mul=kv.q_mul,
+                      stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        mj_decode_attention(a, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mj_merge_lse(a, stream)
+
+    for _ in range(max(3, args.warmup)):
+        device_step()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+
+    # ---- device-resident timed region -------------------------------------
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            device_step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    decode_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = mj_workspace_status(step.workspace, stream)
+
+    # ---- end to end through host buffers ----------------------------------
+    q_host = q.cpu().pin_memory()
+    lens_host = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).pin_memory()
+    bt_host = torch.from_numpy(np.ascontiguousarray(w.block_table)).pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = (q_host.numel() * 2 + lens_host.numel() * 4 + bt_host.numel() * 4 + step.work_host.numel() * 4 +
+           step.nsplit_host.numel() * 4)
+    d2h = out_host.numel() * 2
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        step.plan(w.seq_lens, w.num_seqs, stream)
+        q.copy_(q_host, non_blocking=True)
+        kv.seq_lens.copy_(lens_host, non_blocking=True)
+        kv.block_table.copy_(bt_host, non_blocking=True)
+        device_step()
+        out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    # plan host time alone
+    t0 = time.perf_counter()
+    for _ in range(50):
+        step.plan(w.seq_lens, w.num_seqs, stream)
+    plan_us = (time.perf_counter() - t0) / 50 * 1e6
+    torch.cuda.synchronize(dev)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    ms_per_step = elapsed_ms / args.steps
+    value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    dec_avg_ms = sum(decode_ms) / len(decode_ms)
+    achieved = kv_bytes / (dec_avg_ms * 1e-3) / 1e9
+    kernel_file = "decode_tc.cu" if impl == 2 or (impl == 0 and os.path.exists(
+        os.path.join(ROOT, "paged_fp8_decode_gb300", "csrc", "decode_tc.cu"))) else "decode_simt.cu"
+    traffic = _traffic(kernel_file, args.workload)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/f32", "data": "synthetic",
+        "config": {
+            "workload": args.workload, "num_seqs": w.num_seqs, "q_len": w.q_len, "h_q": w.h_q, "h_k": w.h_k,
+            "d": w.d, "page_size": w.page_size, "seq_len_total": int(w.seq_lens.sum()), "layout": w.layout,
+            "kv_format": w.kv_format, "causal": w.causal, "parallelism": f"replicas{world}",
+            "l2": f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step vs 129 MB L2, no flush",
+            "ctas_per_sm": cps, "max_splits": msplit, "kv_stages": stages, "variant": args.variant,
+            "with_reduction": info["with_reduction"], "chunk_tiles": info["chunk_tiles"],
+            "num_work": info["num_work"],
+        },
+        "kv_bytes_per_step": kv_bytes,
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        f"pct_of_{peak_kind}_hbm": round(100 * value / world / peak, 2),
+        "tokens_per_s": round(tokens * world / (ms_per_step * 1e-3), 1),
+        "plan_host_us": round(plan_us, 2),
+        "clocks": clocks,
+        "e2e": {"value": round(kv_bytes * world / (e2e_s / e2e_steps) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": f"of {peak_kind}", "kernel": kernel_file.replace(".cu", ""),
+                     "decode_us": round(dec_avg_ms * 1e3, 3)},
+        "cpu_baseline": cpu_base,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_decode")
+    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--ctas-per-sm", type=int, default=0)
+    ap.add_argument("--max-splits", type=int, default=0)
+    ap.add_argument("--kv-stages", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", default=None)
+    ap.add_argument("--budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.cpu_baseline_child:
+        cpu_baseline_child(args.cpu_baseline_child, args.budget)
+        return
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    main_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,266 @@
+/*
+ * mj.h — C ABI of libmj: paged decode attention over an e4m3 or packed e2m3
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * One decode step is four calls, in the order the mjolnir-kernel README
+ * lists them ("A decode step", items 1-4):
+ *
+ *   mj_plan_split_kv    (host)   occupancy-pinned split-KV work list
+ *   mj_quantize_q       (device) dynamic per-(request, KV head) e4m3 Q
+ *   mj_decode_attention (device) stream KV pages through the block table,
+ *                                online softmax, P.V
+ *   mj_merge_lse        (device) merge split-KV partials by log-sum-exp
+ *
+ * Conventions (all calls):
+ *  - Every call returns an mj_status; 0 is success, negative is an error.
+ *    Nothing throws, aborts or prints.
+ *  - No call allocates device or host memory and no call synchronises the
+ *    device. All memory is the caller's: device tensors, the plan staging
+ *    buffers, and a device workspace of mj_workspace_size() bytes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *    Device calls only enqueue work on it; argument errors are detected on
+ *    the host before anything is enqueued.
+ *  - Device pointers must be 16-byte aligned ("T5 kernel needs 16-byte
+ *    aligned base pointers", _ptr on the mjolnir/runner.py page); packed e2m3
+ *    K/V bases must be 32-byte aligned (T5DecodeRunner._kv_ptr).
+ *  - Q and O strides are in ELEMENTS; K/V strides are in BYTES, so e4m3 and
+ *    packed e2m3 caches share one convention.
+ *  - Launch shapes depend only on the arguments (the grid is the plan's
+ *    padded num_work), never on device data, so a step can be captured in a
+ *    CUDA graph and replayed with new plans written into the same buffers
+ *    (runner page, module docstring: "FIXED-ADDRESS device buffers ...
+ *    padded to a FIXED grid size per q_len -> CUDA-graph safe").
+ */
+#ifndef MJ_H
+#define MJ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MJ_API __attribute__((visibility("default")))
+#else
+#define MJ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mj_status {
+  MJ_OK = 0,
+  MJ_ERR_INVALID_ARG = -1,  /* null pointer, negative or inconsistent size */
+  MJ_ERR_UNSUPPORTED = -2,  /* valid but not implemented (head size, page size, format) */
+  MJ_ERR_ALIGNMENT = -3,    /* pointer or stride alignment rule broken */
+  MJ_ERR_CAPACITY = -4,     /* a caller buffer (pad_to, workspace) is too small */
+  MJ_ERR_CUDA = -5,         /* a CUDA runtime call failed (launch, symbol lookup) */
+  MJ_ERR_DEVICE_CHECK = -6  /* a kernel recorded an anomaly in the workspace status word */
+} mj_status;
+
+typedef enum mj_kv_format {
+  MJ_KV_E4M3 = 0,  /* one e4m3 code per byte; row = d bytes */
+  MJ_KV_E2M3 = 1   /* packed e2m3: 4 codes per 3 bytes, little-endian bitstream; row = d*3/4 bytes */
+} mj_kv_format;
+
+/* Kernel variant of mj_decode_attention. AUTO picks the tensor-core kernel
+ * whenever its preconditions hold, else the CUDA-core kernel. */
+typedef enum mj_impl { MJ_IMPL_AUTO = 0, MJ_IMPL_SIMT = 1, MJ_IMPL_TCGEN05 = 2 } mj_impl;
+
+#define MJ_KV_TILE 128 /* tokens per KV tile: the plan's unit ("128-row KV tiles") */
+
+/* Human-readable name of a status code (static storage). */
+MJ_API const char* mj_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+MJ_API int mj_version(void);
+
+/* ------------------------------------------------------------------------
+ * mj_tile_width / mj_slots — the plan's occupancy arithmetic.
+ * Source: tile_width() and T5DecodeRunner.n_tiles/.slots on the runner page.
+ *   tile_width = next power of two >= n_q, at least 16, at most 32 (fp8 Q);
+ *   n_tiles    = ceil(n_q / tile_width);
+ *   slots      = max(1, sm_count*ctas_per_sm // (h_k*n_tiles)).
+ * ---------------------------------------------------------------------- */
+MJ_API int mj_tile_width(int n_q);
+MJ_API int mj_slots(int sm_count, int ctas_per_sm, int h_k, int q_len, int h_q);
+
+/* ------------------------------------------------------------------------
+ * mj_plan_split_kv — host-only split-KV plan.
+ * Source: T5DecodeRunner.plan on the runner page (lens = seq_len + margin;
+ * with_reduction = max_splits > 1 && num_seqs < slots, decided by batch SIZE
+ * so that a captured graph stays valid), README "A decode step" item 1 (one
+ * wave of ctas_per_sm CTAs per SM). The body of plan_split_kv is not on the
+ * pages; this implements the reading:
+ *   t_b = ceil((seq_lens[b] + margin) / 128)
+ *   no reduction:  one row (b, 0, t_b, 0) per request; chunk_tiles = max(1, max t_b)
+ *   reduction:     chunk_tiles = smallest c >= 1 with
+ *                  sum_b max(1, ceil(t_b/c)) <= slots and max_b ceil(t_b/c) <= max_splits;
+ *                  rows (b, s*c, min((s+1)*c, t_b), s) for s < n_splits[b] = max(1, ceil(t_b/c)),
+ *                  request-major
+ *   padding rows (0, 0, 0, 0) up to pad_to (an empty row: end <= begin).
+ *
+ * seq_lens_host  [num_seqs] host int32 (exact lengths or an upper bound: the
+ *                kernel masks with the exact device lengths).
+ * pad_to         number of work rows = the decode grid's x extent; must be
+ *                >= max(slots, num_seqs) (T5DecodeRunner.__init__: grid.x is
+ *                max(slots, max_num_seqs)), else MJ_ERR_CAPACITY.
+ * work_host      [pad_to][4] host int32, written: (request, tile_begin,
+ *                tile_end, split).
+ * n_splits_host  [num_seqs] host int32, written.
+ * chunk_tiles, with_reduction, slots: written scalars (any may be NULL).
+ * Deterministic and bit-identical to the CPU oracle's plan.
+ * ---------------------------------------------------------------------- */
+MJ_API int mj_plan_split_kv(const int32_t* seq_lens_host, int num_seqs, int q_len, int h_q, int h_k,
+                     int sm_count, int ctas_per_sm, int max_splits, int margin, int pad_to,
+                     int32_t* work_host, int32_t* n_splits_host, int* chunk_tiles,
+                     int* with_reduction, int* slots);
+
+/* ------------------------------------------------------------------------
+ * mj_quantize_q — dynamic per-(request, KV head) e4m3 quantization of Q.
+ * Source: T5DecodeRunner.run, fp8-Q branch of the "Q" block (runner page):
+ *   x      = float(q) [* q_mul]                      (float32)
+ *   amax   = max |x| over (token, GQA head, channel) of (b, g), clamped >= 1e-6f
+ *   scale  = amax / 448                              (float32 IEEE division)
+ *   code   = e4m3_rne(x / scale)                     (float32 IEEE division)
+ *   q_descale[b*h_k + g] = scale
+ * Bit-exact with the CPU oracle.
+ *
+ * q          device bf16, element (b*q_len + t, h, c) at
+ *            q[(b*q_len+t)*q_tok_stride + h*q_head_stride + c]; channel stride 1.
+ * q_mul      nullable device float32 [h_q][d] (e2m3 KV: K channel scales).
+ * q_codes    device uint8 [num_seqs][h_k][q_len*h_r][d], row t*h_r + r
+ *            (h_r = h_q/h_k), written.
+ * q_descale  device float32 [num_seqs][h_k], written.
+ * d must be 128. Padding requests are quantized too (harmless: the decode
+ * call never reads them).
+ * ---------------------------------------------------------------------- */
+MJ_API int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, int num_seqs,
+                  int q_len, int h_q, int h_k, int d, const float* q_mul, uint8_t* q_codes,
+                  float* q_descale, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mj_decode_args — everything one decode launch reads and writes.
+ * Mirrors the kernel argument list of T5DecodeRunner._launch (runner page):
+ * problem shape, block-table row stride, num_pages, num_work, strides, the
+ * Q/K/V/block_table/seq_lens/work/n_splits/descale/O/LSE/partial pointers and
+ * the softmax scale.
+ * ---------------------------------------------------------------------- */
+typedef struct mj_decode_args {
+  /* problem shape */
+  int num_seqs;   /* requests in the batch (real + trailing padding) */
+  int q_len;      /* query tokens per request (1 = decode; 1+k = speculative verify) */
+  int h_q, h_k;   /* query heads, KV heads; h_q % h_k == 0 */
+  int d;          /* head size; 128 */
+  int causal;     /* 1: query t sees key j iff j <= seq_len - q_len + t;
+                     0: every query token sees every key (README "What it does") */
+  float softmax_scale;
+
+  /* quantized Q (mj_quantize_q outputs) */
+  const uint8_t* q_codes;  /* [num_seqs][h_k][q_len*h_r][d] */
+  const float* q_descale;  /* [num_seqs][h_k] */
+
+  /* paged KV cache: logical (num_pages, page_size, h_k, row) with byte strides */
+  int kv_format;           /* mj_kv_format */
+  int page_size;           /* tokens per page: 16, 32, 64 or 128 */
+  int64_t num_pages;       /* pages in the pool (page ids must be < num_pages) */
+  const void* k_cache;
+  const void* v_cache;
+  int64_t k_stride_page, k_stride_token, k_stride_head;  /* bytes, multiples of 16 */
+  int64_t v_stride_page, v_stride_token, v_stride_head;  /* bytes, multiples of 16 */
+  /* K/V descales, float32; element (b, g) at ptr[b*seq_stride + g*head_stride]:
+     (0,0) per tensor, (0,1) per KV head, (h_k,1) per (request, KV head).
+     Packed e2m3 KV: the channel scales are folded into q_mul / o_mul and
+     these are 1 (_install_fp6_scales, mjolnir/backend.py page). */
+  const float* k_descale;
+  const float* v_descale;
+  int64_t descale_seq_stride, descale_head_stride;
+
+  /* paging */
+  const int32_t* block_table;   /* device; page of token j of request b:
+                                   block_table[b*block_table_stride + j/page_size] */
+  int64_t block_table_stride;
+  const int32_t* seq_lens;      /* device [num_seqs]; exact lengths used for masking.
+                                   0 = padding request: nothing is written for it. */
+
+  /* plan (mj_plan_split_kv outputs, copied to device) */
+  const int32_t* work;          /* device [num_work][4] */
+  const int32_t* n_splits;      /* device [num_seqs] */
+  int num_work;                 /* = pad_to: the grid's x extent */
+  int with_reduction;           /* 1: split partials go to the workspace; call mj_merge_lse */
+  int chunk_tiles;              /* tiles per split (plan output) */
+  int max_splits;               /* the plan's max_splits (partials indexing) */
+  int part_seqs;                /* requests the partial area is sized for (>= num_seqs
+                                   when with_reduction; the plan's slots) */
+
+  /* output */
+  const float* o_mul;           /* nullable device float32 [h_q][d]: O *= o_mul last */
+  void* out;                    /* device bf16; (b*q_len+t, h, c) at
+                                   out[(b*q_len+t)*out_tok_stride + h*out_head_stride + c] */
+  int64_t out_tok_stride, out_head_stride;  /* elements, multiples of 8 */
+  float* lse;                   /* nullable device float32 [num_seqs][h_k][q_len*h_r]:
+                                   natural-log sum of exp(logits) per query row */
+
+  /* caller-owned device workspace (status word + split partials) */
+  void* workspace;
+  size_t workspace_bytes;
+
+  /* tuning knobs (0 = library default) */
+  int impl;          /* mj_impl */
+  int kv_stages;     /* KV ring depth of the tensor-core kernel */
+  int evict_first;   /* 1 = L2 evict-first hint on KV loads (KV is read once) */
+} mj_decode_args;
+
+/* ------------------------------------------------------------------------
+ * mj_workspace_size — bytes of device workspace a decode step needs.
+ * Partials are sized by part_seqs (the plan's slots), not by the batch: the
+ * plan only splits when num_seqs < slots (comment above the partial buffers
+ * in T5DecodeRunner.__init__). Layout: a 256-byte header holding the device
+ * status word, then o_part f32 [part_seqs*max_splits*h_k*n_q_max][d],
+ * m_part f32 [..], l_part f32 [..] (n_q_max = max_q_len*h_q/h_k).
+ * ---------------------------------------------------------------------- */
+MJ_API int mj_workspace_size(int part_seqs, int max_splits, int max_q_len, int h_q, int h_k, int d,
+                      size_t* bytes);
+
+/* Zero the workspace status word (enqueued on `stream`). Call once after
+ * allocating the workspace. */
+MJ_API int mj_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Read and clear the workspace status word. SYNCHRONISES `stream` (a test and
+ * debugging aid, not for the hot path). *device_status = 0 means no kernel
+ * recorded an anomaly; otherwise a bit mask (1: page id out of range,
+ * 2: a bounded wait timed out, 4: a work row outside the partial area). Returns MJ_ERR_DEVICE_CHECK when non-zero. */
+MJ_API int mj_workspace_status(void* workspace, void* stream, uint32_t* device_status);
+
+/* ------------------------------------------------------------------------
+ * mj_decode_attention — paged decode attention over the plan's work rows.
+ * Source: README "A decode step" item 3 (stream KV pages into a shared-memory
+ * ring, tensor-core S and O, online softmax), T5DecodeRunner._launch/run.
+ * Reads each valid KV row once. For a work row (b, tb, te, s) and KV head g
+ * it covers keys [tb*128, min(te*128, seq_lens[b])) and all q_len*h_r query
+ * rows of (b, g):
+ *   - if !with_reduction or n_splits[b] == 1: writes the final bf16 output
+ *     O * v_descale * o_mul and, if lse != NULL, the row LSE;
+ *   - else writes its normalised partial (O~, m, l) into the workspace.
+ * Rows of requests with seq_lens[b] == 0 and empty work rows write nothing.
+ * Grid: num_work x h_k x n_row_tiles, fixed by the arguments.
+ * ---------------------------------------------------------------------- */
+MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mj_merge_lse — combine split-KV partials by log-sum-exp.
+ * Source: README "A decode step" item 4 ("a small second kernel combines the
+ * split-KV partials by LSE"). For each request b with n_splits[b] > 1 and
+ * seq_lens[b] > 0, KV head g and query row:
+ *   M = max_s m_s;  w_s = 2^(m_s - M) * l_s (0 for empty splits);
+ *   O = sum_s w_s O~_s / sum_s w_s, times v_descale and o_mul, rounded to bf16.
+ * Splits whose first key is at or past seq_lens[b] are empty and skipped.
+ * A no-op when args->with_reduction == 0. Same argument struct as
+ * mj_decode_attention (it reads the partials that call left in the workspace).
+ * ---------------------------------------------------------------------- */
+MJ_API int mj_merge_lse(const mj_decode_args* args, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MJ_H */

@@ -1,0 +1,279 @@
+// CUDA-core variant of mj_decode_attention.
+//
+// One CTA (4 warps) per (work row, KV head, query-row tile). Each warp walks
+// 32-key blocks of the work row's key range; lane j owns key j of the block
+// for S = Q.K^T (the whole K row through 16-byte loads) and channels
+// 4*lane .. 4*lane+3 for O += P.V (coalesced 128-byte V reads per key). The
+// online softmax runs per warp in the log2 domain; the four warps' (m, l, O)
+// are merged in shared memory at the end. Keys at or past the request's
+// device seq_len are never read, so stale or poisoned page tails cannot leak
+// into the result.
+//
+// This is the generic path: any row tile up to 32, any strides, e4m3 or
+// packed e2m3. The tensor-core kernel is the fast path.
+#include "mj_device.cuh"
+#include "mj_internal.h"
+
+namespace mj {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+
+// Codes 16*i .. 16*i+15 of one K row as floats (e4m3: bytes 16i..16i+15;
+// e2m3: packed bytes 12i..12i+11 widened to e4m3, value x 2^-6).
+__device__ __forceinline__ void load_k16(const uint8_t* row, int kv_format, int i, float k[16]) {
+  if (kv_format == MJ_KV_E4M3) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + i);
+    e4m3x4_to_float(v.x, k + 0);
+    e4m3x4_to_float(v.y, k + 4);
+    e4m3x4_to_float(v.z, k + 8);
+    e4m3x4_to_float(v.w, k + 12);
+  } else {
+    const uint32_t* r32 = reinterpret_cast<const uint32_t*>(row) + 3 * i;
+    const uint32_t w0 = __ldg(r32), w1 = __ldg(r32 + 1), w2 = __ldg(r32 + 2);
+    const uint32_t g0 = w0 & 0xFFFFFFu;
+    const uint32_t g1 = __funnelshift_r(w0, w1, 24) & 0xFFFFFFu;
+    const uint32_t g2 = __funnelshift_r(w1, w2, 16) & 0xFFFFFFu;
+    const uint32_t g3 = w2 >> 8;
+    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g0)), k + 0);
+    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g1)), k + 4);
+    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g2)), k + 8);
+    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g3)), k + 12);
+  }
+}
+
+// Channels 4*lane .. 4*lane+3 of one V row.
+__device__ __forceinline__ void load_v4(const uint8_t* row, int kv_format, int lane, float v[4]) {
+  if (kv_format == MJ_KV_E4M3) {
+    e4m3x4_to_float(__ldg(reinterpret_cast<const uint32_t*>(row) + lane), v);
+  } else {
+    const uint8_t* p = row + 3 * lane;
+    const uint32_t g = uint32_t(__ldg(p)) | (uint32_t(__ldg(p + 1)) << 8) | (uint32_t(__ldg(p + 2)) << 16);
+    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g)), v);
+  }
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
+  __shared__ __align__(16) float qs[NR][kHeadDim];  // Q rows, later the O accumulator
+  __shared__ float ps[kWarps][32][NR];              // P of each warp's 32-key block
+  __shared__ float red_m[kWarps][NR], red_l[kWarps][NR];
+  __shared__ int page_of[kWarps][32];
+
+  const int g = blockIdx.y;
+  const int4 w = reinterpret_cast<const int4*>(p.work)[blockIdx.x];
+  const int b = w.x;
+  if (w.z <= w.y || b < 0 || b >= p.num_seqs) return;
+  if (p.with_reduction && (w.w < 0 || w.w >= p.max_splits || b >= p.part_seqs)) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPlan);
+    return;
+  }
+  const int L = p.seq_lens[b];
+  if (L <= 0) return;
+  const int64_t k0 = int64_t(w.y) * kKvTile;
+  const int64_t k1 = min(int64_t(w.z) * kKvTile, int64_t(L));
+  if (k1 <= k0) return;
+  const int r0 = blockIdx.z * p.tw;
+  const int nr = min(p.tw, p.n_q - r0);
+  if (nr <= 0) return;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Q codes of this row tile -> shared floats (rows >= nr are zero).
+  const uint8_t* qrow = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
+  for (int i = tid; i < NR * kHeadDim / 4; i += kThreads) {
+    const int row = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (row < nr) e4m3x4_to_float(reinterpret_cast<const uint32_t*>(qrow + row * kHeadDim)[c4], v);
+    *reinterpret_cast<float4*>(&qs[row][4 * c4]) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  __syncthreads();
+
+  const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
+  const float scale = p.q_descale[int64_t(b) * p.h_k + g] * kd * p.qk_scale_log2;
+  const int64_t causal_base = int64_t(L) - p.q_len;  // query t sees key j iff j <= L - q_len + t
+
+  float m[NR], l[NR], o[NR][4];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+    o[r][0] = o[r][1] = o[r][2] = o[r][3] = 0.f;
+  }
+
+  const int64_t kbase_head = int64_t(g) * p.k_sh;
+  const int64_t vbase_head = int64_t(g) * p.v_sh;
+  const int32_t* bt = p.block_table + int64_t(b) * p.bt_stride;
+
+  for (int64_t kb = k0 + int64_t(warp) * 32; kb < k1; kb += kWarps * 32) {
+    const int64_t key = kb + lane;
+    const bool valid = key < k1;
+    int page = 0;
+    bool page_ok = false;
+    if (valid) {
+      page = bt[key / p.page_size];
+      page_ok = page >= 0 && int64_t(page) < p.num_pages;
+      if (!page_ok) atomicOr(p.status, kStatusBadPage);
+    }
+    page_of[warp][lane] = page_ok ? page : -1;
+
+    float t[NR];
+    if (page_ok) {
+      const int slot = int(key % p.page_size);
+      const uint8_t* krow = p.k_cache + int64_t(page) * p.k_sp + int64_t(slot) * p.k_st + kbase_head;
+      float acc[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) acc[r] = 0.f;
+#pragma unroll 1
+      for (int i = 0; i < kHeadDim / 16; ++i) {
+        float kf[16];
+        load_k16(krow, p.kv_format, i, kf);
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            const float4 q4 = *reinterpret_cast<const float4*>(&qs[r][16 * i + c]);
+            acc[r] = fmaf(q4.x, kf[c], acc[r]);
+            acc[r] = fmaf(q4.y, kf[c + 1], acc[r]);
+            acc[r] = fmaf(q4.z, kf[c + 2], acc[r]);
+            acc[r] = fmaf(q4.w, kf[c + 3], acc[r]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const int tq = (r0 + r) / p.h_r;
+        const bool vis = r < nr && (!p.causal || key <= causal_base + tq);
+        t[r] = vis ? acc[r] * scale : -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) t[r] = -INFINITY;
+    }
+
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const float mx = warp_max(t[r]);
+      const float m_new = fmaxf(m[r], mx);
+      float alpha, pr;
+      if (m_new == -INFINITY) {
+        alpha = 1.f;
+        pr = 0.f;
+      } else {
+        alpha = fast_exp2(m[r] - m_new);
+        pr = fast_exp2(t[r] - m_new);
+      }
+      m[r] = m_new;
+      l[r] = l[r] * alpha + pr;
+      o[r][0] *= alpha;
+      o[r][1] *= alpha;
+      o[r][2] *= alpha;
+      o[r][3] *= alpha;
+      ps[warp][lane][r] = pr;
+    }
+    __syncwarp();
+
+    const int nkeys = int(min(int64_t(32), k1 - kb));
+    for (int kk = 0; kk < nkeys; ++kk) {
+      const int pg = page_of[warp][kk];
+      if (pg < 0) continue;
+      const int slot = int((kb + kk) % p.page_size);
+      const uint8_t* vrow = p.v_cache + int64_t(pg) * p.v_sp + int64_t(slot) * p.v_st + vbase_head;
+      float v[4];
+      load_v4(vrow, p.kv_format, lane, v);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const float pr = ps[warp][kk][r];
+        o[r][0] = fmaf(pr, v[0], o[r][0]);
+        o[r][1] = fmaf(pr, v[1], o[r][1]);
+        o[r][2] = fmaf(pr, v[2], o[r][2]);
+        o[r][3] = fmaf(pr, v[3], o[r][3]);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- merge the four warps ------------------------------------------------
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    const float ls = warp_sum(l[r]);
+    if (lane == 0) {
+      red_m[warp][r] = m[r];
+      red_l[warp][r] = ls;
+    }
+  }
+  __syncthreads();  // also: every warp is done reading qs
+
+  float f[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float M = red_m[0][r];
+#pragma unroll
+    for (int w2 = 1; w2 < kWarps; ++w2) M = fmaxf(M, red_m[w2][r]);
+    f[r] = (m[r] == -INFINITY) ? 0.f : fast_exp2(m[r] - M);
+  }
+  for (int w2 = 0; w2 < kWarps; ++w2) {
+    if (warp == w2) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float4* dst = reinterpret_cast<float4*>(&qs[r][4 * lane]);
+        float4 cur = (w2 == 0) ? make_float4(0.f, 0.f, 0.f, 0.f) : *dst;
+        cur.x = fmaf(o[r][0], f[r], cur.x);
+        cur.y = fmaf(o[r][1], f[r], cur.y);
+        cur.z = fmaf(o[r][2], f[r], cur.z);
+        cur.w = fmaf(o[r][3], f[r], cur.w);
+        *dst = cur;
+      }
+    }
+    __syncthreads();
+  }
+
+  const bool direct = !p.with_reduction || p.n_splits[b] <= 1;
+  const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
+  const int c = tid;  // 128 threads = 128 channels
+  for (int r = 0; r < nr; ++r) {
+    float M = red_m[0][r];
+    for (int w2 = 1; w2 < kWarps; ++w2) M = fmaxf(M, red_m[w2][r]);
+    float Lt = 0.f;
+    if (M != -INFINITY)
+      for (int w2 = 0; w2 < kWarps; ++w2)
+        if (red_m[w2][r] != -INFINITY) Lt += red_l[w2][r] * fast_exp2(red_m[w2][r] - M);
+    const float on = Lt > 0.f ? qs[r][c] / Lt : 0.f;
+    const int row = r0 + r;
+    if (direct) {
+      const int tq = row / p.h_r, rr = row % p.h_r, h = g * p.h_r + rr;
+      float val = on * vd;
+      if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + c];
+      p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_bf16_bits(val);
+      if (p.lse && c == 0)
+        p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] = Lt > 0.f ? (M + fast_log2(Lt)) * kLn2 : -INFINITY;
+    } else {
+      const int64_t idx = part_index(p, b, w.w, g, row);
+      p.o_part[idx * kHeadDim + c] = on;
+      if (c == 0) {
+        p.m_part[idx] = Lt > 0.f ? M : -INFINITY;
+        p.l_part[idx] = Lt;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
+  if (p.num_work == 0) return cudaSuccess;
+  dim3 grid(p.num_work, p.h_k, p.n_row_tiles);
+  if (p.tw <= 4)
+    decode_simt_kernel<4><<<grid, kThreads, 0, stream>>>(p);
+  else if (p.tw <= 8)
+    decode_simt_kernel<8><<<grid, kThreads, 0, stream>>>(p);
+  else if (p.tw <= 16)
+    decode_simt_kernel<16><<<grid, kThreads, 0, stream>>>(p);
+  else
+    decode_simt_kernel<32><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mj

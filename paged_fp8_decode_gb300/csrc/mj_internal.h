@@ -1,0 +1,91 @@
+// Internal definitions shared by the host ABI layer (mj_api.cpp) and the
+// kernels. Not part of the public ABI: see include/mj.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mj.h"
+
+namespace mj {
+
+constexpr int kKvTile = 128;   // tokens per KV tile (the plan's unit)
+constexpr int kHeadDim = 128;  // supported head size
+constexpr int kMaxRowTile = 32;
+
+// Workspace layout: a 256-byte header (status word at offset 0), then the
+// split partials o_part [rows][d], m_part [rows], l_part [rows].
+constexpr size_t kWsHeader = 256;
+
+// Status bits a kernel may OR into the workspace status word.
+constexpr uint32_t kStatusBadPage = 1u;
+constexpr uint32_t kStatusTimeout = 2u;
+constexpr uint32_t kStatusBadPlan = 4u;
+
+// Everything a decode / merge launch needs, by value (kernel parameter).
+struct DecodeParams {
+  int num_seqs, q_len, h_q, h_k, h_r, n_q, d;
+  int causal;
+  int kv_format, page_size, row_bytes;
+  int64_t num_pages;
+  int tw, n_row_tiles;  // query rows per CTA, row tiles per (request, head)
+
+  const uint8_t* q_codes;
+  const float* q_descale;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  int64_t k_sp, k_st, k_sh, v_sp, v_st, v_sh;  // byte strides (page, token, head)
+  const float* k_descale;
+  const float* v_descale;
+  int64_t ds_seq, ds_head;
+
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+
+  const int32_t* work;
+  const int32_t* n_splits;
+  int num_work, with_reduction, chunk_tiles, max_splits, part_seqs;
+
+  // logits in the log2 domain: t = (q_code . k_code) * q_descale * k_descale * qk_scale_log2
+  float qk_scale_log2;  // softmax_scale * log2(e) * (format factor of K)
+  float v_fmt;          // format factor of V (64 for widened e2m3, else 1)
+
+  const float* o_mul;
+  uint16_t* out;  // bf16 bits
+  int64_t out_ts, out_hs;
+  float* lse;
+
+  uint32_t* status;
+  float* o_part;
+  float* m_part;
+  float* l_part;
+
+  int kv_stages;
+  int evict_first;
+};
+
+// Index of a partial row: ((b*max_splits + s)*h_k + g)*n_q + row.
+__host__ __device__ inline int64_t part_index(const DecodeParams& p, int b, int s, int g, int row) {
+  return ((int64_t(b) * p.max_splits + s) * p.h_k + g) * p.n_q + row;
+}
+
+__host__ __device__ inline float kv_descale(const float* ds, int64_t seq_stride, int64_t head_stride,
+                                            int b, int g) {
+  return ds[int64_t(b) * seq_stride + int64_t(g) * head_stride];
+}
+
+struct QuantParams {
+  const uint16_t* q;
+  int64_t q_ts, q_hs;
+  int num_seqs, q_len, h_q, h_k, h_r, n_q, d;
+  const float* q_mul;
+  uint8_t* codes;
+  float* descale;
+};
+
+cudaError_t launch_quantize_q(const QuantParams& p, cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace mj

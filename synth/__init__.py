@@ -90,6 +90,10 @@ class Workload:
 # ----------------------------------------------------------------------------
 # synthetic cache writer
 # ----------------------------------------------------------------------------
+def _absmax(x: np.ndarray) -> float:
+    return max(float(x.max()), -float(x.min())) if x.size else 0.0
+
+
 def _e4m3_codes(x: np.ndarray) -> np.ndarray:
     import torch
 
@@ -97,27 +101,22 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
     return t.view(torch.uint8).numpy()
 
 
-def _e2m3_grid():
-    """The 32 non-negative e2m3 magnitudes in code order (codes 0..31)."""
-    vals = []
-    for code in range(32):
-        e, m = code >> 3, code & 7
-        vals.append(m / 8.0 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 1))
-    return np.array(vals)
-
-
-_E2M3_GRID = _e2m3_grid()
-
-
 def _e2m3_codes(x: np.ndarray) -> np.ndarray:
-    a = np.abs(x.astype(np.float64))
-    i = np.clip(np.searchsorted(_E2M3_GRID, a, side="right") - 1, 0, 31)
-    j = np.minimum(i + 1, 31)
-    lo, hi = _E2M3_GRID[i], _E2M3_GRID[j]
-    up = (2 * a > lo + hi) | ((2 * a == lo + hi) & (i % 2 == 1))
-    c = np.where(up, j, i)
-    c = np.where(a >= 7.5, 31, c)
-    return (c | np.where(np.signbit(x), 0x20, 0)).astype(np.uint8)
+    """Nearest e2m3 code (ties to even) of float32 values with |x| <= 7.5.
+
+    In [1, 7.5] e2m3 and e4m3 both carry 3 mantissa bits with normal
+    exponents, so torch's e4m3 conversion rounds identically there and the
+    e2m3 code is the e4m3 code with the exponent rebased (bias 7 -> bias 1).
+    Below 1, e2m3 is the subnormal grid k/8 and the code is rint(8|x|)
+    (ties to the even k, i.e. the even code)."""
+    a = np.abs(x.astype(np.float32, copy=False))
+    big = a >= 1.0
+    c8 = _e4m3_codes(np.minimum(a, np.float32(7.5)))
+    e4 = (c8 >> 3).astype(np.int16)
+    hi = ((e4 - 6) << 3) | (c8 & 7)
+    lo = np.rint(a * np.float32(8.0)).astype(np.int16)
+    code = np.where(big, np.minimum(hi, 31), lo).astype(np.uint8)
+    return code | np.where(np.signbit(x), np.uint8(0x20), np.uint8(0))
 
 
 def pack_e2m3(codes: np.ndarray) -> np.ndarray:
@@ -187,46 +186,60 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
     else:
         poison_row = pack_e2m3(np.full(d, E2M3_POISON, dtype=np.uint8))
 
+    # flat row index of (page, head g, slot) in the physical buffer
+    def flat_rows(g):
+        if layout == "HND":
+            return (tok_pages.astype(np.int64) * h_k + g) * page_size + tok_slots
+        return (tok_pages.astype(np.int64) * page_size + tok_slots) * h_k + g
+
     meta = {}
     caches, scales, chans = {}, {}, {}
     for which, stream, ostream in (("k", _S_K, _S_OUTLIER_K), ("v", _S_V, _S_OUTLIER_V)):
         buf = np.empty(shape, dtype=np.uint8)
         buf[...] = poison_row
+        rows = buf.reshape(-1, row_bytes)
         rng = _rng(seed, stream)
         orng = _rng(seed, ostream)
         per_head_scale = np.zeros(h_k, dtype=np.float32)
         ch_scale = np.zeros((h_k, d), dtype=np.float32)
-        tensor_scale = np.float32(1.0)
-        xs = []
-        for g in range(h_k):
-            x = rng.standard_normal((n_tok, d), dtype=np.float32)
+
+        xbuf = np.empty((n_tok, d), dtype=np.float32)
+
+        def draw(out=None):
+            x = rng.standard_normal((n_tok, d), dtype=np.float32, out=xbuf if out is None else out)
             if outlier_channels:
                 ch = orng.choice(d, size=outlier_channels, replace=False)
                 x[:, ch] *= np.float32(outlier_gain)
                 meta.setdefault(f"{which}_outlier_channels", []).append(sorted(int(c) for c in ch))
-            xs.append(x)
+            return x
+
+        tensor_scale = np.float32(1.0)
+        xs = None
         if kv_format == "fp8" and scale_mode == "tensor":
-            amax = max([float(np.abs(x).max()) if x.size else 0.0 for x in xs] + [1e-30])
+            xs = [draw(np.empty((n_tok, d), dtype=np.float32)) for _ in range(h_k)]
+            amax = max([_absmax(x) for x in xs] + [1e-30])
             tensor_scale = np.float32(amax / 448.0)
         for g in range(h_k):
-            x = xs[g]
+            x = xs[g] if xs is not None else draw()
             if kv_format == "fp8":
                 if scale_mode == "tensor":
-                    s = tensor_scale
+                    s_ = tensor_scale
                 else:
-                    s = np.float32((float(np.abs(x).max()) if x.size else 1.0) / 448.0)
-                    per_head_scale[g] = s
-                codes = _e4m3_codes(x / s)
+                    s_ = np.float32((_absmax(x) if x.size else 1.0) / 448.0)
+                    per_head_scale[g] = s_
+                np.divide(x, s_, out=x)
+                codes = _e4m3_codes(x)
             else:
-                s_c = (np.abs(x).max(axis=0) if x.size else np.ones(d)).astype(np.float32) / np.float32(7.5)
-                s_c = np.maximum(s_c, np.float32(1e-30))
+                s_c = (np.maximum(x.max(axis=0), -x.min(axis=0)) if x.size
+                       else np.ones(d, np.float32)).astype(np.float32)
+                s_c = np.maximum(s_c / np.float32(7.5), np.float32(1e-30))
                 ch_scale[g] = s_c
-                codes = pack_e2m3(_e2m3_codes(x / s_c[None, :]))
-            if layout == "HND":
-                buf[tok_pages, g, tok_slots, :] = codes
-            else:
-                buf[tok_pages, tok_slots, g, :] = codes
-            xs[g] = None
+                np.divide(x, s_c[None, :], out=x)
+                codes = pack_e2m3(_e2m3_codes(x))
+            rows[flat_rows(g)] = codes
+            if xs is not None:
+                xs[g] = None
+            del x, codes
         caches[which] = buf
         if kv_format == "fp8":
             scales[which] = (np.array([tensor_scale], dtype=np.float32) if scale_mode == "tensor"

@@ -1,0 +1,160 @@
+"""The C ABI on the host: the library loads, exports every declared symbol,
+validates arguments before touching the device, and plans bit-identically
+to the oracle. No GPU is needed (no call here reaches a kernel launch)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_fp8_decode_gb300 as mj
+from oracle import plan as OP
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_fp8_decode_gb300.build import build
+
+    build()
+    return mj.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mj.h")).read()
+    return re.findall(r"MJ_API\s+[\w\s\*]+?\b(mj_\w+)\s*\(", src)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11
+    assert set(names) == set(mj.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.mj_status_string(code)
+    assert mj.mj_version() == 100
+
+
+def test_tile_width_and_slots_match_oracle(lib):
+    for n_q in range(1, 80):
+        assert mj.mj_tile_width(n_q) == OP.tile_width(n_q, True)
+    for sm, cps, h_k, ql, h_q in [(152, 2, 8, 1, 32), (152, 4, 8, 4, 32), (20, 2, 8, 1, 32), (152, 2, 8, 1, 64),
+                                  (152, 1, 2, 3, 32)]:
+        assert mj.mj_slots(sm, cps, h_k, ql, h_q) == OP.slots(sm, cps, h_k, OP.n_tiles(ql, h_q // h_k))
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_plan_bit_identical_to_oracle(lib, seed):
+    rng = np.random.default_rng(100 + seed)
+    num_seqs = int(rng.integers(0, 40))
+    lens = rng.integers(0, 200000 if seed % 3 == 0 else 5000, size=num_seqs).astype(np.int32)
+    if num_seqs and seed % 4 == 0:
+        lens[-min(3, num_seqs):] = 0
+    h_k = int(rng.choice([1, 2, 4, 8]))
+    h_q = h_k * int(rng.choice([1, 4, 8]))
+    q_len = int(rng.integers(1, 6))
+    sm, cps = int(rng.choice([20, 148, 152])), int(rng.integers(1, 5))
+    max_splits = int(rng.choice([1, 2, 16, 64, 128]))
+    margin = int(rng.integers(0, 5))
+    s = OP.slots(sm, cps, h_k, OP.n_tiles(q_len, h_q // h_k))
+    pad_to = max(s, num_seqs) + int(rng.integers(0, 3))
+    ref = OP.plan_split_kv(lens, num_seqs, q_len, h_q, h_k, sm, cps, max_splits, margin, pad_to)
+    got = mj.mj_plan_split_kv(lens, num_seqs, q_len, h_q, h_k, sm, cps, max_splits, margin, pad_to)
+    assert got["slots"] == ref.slots
+    assert got["with_reduction"] == ref.with_reduction
+    assert got["chunk_tiles"] == ref.chunk_tiles
+    assert np.array_equal(got["work"], np.array(ref.work, dtype=np.int32).reshape(pad_to, 4))
+    assert list(got["n_splits"][:num_seqs]) == ref.n_splits
+
+
+def test_plan_rejects_small_pad_to(lib):
+    with pytest.raises(mj.MjError) as e:
+        mj.mj_plan_split_kv(np.full(10, 100, np.int32), 10, 1, 32, 8, 152, 2, 16, 0, 5)
+    assert e.value.status == mj.MJ_ERR_CAPACITY
+
+
+def _valid_args():
+    """A well-formed argument struct with fake (never dereferenced) 256-byte
+    aligned addresses; each test breaks one thing and expects the host-side
+    check to reject it before any launch."""
+    a = mj.mj_decode_args()
+    base = 1 << 40
+    a.num_seqs, a.q_len, a.h_q, a.h_k, a.d, a.causal, a.softmax_scale = 2, 1, 8, 2, 128, 1, 0.088
+    a.q_codes, a.q_descale = base, base + 0x1000
+    a.kv_format, a.page_size, a.num_pages = 0, 16, 10
+    a.k_cache, a.v_cache = base + 0x10000, base + 0x20000
+    a.k_stride_page, a.k_stride_token, a.k_stride_head = 4096, 128, 2048
+    a.v_stride_page, a.v_stride_token, a.v_stride_head = 4096, 128, 2048
+    a.k_descale, a.v_descale = base + 0x2000, base + 0x2100
+    a.descale_seq_stride, a.descale_head_stride = 0, 0
+    a.block_table, a.block_table_stride, a.seq_lens = base + 0x3000, 8, base + 0x3100
+    a.work, a.n_splits, a.num_work = base + 0x4000, base + 0x4100, 2
+    a.with_reduction, a.chunk_tiles, a.max_splits, a.part_seqs = 0, 1, 16, 2
+    a.out, a.out_tok_stride, a.out_head_stride = base + 0x5000, 1024, 128
+    a.workspace, a.workspace_bytes = base + 0x8000, 256
+    return a
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("d", 64, mj.MJ_ERR_UNSUPPORTED),
+    ("d", 256, mj.MJ_ERR_UNSUPPORTED),
+    ("page_size", 8, mj.MJ_ERR_UNSUPPORTED),
+    ("kv_format", 7, mj.MJ_ERR_UNSUPPORTED),
+    ("h_q", 9, mj.MJ_ERR_INVALID_ARG),
+    ("q_len", 0, mj.MJ_ERR_INVALID_ARG),
+    ("q_codes", None, mj.MJ_ERR_INVALID_ARG),
+    ("block_table", None, mj.MJ_ERR_INVALID_ARG),
+    ("workspace", None, mj.MJ_ERR_INVALID_ARG),
+    ("q_codes", (1 << 40) + 8, mj.MJ_ERR_ALIGNMENT),
+    ("out", (1 << 40) + 0x5002, mj.MJ_ERR_ALIGNMENT),
+    ("k_stride_token", 130, mj.MJ_ERR_ALIGNMENT),
+    ("out_head_stride", 130, mj.MJ_ERR_ALIGNMENT),
+    ("softmax_scale", 0.0, mj.MJ_ERR_INVALID_ARG),
+    ("workspace_bytes", 16, mj.MJ_ERR_CAPACITY),
+    ("impl", 9, mj.MJ_ERR_INVALID_ARG),
+])
+def test_decode_args_rejected_on_host(lib, field, value, status):
+    a = _valid_args()
+    setattr(a, field, value)
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == status
+    assert lib.mj_merge_lse(ctypes.byref(a), None) == status
+
+
+def test_e2m3_needs_32_byte_kv_alignment(lib):
+    a = _valid_args()
+    a.kv_format = 1
+    a.k_cache = (1 << 40) + 0x10010  # 16- but not 32-byte aligned
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_ALIGNMENT
+
+
+def test_reduction_needs_a_large_enough_workspace(lib):
+    a = _valid_args()
+    a.with_reduction = 1
+    need = mj.mj_workspace_size(a.part_seqs, a.max_splits, a.q_len, a.h_q, a.h_k)
+    a.workspace_bytes = need - 4
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_CAPACITY
+    a.part_seqs = 1  # fewer than num_seqs
+    a.workspace_bytes = need
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_INVALID_ARG
+
+
+def test_workspace_size_formula(lib):
+    n = mj.mj_workspace_size(38, 64, 1, 32, 8)
+    assert n == 256 + 38 * 64 * 8 * 4 * (128 + 2) * 4
+
+
+def test_quantize_rejections(lib):
+    f = lib.mj_quantize_q
+    base = 1 << 40
+    assert f(base, 4096, 128, 2, 1, 32, 8, 64, None, base, base, None) == mj.MJ_ERR_UNSUPPORTED
+    assert f(base, 4096, 128, 2, 1, 30, 8, 128, None, base, base, None) == mj.MJ_ERR_INVALID_ARG
+    assert f(None, 4096, 128, 2, 1, 32, 8, 128, None, base, base, None) == mj.MJ_ERR_INVALID_ARG
+    assert f(base + 2, 4096, 128, 2, 1, 32, 8, 128, None, base, base, None) == mj.MJ_ERR_ALIGNMENT
+    assert f(base, 4096, 128, 0, 1, 32, 8, 128, None, None, None, None) == mj.MJ_OK  # empty batch: no-op

@@ -1,0 +1,160 @@
+"""GPU parity: every exported call against the CPU oracle on seeded inputs.
+
+Bit-exact: the quantized Q codes and scales. Within max|err| <= 2e-2 max|V|
+and mean|err| <= 2e-3 max|V|: the bf16 output. Padding requests must stay
+untouched, the device status word must stay clean.
+"""
+
+import numpy as np
+import pytest
+
+import synth
+from tests._harness import SENTINEL, all_units, compare, run_gpu, run_oracle, sample_units
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = [1]  # MJ_IMPL_SIMT; the tensor-core kernel joins when it exists
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_fp8_decode_gb300.build import build
+
+    build()
+
+
+def _case(name):
+    if name == "ragged_hnd":
+        return synth.make_case(name=name, num_seqs=6, q_len=1, h_q=32, h_k=8, page_size=16,
+                               seq_lens=[1, 15, 16, 17, 300, 1000], layout="HND", pool_pages=200, seed=21)
+    if name == "split_nhd":
+        return synth.make_case(name=name, num_seqs=3, q_len=1, h_q=32, h_k=8, page_size=64,
+                               seq_lens=[5000, 9000, 300], layout="NHD", seed=22)
+    if name == "spec_causal":
+        return synth.make_case(name=name, num_seqs=7, q_len=4, h_q=32, h_k=8, page_size=32,
+                               seq_lens=[40, 129, 700, 2000, 3, 0, 0], layout="HND", scale_mode="tensor",
+                               seed=23, causal=True)
+    if name == "spec_noncausal":
+        return synth.make_case(name=name, num_seqs=7, q_len=4, h_q=32, h_k=8, page_size=32,
+                               seq_lens=[40, 129, 700, 2000, 3, 0, 0], layout="HND", scale_mode="tensor",
+                               seed=23, causal=False)
+    if name == "fp6_small":
+        return synth.make_case(name=name, num_seqs=3, q_len=1, h_q=64, h_k=8, page_size=128,
+                               seq_lens=[130, 1000, 257], layout="HND", kv_format="e2m3",
+                               outlier_channels=4, seed=24)
+    if name == "fp6_nhd_spec":
+        return synth.make_case(name=name, num_seqs=3, q_len=2, h_q=16, h_k=4, page_size=32,
+                               seq_lens=[33, 500, 1], layout="NHD", kv_format="e2m3", outlier_channels=4,
+                               seed=25)
+    raise KeyError(name)
+
+
+SMALL = ["ragged_hnd", "split_nhd", "spec_causal", "spec_noncausal", "fp6_small", "fp6_nhd_spec"]
+
+
+@pytest.mark.parametrize("name", ["tiny"] + SMALL)
+def test_quantize_q_bit_exact(name):
+    w = synth.tiny() if name == "tiny" else _case(name)
+    got = run_gpu(w, impl=1)
+    _, _, codes, desc = run_oracle(w, units=[])
+    assert np.array_equal(got["q_codes"], codes)
+    assert np.array_equal(got["q_descale"], desc)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_tiny(impl):
+    w = synth.tiny()
+    got = run_gpu(w, impl=impl)
+    ref, lse, _, _ = run_oracle(w)
+    compare(w, got["out"], ref, all_units(w), "tiny")
+    np.testing.assert_allclose(got["lse"], lse, atol=2e-3, rtol=1e-4)
+    assert got["status"] == 0
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", SMALL)
+def test_small_cases(impl, name):
+    w = _case(name)
+    got = run_gpu(w, impl=impl)
+    ref, lse, _, _ = run_oracle(w)
+    compare(w, got["out"], ref, all_units(w), name)
+    real = w.seq_lens > 0
+    np.testing.assert_allclose(got["lse"][real], lse[real], atol=2e-3, rtol=1e-4)
+    assert np.all(got["lse"][~real] == SENTINEL)
+    assert got["status"] == 0
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_split_equals_unsplit(impl):
+    w = _case("split_nhd")
+    a = run_gpu(w, impl=impl, max_splits=1)
+    b = run_gpu(w, impl=impl, max_splits=16)
+    assert not a["info"]["with_reduction"] and b["info"]["with_reduction"]
+    assert max(b["info"]["n_splits"][: w.num_seqs]) > 1
+    ref, _, _, _ = run_oracle(w)
+    compare(w, a["out"], ref, all_units(w), "unsplit")
+    compare(w, b["out"], ref, all_units(w), "split")
+    vm = np.abs(a["out"]).max()
+    assert np.abs(a["out"] - b["out"]).max() <= 2e-2 * max(vm, 1e-6)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_upper_bound_plan_and_margin(impl):
+    """Planning on longer lengths (upper bound + draft margin) must not change
+    the result: the kernel masks with the exact device lengths."""
+    w = _case("split_nhd")
+    got = run_gpu(w, impl=impl, plan_lens=w.seq_lens + 700, margin=3)
+    ref, _, _, _ = run_oracle(w)
+    compare(w, got["out"], ref, all_units(w), "upper-bound plan")
+    w2 = _case("ragged_hnd")
+    got2 = run_gpu(w2, impl=impl, plan_lens=w2.seq_lens + 129, margin=2, ctas_per_sm=1, sm_count=20)
+    ref2, _, _, _ = run_oracle(w2)
+    compare(w2, got2["out"], ref2, all_units(w2), "upper-bound plan, split")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_per_seq_descales_and_strided_output(impl):
+    w = _case("ragged_hnd")
+    got = run_gpu(w, impl=impl, descale_per_seq=True, out_strided=True)
+    ref, _, _, _ = run_oracle(w)
+    compare(w, got["out"], ref, all_units(w), "per-(seq, head) descales, strided O")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_repeated_steps_are_identical(impl):
+    w = _case("spec_causal")
+    a = run_gpu(w, impl=impl, steps=1)
+    b = run_gpu(w, impl=impl, steps=3)
+    assert np.array_equal(a["out"], b["out"])
+
+
+# ----------------------------------------------------------------------------
+# the five configurations at full size, in the benchmark's launch settings
+# ----------------------------------------------------------------------------
+FULL = {
+    "qwen3_8b_decode": dict(ctas_per_sm=4, max_splits=64),
+    "long_split": dict(ctas_per_sm=2, max_splits=64),
+    "long_single": dict(ctas_per_sm=2, max_splits=64),
+    "spec_verify": dict(ctas_per_sm=2, max_splits=64),
+    "spec_verify_noncausal": dict(ctas_per_sm=2, max_splits=64),
+    "fp6_decode": dict(ctas_per_sm=2, max_splits=64),
+}
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_sampled(impl, name):
+    w = synth.WORKLOADS[name]()
+    got = run_gpu(w, impl=impl, **FULL[name])
+    units = sample_units(w, 6, seed=3)
+    # always include the last request (padding in spec_verify) and request 0
+    units = sorted(set(units) | {(w.num_seqs - 1, 0), (0, w.h_k - 1)})
+    ref, _, _, _ = run_oracle(w, units=units)
+    compare(w, got["out"], ref, units, name)
+    real_rows = np.repeat(w.seq_lens > 0, w.q_len)
+    assert np.all(np.isfinite(got["out"][real_rows]))
+    assert np.all(got["out"][~real_rows] == SENTINEL)
+    assert got["status"] == 0

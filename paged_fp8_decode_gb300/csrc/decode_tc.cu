@@ -1,0 +1,548 @@
+// Tensor-core variant of mj_decode_attention for sm_103a: TMA page streaming
+// into a shared-memory ring, tcgen05.mma (kind f8f6f4, e4m3 x e4m3 -> f32) with
+// accumulators in tensor memory, online softmax on CUDA cores.
+//
+// The README of the mjolnir-kernel package ("A decode step", item 3) describes
+// the shape of this design for Jetson Thor: TMA page loads into a ring with an
+// L2 evict-first hint, tcgen05 MMAs accumulating S and O in TMEM, softmax
+// warpgroups. This kernel is written for GB300 from that description:
+//
+// * One CTA per (work row, KV head, query-row tile); 6 warps:
+//     warp 0     TMA producer: block-table lookups (32 entries per warp load),
+//                one 4-D tensor-map load per (page, head) into the ring;
+//     warp 1     TMEM allocation and the single-thread MMA issuer;
+//     warps 2-5  softmax warpgroup: thread x owns TMEM lane x, i.e. key x of a
+//                128-key tile for S and channel x for O.
+// * The ring alternates K and V tiles of 128 keys x 128 bytes, 128-byte
+//   swizzled by the TMA so that tcgen05.mma reads them directly.
+// * Both products are issued "keys as M" so that M = 128 fills the tensor
+//   core even for a handful of query rows:
+//     S^T[key][row] = K[key][:] . Q[row][:]       A = K tile (K-major), B = Q tile
+//     O^T[d][col]  += V^T[d][key] . P^T[key][col] A = V tile (MN-major), B = P tile
+// * P is written as two e4m3 terms, hi = e4m3(p) and lo = e4m3(p - hi), in
+//   separate columns of the same PV product (the query rows leave spare N
+//   columns anyway): O gets P to ~2^-8 relative precision at no extra MMA.
+//   P is scaled by 2^8 (p = 2^(t - m + 8) <= 256) so that its e4m3 terms stay
+//   normal well into the tail of the softmax; the factor cancels in O / l.
+// * Keys at or past the device seq_len are masked by select on S; in a
+//   request's last, partial tile the softmax warps also zero the V rows past
+//   the end before the PV product (page tails may hold NaN codes, and 0 * NaN
+//   would reach O through the MMA).
+// * Every wait is bounded (2 s); a timeout raises a status bit and the CTA
+//   unwinds, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mj_device.cuh"
+#include "mj_internal.h"
+#include "tc_ptx.cuh"
+
+namespace mj {
+
+namespace {
+
+constexpr int kThreadsTc = 192;
+constexpr int kSoftmaxWarp0 = 2;
+constexpr int kTileBytes = kKvTile * 128;  // 128 keys x 128 bytes
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct TcSmem {
+  // offsets (bytes) from the 1024-aligned dynamic shared-memory base
+  uint32_t ring, q, p0, p1, ctrl, total;
+};
+
+__host__ __device__ inline TcSmem tc_smem_layout(int stages, int nqk, int npv) {
+  TcSmem s;
+  s.ring = 0;
+  s.q = stages * kTileBytes;
+  s.p0 = s.q + ((nqk * 128 + 1023) / 1024) * 1024;
+  s.p1 = s.p0 + ((npv * 128 + 1023) / 1024) * 1024;
+  s.ctrl = s.p1 + ((npv * 128 + 1023) / 1024) * 1024;
+  s.total = s.ctrl + 2048;
+  return s;
+}
+
+// control block inside the ctrl region
+struct Ctrl {
+  uint64_t full[16];
+  uint64_t empty[16];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t red_bar[2];  // the 4 softmax warps have posted their row maxima
+  uint64_t sum_bar;     // ... their row sums
+  uint64_t drain;       // MMA drain after an abort
+  uint32_t tmem_base;
+  int abort;
+  float red[2][4][32];  // per-tile row maxima of the 4 softmax warps
+  float lsum[4][32];    // row sums of the 4 softmax warps
+};
+static_assert(sizeof(Ctrl) <= 2048, "control block");
+
+__device__ __forceinline__ uint32_t p_byte_offset(int n, int key) {
+  // P^T tile: row n (a B-matrix column), 128 keys, K-major, 128-byte swizzle
+  return uint32_t(n) * 128u + ((uint32_t((key >> 4) ^ (n & 7))) << 4) + uint32_t(key & 15);
+}
+
+template <int NQK, int NPV>
+__global__ void __launch_bounds__(kThreadsTc, 2)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                     DecodeParams p) {
+  constexpr int NH = NPV / 2;  // query rows per P half (hi | lo)
+  static_assert(NH <= NQK, "row tile");
+  constexpr uint32_t kTmemCols = (2 * (NQK + NPV) <= 64) ? 64 : (2 * (NQK + NPV) <= 128 ? 128 : 256);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int g = blockIdx.y;
+  const int4 w = reinterpret_cast<const int4*>(p.work)[blockIdx.x];
+  const int b = w.x;
+  if (w.z <= w.y || b < 0 || b >= p.num_seqs) return;
+  if (p.with_reduction && (w.w < 0 || w.w >= p.max_splits || b >= p.part_seqs)) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPlan);
+    return;
+  }
+  const int L = p.seq_lens[b];
+  if (L <= 0) return;
+  const int64_t k0 = int64_t(w.y) * kKvTile;
+  const int64_t k1 = min(int64_t(w.z) * kKvTile, int64_t(L));
+  if (k1 <= k0) return;
+  const int r0 = blockIdx.z * p.tw;
+  const int nr = min(min(p.tw, p.n_q - r0), NH);
+  if (nr <= 0) return;
+  const int ntiles = int((k1 - k0 + kKvTile - 1) / kKvTile);
+  const int stages = p.kv_stages;
+
+  const TcSmem lay = tc_smem_layout(stages, NQK, NPV);
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + lay.ctrl);
+  const uint32_t ring_addr = tc::smem_u32(smem + lay.ring);
+  const uint32_t q_addr = tc::smem_u32(smem + lay.q);
+  const uint32_t p_stride = lay.p1 - lay.p0;  // P buffer j at p0 + j * p_stride
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- set-up: barriers, TMEM, Q tile ------------------------------------
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      tc::mbar_init(tc::smem_u32(&ctl.full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(tc::smem_u32(&ctl.s_full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.p_full[s]), 128);
+      tc::mbar_init(tc::smem_u32(&ctl.o_full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.red_bar[s]), 4);
+    }
+    tc::mbar_init(tc::smem_u32(&ctl.sum_bar), 4);
+    tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
+    ctl.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tmap_k);
+    tc::prefetch_tmap(&tmap_v);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp >= kSoftmaxWarp0) {
+    // Q codes rows r0 .. r0+nr-1 -> Q tile [NQK rows][128 B], K-major, 128-byte
+    // swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); other rows 0.
+    const int x = tid - kSoftmaxWarp0 * 32;
+    const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
+    for (int i = x; i < NQK * 8; i += 128) {
+      const int r = i >> 3, c = i & 7;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * kHeadDim + c * 16);
+      *reinterpret_cast<uint4*>(smem + lay.q + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+    }
+    tc::fence_async_smem();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort = &ctl.abort;
+
+  // TMEM columns: S buffers at [0, NQK) and [NQK, 2 NQK), O buffers after them
+  auto tS = [&](int j) { return tmem + uint32_t((j & 1) * NQK); };
+  auto tO = [&](int j) { return tmem + uint32_t(2 * NQK + (j & 1) * NPV); };
+
+  if (warp == 0) {
+    // ======================= TMA producer ===================================
+    const uint64_t pol = p.evict_first ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
+    const int ps = p.page_size;
+    const int ppt = kKvTile / ps;
+    const int64_t first_page = k0 / ps;
+    const int64_t npages = (k1 + ps - 1) / ps - first_page;
+    const int32_t* bt = p.block_table + int64_t(b) * p.bt_stride + first_page;
+    const uint32_t page_bytes = uint32_t(ps) * 128u;
+    int64_t batch = -1;
+    int entry = -1;
+    bool ok = true;
+    int issued = 0;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      int pg[8];
+      const int nvalid = int(min(int64_t(ppt), npages - int64_t(i) * ppt));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        pg[j] = -1;
+        if (j < nvalid) {
+          const int64_t e = int64_t(i) * ppt + j;
+          if (batch < 0 || e >= batch + 32) {
+            batch = e;
+            entry = (e + lane < npages) ? bt[e + lane] : -1;
+          }
+          pg[j] = __shfl_sync(0xFFFFFFFFu, entry, int(e - batch));
+        }
+      }
+      for (int half = 0; half < 2 && ok; ++half) {
+        const int u = 2 * i + half;
+        const int slot = u % stages;
+        const uint32_t round = uint32_t(u / stages);
+        if (lane == 0) {
+          ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
+          if (ok) {
+            const uint32_t full = tc::smem_u32(&ctl.full[slot]);
+            tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_bytes);
+            const CUtensorMap* map = half ? &tmap_v : &tmap_k;
+            const uint32_t dst = ring_addr + uint32_t(slot) * kTileBytes;
+            for (int j = 0; j < nvalid; ++j) {
+              if (pg[j] < 0 || int64_t(pg[j]) >= p.num_pages) atomicOr(p.status, kStatusBadPage);
+              if (p.tma_head_inner)
+                tc::tma_load_4d(dst + j * page_bytes, map, full, 0, g, 0, pg[j], pol);
+              else
+                tc::tma_load_4d(dst + j * page_bytes, map, full, 0, 0, g, pg[j], pol);
+            }
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      }
+    }
+    if (!ok && lane == 0) {
+      // abort: wait (bounded) for the loads still in flight before the CTA exits
+      const uint64_t t0 = tc::globaltimer_ns();
+      for (int u = max(0, issued - stages); u < issued; ++u)
+        while (!tc::mbar_try_wait(tc::smem_u32(&ctl.full[u % stages]), uint32_t(u / stages) & 1u) &&
+               tc::globaltimer_ns() - t0 < 100000000ull) {
+        }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer ======================================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false);
+      constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, false);
+      const uint64_t qdesc = tc::smem_desc(q_addr, 16, 1024, tc::kSwizzle128B);
+      bool ok = true;
+      auto issue_qk = [&](int j) {
+        const int u = 2 * j;
+        const int slot = u % stages;
+        ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
+        if (!ok) return;
+        tc::tc_fence_after();
+        const uint64_t kdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, 16, 1024, tc::kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = 128 channels in steps of 32 bytes
+          tc::umma_f8f6f4(tS(j), kdesc + uint64_t(2 * k), qdesc + uint64_t(2 * k), idesc_qk, k > 0);
+        tc::umma_commit(tc::smem_u32(&ctl.s_full[j & 1]));
+        tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
+      };
+      issue_qk(0);
+      for (int i = 0; i < ntiles && ok; ++i) {
+        if (i + 1 < ntiles) issue_qk(i + 1);
+        if (!ok) break;
+        ok = tc::mbar_wait(tc::smem_u32(&ctl.p_full[i & 1]), uint32_t(i >> 1) & 1u, abort, kWaitLimitNs);
+        const int u = 2 * i + 1;
+        const int slot = u % stages;
+        ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint64_t vdesc =
+            tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, kTileBytes, 1024, tc::kSwizzle128B);
+        const uint64_t pdesc =
+            tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(i & 1) * p_stride, 16, 1024, tc::kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V)
+          tc::umma_f8f6f4(tO(i), vdesc + uint64_t(256 * k), pdesc + uint64_t(2 * k), idesc_pv, k > 0);
+        tc::umma_commit(tc::smem_u32(&ctl.o_full[i & 1]));
+        tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
+      }
+      if (!ok) {
+        // abort: wait (bounded) until every MMA issued so far has completed
+        tc::umma_commit(tc::smem_u32(&ctl.drain));
+        const uint64_t t0 = tc::globaltimer_ns();
+        while (!tc::mbar_try_wait(tc::smem_u32(&ctl.drain), 0) && tc::globaltimer_ns() - t0 < 100000000ull) {
+        }
+      }
+    }
+  } else {
+    // ======================= softmax warpgroup ===============================
+    const int qd = warp & 3;          // TMEM lane quadrant of this warp
+    const int x = qd * 32 + lane;     // key of the tile (S) / channel (O)
+    const uint32_t lane_off = uint32_t(qd * 32) << 16;
+    const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
+    const float scale = p.q_descale[int64_t(b) * p.h_k + g] * kd * p.qk_scale_log2;
+    const int64_t causal_base = int64_t(L) - p.q_len;
+
+    float m_run[NH], l_part[NH], o_acc[NH], alpha_prev[NH];
+#pragma unroll
+    for (int r = 0; r < NH; ++r) {
+      m_run[r] = -INFINITY;
+      l_part[r] = 0.f;
+      o_acc[r] = 0.f;
+      alpha_prev[r] = 1.f;
+    }
+    bool ok = true;
+
+    auto absorb = [&](int j) {
+      ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[j & 1]), uint32_t(j >> 1) & 1u, abort, kWaitLimitNs);
+      if (!ok) return;
+      tc::tc_fence_after();
+      float ov[NPV];
+#pragma unroll
+      for (int c = 0; c < NPV; c += 16) tc::tmem_ld16(tO(j) + lane_off + c, ov + c);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int r = 0; r < NH; ++r) o_acc[r] = fmaf(o_acc[r], alpha_prev[r], ov[r] + ov[NH + r]);
+    };
+
+    for (int i = 0; i < ntiles; ++i) {
+      ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.s_full[i & 1]), uint32_t(i >> 1) & 1u, abort, kWaitLimitNs);
+      if (!ok) break;
+      tc::tc_fence_after();
+      float s[NQK];
+#pragma unroll
+      for (int c = 0; c < NQK; c += 16) tc::tmem_ld16(tS(i) + lane_off + c, s + c);
+      tc::tmem_wait_ld();
+
+      const int64_t tile0 = k0 + int64_t(i) * kKvTile;
+      const int64_t key = tile0 + x;
+      const bool valid = key < k1;
+      float t[NH];
+#pragma unroll
+      for (int r = 0; r < NH; ++r) {
+        const int tq = (r0 + r) / p.h_r;
+        const bool vis = valid && r < nr && (!p.causal || key <= causal_base + tq);
+        t[r] = vis ? s[r] * scale : -INFINITY;
+        const float wm = warp_max(t[r]);
+        if (lane == 0) ctl.red[i & 1][qd][r] = wm;
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.red_bar[i & 1]));
+      ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[i & 1]), uint32_t(i >> 1) & 1u, abort, kWaitLimitNs);
+      if (!ok) break;
+
+      float alpha_cur[NH];
+#pragma unroll
+      for (int r = 0; r < NH; ++r) {
+        const float tm = fmaxf(fmaxf(ctl.red[i & 1][0][r], ctl.red[i & 1][1][r]),
+                               fmaxf(ctl.red[i & 1][2][r], ctl.red[i & 1][3][r]));
+        const float m_new = fmaxf(m_run[r], tm);
+        float pr = 0.f, alpha = 1.f;
+        if (m_new != -INFINITY) {
+          alpha = fast_exp2(m_run[r] - m_new);  // 0 when m_run = -inf
+          pr = fast_exp2(t[r] - m_new + 8.f);   // <= 256; 0 for masked keys
+        }
+        const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(pr, 0.f), __NV_SATFINITE, __NV_E4M3);
+        const float hi = e4m3x2_to_float2(hi2).x;
+        const __nv_fp8x2_storage_t lo2 =
+            __nv_cvt_float2_to_fp8x2(make_float2(pr - hi, 0.f), __NV_SATFINITE, __NV_E4M3);
+        const float lo = e4m3x2_to_float2(lo2).x;
+        l_part[r] = fmaf(l_part[r], alpha, hi + lo);
+        m_run[r] = m_new;
+        alpha_cur[r] = alpha;
+        uint8_t* pt = smem + lay.p0 + (i & 1) * p_stride;
+        pt[p_byte_offset(r, x)] = uint8_t(hi2 & 0xFF);
+        pt[p_byte_offset(NH + r, x)] = uint8_t(lo2 & 0xFF);
+      }
+      if (tile0 + kKvTile > k1) {
+        // last, partial tile: zero the V rows past the end before the PV product
+        const int u = 2 * i + 1;
+        const int slot = u % stages;
+        ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
+        if (ok && !valid) {
+          uint4* row = reinterpret_cast<uint4*>(smem + lay.ring + slot * kTileBytes + x * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      tc::fence_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(tc::smem_u32(&ctl.p_full[i & 1]));
+      if (i > 0) absorb(i - 1);
+#pragma unroll
+      for (int r = 0; r < NH; ++r) alpha_prev[r] = alpha_cur[r];
+      if (!ok) break;
+    }
+    if (ok) absorb(ntiles - 1);
+
+    // ---- epilogue --------------------------------------------------------
+#pragma unroll
+    for (int r = 0; r < NH; ++r) {
+      const float ls = warp_sum(l_part[r]);
+      if (lane == 0) ctl.lsum[qd][r] = ls;
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.sum_bar));
+    ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.sum_bar), 0, abort, kWaitLimitNs);
+    if (ok) {
+      const bool direct = !p.with_reduction || p.n_splits[b] <= 1;
+      const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
+#pragma unroll
+      for (int r = 0; r < NH; ++r) {
+        if (r >= nr) break;
+        const float lr = ctl.lsum[0][r] + ctl.lsum[1][r] + ctl.lsum[2][r] + ctl.lsum[3][r];
+        const float on = lr > 0.f ? o_acc[r] / lr : 0.f;
+        const int row = r0 + r;
+        if (direct) {
+          const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
+          float val = on * vd;
+          if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + x];
+          p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + x] = float_to_bf16_bits(val);
+          if (p.lse && x == 0)
+            p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
+                lr > 0.f ? (m_run[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
+        } else {
+          const int64_t idx = part_index(p, b, w.w, g, row);
+          p.o_part[idx * kHeadDim + x] = on;
+          if (x == 0) {
+            p.m_part[idx] = lr > 0.f ? m_run[r] : -INFINITY;
+            p.l_part[idx] = lr * (1.f / 256.f);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown ------------------------------------------------------------
+  if (*abort && tid == 0) atomicOr(p.status, kStatusTimeout);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 4-D byte tensor (row, token, head, page) of one K or V cache; the smaller of
+// the token / head strides goes to dimension 1 (a box extent of 1 in the head
+// dimension leaves the shared-memory layout [token][128 B] either way).
+bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, int64_t sp, int64_t st, int64_t sh,
+                   bool head_inner) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int64_t sh_eff = p.h_k == 1 ? (head_inner ? 16 : sp) : sh;
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  dims[0] = 128;
+  box[0] = 128;
+  if (head_inner) {
+    dims[1] = cuuint64_t(p.h_k);
+    dims[2] = cuuint64_t(p.page_size);
+    strides[0] = cuuint64_t(sh_eff);
+    strides[1] = cuuint64_t(st);
+    box[1] = 1;
+    box[2] = cuuint32_t(p.page_size);
+  } else {
+    dims[1] = cuuint64_t(p.page_size);
+    dims[2] = cuuint64_t(p.h_k);
+    strides[0] = cuuint64_t(st);
+    strides[1] = cuuint64_t(sh_eff);
+    box[1] = cuuint32_t(p.page_size);
+    box[2] = 1;
+  }
+  dims[3] = cuuint64_t(p.num_pages);
+  strides[2] = cuuint64_t(sp);
+  box[3] = 1;
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int NQK, int NPV>
+cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
+  const TcSmem lay = tc_smem_layout(p.kv_stages, NQK, NPV);
+  const int bytes = int(lay.total) + 1024;
+  static int configured = 0;  // largest dynamic smem size set so far
+  if (bytes > configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bytes);
+    if (e != cudaSuccess) return e;
+    configured = bytes;
+  }
+  dim3 grid(p.num_work, p.h_k, p.n_row_tiles);
+  decode_tc_kernel<NQK, NPV><<<grid, kThreadsTc, bytes, stream>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_default_stages() { return 6; }
+
+bool tc_supported(const DecodeParams& p) {
+  if (p.kv_format != MJ_KV_E4M3) return false;
+  if (p.n_q > 32 && p.tw != 32) return false;
+  if (p.num_pages > INT32_MAX || p.h_k > 65535) return false;
+  const int64_t sm[] = {p.k_sp, p.v_sp};
+  for (int64_t s : sm)
+    if (s == 0) return false;
+  if (!encode_fn()) return false;
+  return true;
+}
+
+int tc_max_stages() { return 13; }
+
+cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsupported) {
+  *unsupported = false;
+  if (!tc_supported(p)) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  if (p.kv_stages <= 0) p.kv_stages = tc_default_stages();
+  if (p.kv_stages > tc_max_stages()) p.kv_stages = tc_max_stages();
+  p.tma_head_inner = (p.k_sh < p.k_st) ? 1 : 0;
+  if (((p.v_sh < p.v_st) ? 1 : 0) != p.tma_head_inner) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  CUtensorMap mk, mv;
+  if (!encode_kv_map(&mk, p.k_cache, p, p.k_sp, p.k_st, p.k_sh, p.tma_head_inner) ||
+      !encode_kv_map(&mv, p.v_cache, p, p.v_sp, p.v_st, p.v_sh, p.tma_head_inner)) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  if (p.num_work == 0) return cudaSuccess;
+  // row tile = the plan's tile width (16 or 32 rows)
+  if (p.tw <= 16) {
+    if (p.n_q <= 8) return launch_tc<16, 16>(mk, mv, p, stream);
+    return launch_tc<16, 32>(mk, mv, p, stream);
+  }
+  return launch_tc<32, 64>(mk, mv, p, stream);
+}
+
+}  // namespace mj

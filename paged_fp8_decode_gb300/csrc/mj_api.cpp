@@ -297,6 +297,12 @@ int mj_decode_attention(const mj_decode_args* args, void* stream) {
   int st = make_params(args, &p);
   if (st != MJ_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (args->impl != MJ_IMPL_SIMT) {
+    bool unsupported = false;
+    const cudaError_t e = mj::launch_decode_tc(p, s, &unsupported);
+    if (!unsupported) return status_of(e);
+    if (args->impl == MJ_IMPL_TCGEN05) return MJ_ERR_UNSUPPORTED;
+  }
   // The CUDA-core kernel tiles query rows by the smallest power of two that
   // holds them (at least 4, at most 32).
   p.tw = std::max(4, std::min(32, next_pow2(p.n_q)));

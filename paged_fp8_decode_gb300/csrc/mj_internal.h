@@ -63,6 +63,7 @@ struct DecodeParams {
 
   int kv_stages;
   int evict_first;
+  int tma_head_inner;  // tensor-core kernel: head dimension is the TMA's dim 1
 };
 
 // Index of a partial row: ((b*max_splits + s)*h_k + g)*n_q + row.
@@ -87,5 +88,8 @@ struct QuantParams {
 cudaError_t launch_quantize_q(const QuantParams& p, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
+// Tensor-core kernel; sets *unsupported (and launches nothing) when the
+// arguments are outside its envelope.
+cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsupported);
 
 }  // namespace mj

@@ -13,7 +13,12 @@ from tests._harness import SENTINEL, all_units, compare, run_gpu, run_oracle, sa
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = [1]  # MJ_IMPL_SIMT; the tensor-core kernel joins when it exists
+IMPLS = [1, 2]  # MJ_IMPL_SIMT, MJ_IMPL_TCGEN05
+
+
+def _skip_unsupported(impl, w):
+    if impl == 2 and w.kv_format == "e2m3":
+        pytest.skip("the tensor-core kernel reads e4m3 caches only")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -78,6 +83,7 @@ def test_tiny(impl):
 @pytest.mark.parametrize("name", SMALL)
 def test_small_cases(impl, name):
     w = _case(name)
+    _skip_unsupported(impl, w)
     got = run_gpu(w, impl=impl)
     ref, lse, _, _ = run_oracle(w)
     compare(w, got["out"], ref, all_units(w), name)
@@ -148,6 +154,7 @@ FULL = {
 @pytest.mark.parametrize("name", list(FULL))
 def test_full_size_sampled(impl, name):
     w = synth.WORKLOADS[name]()
+    _skip_unsupported(impl, w)
     got = run_gpu(w, impl=impl, **FULL[name])
     units = sample_units(w, 6, seed=3)
     # always include the last request (padding in spec_verify) and request 0
@@ -158,3 +165,12 @@ def test_full_size_sampled(impl, name):
     assert np.all(np.isfinite(got["out"][real_rows]))
     assert np.all(got["out"][~real_rows] == SENTINEL)
     assert got["status"] == 0
+
+
+def test_tcgen05_rejects_what_it_cannot_run():
+    import paged_fp8_decode_gb300 as mj
+
+    w = _case("fp6_small")
+    with pytest.raises(mj.MjError) as e:
+        run_gpu(w, impl=2)
+    assert e.value.status == mj.MJ_ERR_UNSUPPORTED

@@ -259,6 +259,31 @@ MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
  * ---------------------------------------------------------------------- */
 MJ_API int mj_merge_lse(const mj_decode_args* args, void* stream);
 
+/* ------------------------------------------------------------------------
+ * mj_decode_attention_noalloc — mj_decode_attention followed by mj_merge_lse,
+ * with the split-KV partials in scratch memory compiled into the library
+ * instead of a caller workspace. The pages have no counterpart for this call.
+ *
+ * For callers that cannot allocate device memory: an engine that reserves
+ * almost all of HBM for its KV-cache pool at start-up and allows no later
+ * cudaMalloc, or a plugin inside a framework whose caching allocator owns
+ * device memory (a raw cudaMalloc/cudaFree would bypass it and synchronise
+ * the device). Such a caller still passes every input and output; only
+ * args->workspace and args->workspace_bytes are ignored.
+ *
+ * The scratch is a fixed MJ_NOALLOC_SCRATCH_BYTES array (16 MiB) that every
+ * GPU loading the library holds until the process exits. A plan whose
+ * partials need more (mj_workspace_size(part_seqs, max_splits, ...) above the
+ * limit) is rejected with MJ_ERR_CAPACITY before anything is enqueued. The
+ * first call on a device looks up the array's device address and zeroes its
+ * status header (synchronously); make that first call before any stream
+ * capture. All calls share the array and it keeps the last call's contents:
+ * calls whose kernels overlap on the GPU race on it, so issue them in order
+ * on one stream. The status word in this scratch is not readable by callers.
+ * ---------------------------------------------------------------------- */
+#define MJ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+MJ_API int mj_decode_attention_noalloc(const mj_decode_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

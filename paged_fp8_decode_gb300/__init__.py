@@ -40,8 +40,10 @@ KV_TILE = 128
 EXPORTS = (
     "mj_status_string", "mj_version", "mj_tile_width", "mj_slots", "mj_plan_split_kv",
     "mj_quantize_q", "mj_workspace_size", "mj_workspace_init", "mj_workspace_status",
-    "mj_decode_attention", "mj_merge_lse",
+    "mj_decode_attention", "mj_merge_lse", "mj_decode_attention_noalloc",
 )
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class MjError(RuntimeError):
@@ -101,6 +103,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mj_workspace_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.mj_decode_attention.argtypes = [ctypes.POINTER(mj_decode_args), vp]
     lib.mj_merge_lse.argtypes = [ctypes.POINTER(mj_decode_args), vp]
+    lib.mj_decode_attention_noalloc.argtypes = [ctypes.POINTER(mj_decode_args), vp]
     _lib = lib
     return lib
 
@@ -207,6 +210,14 @@ def mj_decode_attention(args: mj_decode_args, stream=None):
 
 def mj_merge_lse(args: mj_decode_args, stream=None):
     _check("mj_merge_lse", load_library().mj_merge_lse(ctypes.byref(args), _stream(stream)))
+
+
+def mj_decode_attention_noalloc(args: mj_decode_args, stream=None):
+    """Decode + merge with the library's fixed scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory; see
+    include/mj.h)."""
+    _check("mj_decode_attention_noalloc",
+           load_library().mj_decode_attention_noalloc(ctypes.byref(args), _stream(stream)))
 
 
 from .step import DecodeStep  # noqa: E402,F401

@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 # knobs per workload: (ctas_per_sm, max_splits, kv_stages)
 DEFAULT_KNOBS = {
-    "qwen3_8b_decode": (4, 64, 0),
+    "qwen3_8b_decode": (2, 64, 6),
     "long_split": (2, 64, 0),
     "long_single": (2, 64, 0),
     "spec_verify": (2, 64, 0),

@@ -33,6 +33,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <climits>
+#include <cstddef>
 #include <mutex>
 
 #include "mj_device.cuh"
@@ -76,22 +78,50 @@ struct Ctrl {
   uint64_t drain;       // MMA drain after an abort
   uint32_t tmem_base;
   int abort;
-  float red[2][4][32];  // per-tile row maxima of the 4 softmax warps
-  float lsum[4][32];    // row sums of the 4 softmax warps
+  alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
+  alignas(16) float lsum[4][32];    // row sums of the 4 softmax warps
 };
 static_assert(sizeof(Ctrl) <= 2048, "control block");
+static_assert(offsetof(Ctrl, red) % 16 == 0 && offsetof(Ctrl, lsum) % 16 == 0, "float4 access to red/lsum");
+
+// Reduce NR per-lane values over the 32 lanes of a warp, one row per lane
+// group: a reduce-scatter (each step halves the rows a lane keeps and
+// exchanges the other half) followed by a butterfly over the lanes that share
+// a row. Row r ends up in lanes r*(32/NR) .. r*(32/NR) + 32/NR - 1. This takes
+// NR - 1 + log2(32/NR) shuffles instead of 5*NR for independent butterflies.
+template <int NR, bool MAX>
+__device__ __forceinline__ float rs_reduce(float (&v)[NR], int lane) {
+#pragma unroll
+  for (int c = NR, m = 16; c > 1; c >>= 1, m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < c / 2; ++j) {
+      const float send = upper ? v[j] : v[c / 2 + j];
+      const float keep = upper ? v[c / 2 + j] : v[j];
+      const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
+      v[j] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int m = 16 / NR; m > 0; m >>= 1) {
+    const float o = __shfl_xor_sync(0xFFFFFFFFu, r, m);
+    r = MAX ? fmaxf(r, o) : r + o;
+  }
+  return r;
+}
 
 __device__ __forceinline__ uint32_t p_byte_offset(int n, int key) {
   // P^T tile: row n (a B-matrix column), 128 keys, K-major, 128-byte swizzle
   return uint32_t(n) * 128u + ((uint32_t((key >> 4) ^ (n & 7))) << 4) + uint32_t(key & 15);
 }
 
-template <int NQK, int NPV>
+template <int NQK, int NPV, int NR>
 __global__ void __launch_bounds__(kThreadsTc, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
-  constexpr int NH = NPV / 2;  // query rows per P half (hi | lo)
-  static_assert(NH <= NQK, "row tile");
+  constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
+  static_assert(NH <= NQK && NR <= NH && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
   constexpr uint32_t kTmemCols = (2 * (NQK + NPV) <= 64) ? 64 : (2 * (NQK + NPV) <= 128 ? 128 : 256);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -111,7 +141,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   const int64_t k1 = min(int64_t(w.z) * kKvTile, int64_t(L));
   if (k1 <= k0) return;
   const int r0 = blockIdx.z * p.tw;
-  const int nr = min(min(p.tw, p.n_q - r0), NH);
+  const int nr = min(min(p.tw, p.n_q - r0), NR);
   if (nr <= 0) return;
   const int ntiles = int((k1 - k0 + kKvTile - 1) / kKvTile);
   const int stages = p.kv_stages;
@@ -186,42 +216,35 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     bool ok = true;
     int issued = 0;
     for (int i = 0; i < ntiles && ok; ++i) {
-      int pg[8];
+      // lane j < nvalid issues the load of page j of tile i (one page id per lane)
       const int nvalid = int(min(int64_t(ppt), npages - int64_t(i) * ppt));
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        pg[j] = -1;
-        if (j < nvalid) {
-          const int64_t e = int64_t(i) * ppt + j;
-          if (batch < 0 || e >= batch + 32) {
-            batch = e;
-            entry = (e + lane < npages) ? bt[e + lane] : -1;
-          }
-          pg[j] = __shfl_sync(0xFFFFFFFFu, entry, int(e - batch));
-        }
+      const int64_t e0 = int64_t(i) * ppt;
+      if (batch < 0 || e0 + nvalid > batch + 32) {
+        batch = e0;
+        entry = (e0 + lane < npages) ? bt[e0 + lane] : -1;
       }
+      const int pg = __shfl_sync(0xFFFFFFFFu, entry, int(e0 - batch) + (lane & 7));
+      if (lane < nvalid && (pg < 0 || int64_t(pg) >= p.num_pages)) atomicOr(p.status, kStatusBadPage);
       for (int half = 0; half < 2 && ok; ++half) {
         const int u = 2 * i + half;
         const int slot = u % stages;
         const uint32_t round = uint32_t(u / stages);
+        const uint32_t full = tc::smem_u32(&ctl.full[slot]);
         if (lane == 0) {
           ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
-          if (ok) {
-            const uint32_t full = tc::smem_u32(&ctl.full[slot]);
-            tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_bytes);
-            const CUtensorMap* map = half ? &tmap_v : &tmap_k;
-            const uint32_t dst = ring_addr + uint32_t(slot) * kTileBytes;
-            for (int j = 0; j < nvalid; ++j) {
-              if (pg[j] < 0 || int64_t(pg[j]) >= p.num_pages) atomicOr(p.status, kStatusBadPage);
-              if (p.tma_head_inner)
-                tc::tma_load_4d(dst + j * page_bytes, map, full, 0, g, 0, pg[j], pol);
-              else
-                tc::tma_load_4d(dst + j * page_bytes, map, full, 0, 0, g, pg[j], pol);
-            }
-            ++issued;
-          }
+          if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_bytes);
         }
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (ok && lane < nvalid) {
+          const CUtensorMap* map = half ? &tmap_v : &tmap_k;
+          const uint32_t dst = ring_addr + uint32_t(slot) * kTileBytes + uint32_t(lane) * page_bytes;
+          if (p.tma_head_inner)
+            tc::tma_load_4d(dst, map, full, 0, g, 0, pg, pol);
+          else
+            tc::tma_load_4d(dst, map, full, 0, 0, g, pg, pol);
+        }
+        if (ok) ++issued;
+        __syncwarp();
       }
     }
     if (!ok && lane == 0) {
@@ -238,39 +261,62 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
       constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, false);
       const uint64_t qdesc = tc::smem_desc(q_addr, 16, 1024, tc::kSwizzle128B);
+      // Event loop: issue QK_nq as soon as K tile nq has landed (at most one
+      // tile ahead of PV: two S buffers), and PV_np as soon as P_np is
+      // written and V tile np has landed. Neither product waits behind the
+      // other's operands.
       bool ok = true;
-      auto issue_qk = [&](int j) {
-        const int u = 2 * j;
-        const int slot = u % stages;
-        ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
-        if (!ok) return;
-        tc::tc_fence_after();
-        const uint64_t kdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, 16, 1024, tc::kSwizzle128B);
+      int nq = 0, np = 0;
+      uint64_t t_idle = 0;
+      while (np < ntiles) {
+        bool progressed = false;
+        if (nq < ntiles && nq <= np + 1) {
+          const int u = 2 * nq;
+          const int slot = u % stages;
+          if (tc::mbar_test_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u)) {
+            tc::tc_fence_after();
+            const uint64_t kdesc =
+                tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, 16, 1024, tc::kSwizzle128B);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // K = 128 channels in steps of 32 bytes
-          tc::umma_f8f6f4(tS(j), kdesc + uint64_t(2 * k), qdesc + uint64_t(2 * k), idesc_qk, k > 0);
-        tc::umma_commit(tc::smem_u32(&ctl.s_full[j & 1]));
-        tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
-      };
-      issue_qk(0);
-      for (int i = 0; i < ntiles && ok; ++i) {
-        if (i + 1 < ntiles) issue_qk(i + 1);
-        if (!ok) break;
-        ok = tc::mbar_wait(tc::smem_u32(&ctl.p_full[i & 1]), uint32_t(i >> 1) & 1u, abort, kWaitLimitNs);
-        const int u = 2 * i + 1;
-        const int slot = u % stages;
-        ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
-        if (!ok) break;
-        tc::tc_fence_after();
-        const uint64_t vdesc =
-            tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, kTileBytes, 1024, tc::kSwizzle128B);
-        const uint64_t pdesc =
-            tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(i & 1) * p_stride, 16, 1024, tc::kSwizzle128B);
+            for (int k = 0; k < 4; ++k)  // K = 128 channels in steps of 32 bytes
+              tc::umma_f8f6f4(tS(nq), kdesc + uint64_t(2 * k), qdesc + uint64_t(2 * k), idesc_qk, k > 0);
+            tc::umma_commit(tc::smem_u32(&ctl.s_full[nq & 1]));
+            tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
+            ++nq;
+            progressed = true;
+          }
+        }
+        if (np < nq) {
+          const int u = 2 * np + 1;
+          const int slot = u % stages;
+          if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[np & 1]), uint32_t(np >> 1) & 1u) &&
+              tc::mbar_test_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u)) {
+            tc::tc_fence_after();
+            const uint64_t vdesc =
+                tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, kTileBytes, 1024, tc::kSwizzle128B);
+            const uint64_t pdesc = tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(np & 1) * p_stride, 16,
+                                                 1024, tc::kSwizzle128B);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V)
-          tc::umma_f8f6f4(tO(i), vdesc + uint64_t(256 * k), pdesc + uint64_t(2 * k), idesc_pv, k > 0);
-        tc::umma_commit(tc::smem_u32(&ctl.o_full[i & 1]));
-        tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
+            for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V)
+              tc::umma_f8f6f4(tO(np), vdesc + uint64_t(256 * k), pdesc + uint64_t(2 * k), idesc_pv, k > 0);
+            tc::umma_commit(tc::smem_u32(&ctl.o_full[np & 1]));
+            tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
+            ++np;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          const uint64_t now = tc::globaltimer_ns();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > kWaitLimitNs || *abort) {
+            *abort = 1;
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) {
         // abort: wait (bounded) until every MMA issued so far has completed
@@ -287,17 +333,23 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     const uint32_t lane_off = uint32_t(qd * 32) << 16;
     const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
     const float scale = p.q_descale[int64_t(b) * p.h_k + g] * kd * p.qk_scale_log2;
-    const int64_t causal_base = int64_t(L) - p.q_len;
-
-    float m_run[NH], l_part[NH], o_acc[NH], alpha_prev[NH];
+    // last visible key of each row (query token t sees keys j <= L - q_len + t)
+    int lim[NR];
 #pragma unroll
-    for (int r = 0; r < NH; ++r) {
+    for (int r = 0; r < NR; ++r)
+      lim[r] = r < nr ? (p.causal ? L - p.q_len + (r0 + r) / p.h_r : INT_MAX) : -1;
+
+    float m_run[NR], l_part[NR], o_acc[NR], alpha_prev[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
       m_run[r] = -INFINITY;
       l_part[r] = 0.f;
       o_acc[r] = 0.f;
       alpha_prev[r] = 1.f;
     }
     bool ok = true;
+    constexpr int kGroup = 32 / NR;  // lanes that share a row after rs_reduce
+    const int my_row = lane / kGroup;
 
     auto absorb = [&](int j) {
       ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[j & 1]), uint32_t(j >> 1) & 1u, abort, kWaitLimitNs);
@@ -308,7 +360,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
       for (int c = 0; c < NPV; c += 16) tc::tmem_ld16(tO(j) + lane_off + c, ov + c);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int r = 0; r < NH; ++r) o_acc[r] = fmaf(o_acc[r], alpha_prev[r], ov[r] + ov[NH + r]);
+      for (int r = 0; r < NR; ++r) o_acc[r] = fmaf(o_acc[r], alpha_prev[r], ov[r] + ov[NH + r]);
     };
 
     for (int i = 0; i < ntiles; ++i) {
@@ -320,29 +372,39 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
       for (int c = 0; c < NQK; c += 16) tc::tmem_ld16(tS(i) + lane_off + c, s + c);
       tc::tmem_wait_ld();
 
-      const int64_t tile0 = k0 + int64_t(i) * kKvTile;
-      const int64_t key = tile0 + x;
-      const bool valid = key < k1;
-      float t[NH];
+      const int tile0 = int(k0) + i * kKvTile;
+      const int key = tile0 + x;
+      const bool valid = key < int(k1);
+      float t[NR], tmp[NR];
 #pragma unroll
-      for (int r = 0; r < NH; ++r) {
-        const int tq = (r0 + r) / p.h_r;
-        const bool vis = valid && r < nr && (!p.causal || key <= causal_base + tq);
-        t[r] = vis ? s[r] * scale : -INFINITY;
-        const float wm = warp_max(t[r]);
-        if (lane == 0) ctl.red[i & 1][qd][r] = wm;
+      for (int r = 0; r < NR; ++r) {
+        t[r] = (valid && key <= lim[r]) ? s[r] * scale : -INFINITY;
+        tmp[r] = t[r];
       }
+      const float wmax = rs_reduce<NR, true>(tmp, lane);
+      if (lane % kGroup == 0) ctl.red[i & 1][qd][my_row] = wmax;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.red_bar[i & 1]));
       ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[i & 1]), uint32_t(i >> 1) & 1u, abort, kWaitLimitNs);
       if (!ok) break;
 
-      float alpha_cur[NH];
+      float tm[NR];
 #pragma unroll
-      for (int r = 0; r < NH; ++r) {
-        const float tm = fmaxf(fmaxf(ctl.red[i & 1][0][r], ctl.red[i & 1][1][r]),
-                               fmaxf(ctl.red[i & 1][2][r], ctl.red[i & 1][3][r]));
-        const float m_new = fmaxf(m_run[r], tm);
+      for (int r = 0; r < NR; r += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(&ctl.red[i & 1][0][r]);
+        const float4 b4 = *reinterpret_cast<const float4*>(&ctl.red[i & 1][1][r]);
+        const float4 c4 = *reinterpret_cast<const float4*>(&ctl.red[i & 1][2][r]);
+        const float4 d4 = *reinterpret_cast<const float4*>(&ctl.red[i & 1][3][r]);
+        tm[r + 0] = fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x));
+        tm[r + 1] = fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y));
+        tm[r + 2] = fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z));
+        tm[r + 3] = fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w));
+      }
+      float alpha_cur[NR];
+      uint8_t* pt = smem + lay.p0 + (i & 1) * p_stride;
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const float m_new = fmaxf(m_run[r], tm[r]);
         float pr = 0.f, alpha = 1.f;
         if (m_new != -INFINITY) {
           alpha = fast_exp2(m_run[r] - m_new);  // 0 when m_run = -inf
@@ -356,11 +418,10 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
         l_part[r] = fmaf(l_part[r], alpha, hi + lo);
         m_run[r] = m_new;
         alpha_cur[r] = alpha;
-        uint8_t* pt = smem + lay.p0 + (i & 1) * p_stride;
         pt[p_byte_offset(r, x)] = uint8_t(hi2 & 0xFF);
         pt[p_byte_offset(NH + r, x)] = uint8_t(lo2 & 0xFF);
       }
-      if (tile0 + kKvTile > k1) {
+      if (tile0 + kKvTile > int(k1)) {
         // last, partial tile: zero the V rows past the end before the PV product
         const int u = 2 * i + 1;
         const int slot = u % stages;
@@ -376,16 +437,18 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
       tc::mbar_arrive(tc::smem_u32(&ctl.p_full[i & 1]));
       if (i > 0) absorb(i - 1);
 #pragma unroll
-      for (int r = 0; r < NH; ++r) alpha_prev[r] = alpha_cur[r];
+      for (int r = 0; r < NR; ++r) alpha_prev[r] = alpha_cur[r];
       if (!ok) break;
     }
     if (ok) absorb(ntiles - 1);
 
     // ---- epilogue --------------------------------------------------------
+    {
+      float tmp[NR];
 #pragma unroll
-    for (int r = 0; r < NH; ++r) {
-      const float ls = warp_sum(l_part[r]);
-      if (lane == 0) ctl.lsum[qd][r] = ls;
+      for (int r = 0; r < NR; ++r) tmp[r] = l_part[r];
+      const float wsum = rs_reduce<NR, false>(tmp, lane);
+      if (lane % kGroup == 0) ctl.lsum[qd][my_row] = wsum;
     }
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.sum_bar));
@@ -394,7 +457,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
       const bool direct = !p.with_reduction || p.n_splits[b] <= 1;
       const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
 #pragma unroll
-      for (int r = 0; r < NH; ++r) {
+      for (int r = 0; r < NR; ++r) {
         if (r >= nr) break;
         const float lr = ctl.lsum[0][r] + ctl.lsum[1][r] + ctl.lsum[2][r] + ctl.lsum[3][r];
         const float on = lr > 0.f ? o_acc[r] / lr : 0.f;
@@ -484,19 +547,19 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   return r == CUDA_SUCCESS;
 }
 
-template <int NQK, int NPV>
+template <int NQK, int NPV, int NR>
 cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
   const TcSmem lay = tc_smem_layout(p.kv_stages, NQK, NPV);
   const int bytes = int(lay.total) + 1024;
   static int configured = 0;  // largest dynamic smem size set so far
   if (bytes > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bytes);
     if (e != cudaSuccess) return e;
     configured = bytes;
   }
   dim3 grid(p.num_work, p.h_k, p.n_row_tiles);
-  decode_tc_kernel<NQK, NPV><<<grid, kThreadsTc, bytes, stream>>>(mk, mv, p);
+  decode_tc_kernel<NQK, NPV, NR><<<grid, kThreadsTc, bytes, stream>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -539,10 +602,11 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
   if (p.num_work == 0) return cudaSuccess;
   // row tile = the plan's tile width (16 or 32 rows)
   if (p.tw <= 16) {
-    if (p.n_q <= 8) return launch_tc<16, 16>(mk, mv, p, stream);
-    return launch_tc<16, 32>(mk, mv, p, stream);
+    if (p.n_q <= 4) return launch_tc<16, 16, 4>(mk, mv, p, stream);
+    if (p.n_q <= 8) return launch_tc<16, 16, 8>(mk, mv, p, stream);
+    return launch_tc<16, 32, 16>(mk, mv, p, stream);
   }
-  return launch_tc<32, 64>(mk, mv, p, stream);
+  return launch_tc<32, 64, 32>(mk, mv, p, stream);
 }
 
 }  // namespace mj

@@ -45,8 +45,9 @@ namespace mj {
 
 namespace {
 
-constexpr int kThreadsTc = 192;
-constexpr int kSoftmaxWarp0 = 2;
+constexpr int kThreadsTc = 224;
+constexpr int kSoftmaxWarp0 = 2;     // warps 2-5: softmax warpgroup
+constexpr int kVProducerWarp = 6;
 constexpr int kTileBytes = kKvTile * 128;  // 128 keys x 128 bytes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -117,7 +118,7 @@ __device__ __forceinline__ uint32_t p_byte_offset(int n, int key) {
 }
 
 template <int NQK, int NPV, int NR>
-__global__ void __launch_bounds__(kThreadsTc, 2)
+__global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
   constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), kTmemCols);
     tc::tmem_relinquish();
   }
-  if (warp >= kSoftmaxWarp0) {
+  if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // Q codes rows r0 .. r0+nr-1 -> Q tile [NQK rows][128 B], K-major, 128-byte
     // swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); other rows 0.
     const int x = tid - kSoftmaxWarp0 * 32;
@@ -202,8 +203,13 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   auto tS = [&](int j) { return tmem + uint32_t((j & 1) * NQK); };
   auto tO = [&](int j) { return tmem + uint32_t(2 * NQK + (j & 1) * NPV); };
 
-  if (warp == 0) {
-    // ======================= TMA producer ===================================
+  if (warp == 0 || warp == kVProducerWarp) {
+    // ======================= TMA producers ==================================
+    // warp 0 loads the K tiles (ring entries u = 2i), warp kVProducerWarp the
+    // V tiles (u = 2i + 1), concurrently: a CTA's TMA issue rate, not HBM,
+    // bounds small-page streaming, and two issuing warps double it.
+    const int half = warp == 0 ? 0 : 1;
+    const CUtensorMap* map = half ? &tmap_v : &tmap_k;
     const uint64_t pol = p.evict_first ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
     const int ps = p.page_size;
     const int ppt = kKvTile / ps;
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
     int64_t batch = -1;
     int entry = -1;
     bool ok = true;
-    int issued = 0;
+    int issued = 0;  // tiles whose load this warp issued
     for (int i = 0; i < ntiles && ok; ++i) {
       // lane j < nvalid issues the load of page j of tile i (one page id per lane)
       const int nvalid = int(min(int64_t(ppt), npages - int64_t(i) * ppt));
@@ -224,36 +230,35 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
         entry = (e0 + lane < npages) ? bt[e0 + lane] : -1;
       }
       const int pg = __shfl_sync(0xFFFFFFFFu, entry, int(e0 - batch) + (lane & 7));
-      if (lane < nvalid && (pg < 0 || int64_t(pg) >= p.num_pages)) atomicOr(p.status, kStatusBadPage);
-      for (int half = 0; half < 2 && ok; ++half) {
-        const int u = 2 * i + half;
-        const int slot = u % stages;
-        const uint32_t round = uint32_t(u / stages);
-        const uint32_t full = tc::smem_u32(&ctl.full[slot]);
-        if (lane == 0) {
-          ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
-          if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_bytes);
-        }
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-        if (ok && lane < nvalid) {
-          const CUtensorMap* map = half ? &tmap_v : &tmap_k;
-          const uint32_t dst = ring_addr + uint32_t(slot) * kTileBytes + uint32_t(lane) * page_bytes;
-          if (p.tma_head_inner)
-            tc::tma_load_4d(dst, map, full, 0, g, 0, pg, pol);
-          else
-            tc::tma_load_4d(dst, map, full, 0, 0, g, pg, pol);
-        }
-        if (ok) ++issued;
-        __syncwarp();
+      if (half == 0 && lane < nvalid && (pg < 0 || int64_t(pg) >= p.num_pages)) atomicOr(p.status, kStatusBadPage);
+      const int u = 2 * i + half;
+      const int slot = u % stages;
+      const uint32_t round = uint32_t(u / stages);
+      const uint32_t full = tc::smem_u32(&ctl.full[slot]);
+      if (lane == 0) {
+        ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
+        if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_bytes);
       }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (ok && lane < nvalid) {
+        const uint32_t dst = ring_addr + uint32_t(slot) * kTileBytes + uint32_t(lane) * page_bytes;
+        if (p.tma_head_inner)
+          tc::tma_load_4d(dst, map, full, 0, g, 0, pg, pol);
+        else
+          tc::tma_load_4d(dst, map, full, 0, 0, g, pg, pol);
+      }
+      if (ok) ++issued;
+      __syncwarp();
     }
     if (!ok && lane == 0) {
-      // abort: wait (bounded) for the loads still in flight before the CTA exits
+      // abort: wait (bounded) for this warp's loads still in flight before the CTA exits
       const uint64_t t0 = tc::globaltimer_ns();
-      for (int u = max(0, issued - stages); u < issued; ++u)
+      for (int i = max(0, issued - stages); i < issued; ++i) {
+        const int u = 2 * i + half;
         while (!tc::mbar_try_wait(tc::smem_u32(&ctl.full[u % stages]), uint32_t(u / stages) & 1u) &&
                tc::globaltimer_ns() - t0 < 100000000ull) {
         }
+      }
     }
   } else if (warp == 1) {
     // ======================= MMA issuer ======================================

@@ -77,6 +77,7 @@ struct Ctrl {
   uint64_t red_bar[2];  // the 4 softmax warps have posted their row maxima
   uint64_t sum_bar;     // ... their row sums
   uint64_t drain;       // MMA drain after an abort
+  uint64_t q_ready;     // the softmax warps have written the Q tile
   uint32_t tmem_base;
   int abort;
   alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
@@ -118,7 +119,7 @@ __device__ __forceinline__ uint32_t p_byte_offset(int n, int key) {
 }
 
 template <int NQK, int NPV, int NR>
-__global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
+__global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
   constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
     }
     tc::mbar_init(tc::smem_u32(&ctl.sum_bar), 4);
     tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
+    tc::mbar_init(tc::smem_u32(&ctl.q_ready), 128);
     ctl.abort = 0;
     tc::fence_mbar_init();
   }
@@ -179,19 +181,6 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), kTmemCols);
     tc::tmem_relinquish();
-  }
-  if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
-    // Q codes rows r0 .. r0+nr-1 -> Q tile [NQK rows][128 B], K-major, 128-byte
-    // swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); other rows 0.
-    const int x = tid - kSoftmaxWarp0 * 32;
-    const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
-    for (int i = x; i < NQK * 8; i += 128) {
-      const int r = i >> 3, c = i & 7;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * kHeadDim + c * 16);
-      *reinterpret_cast<uint4*>(smem + lay.q + r * 128 + ((c ^ (r & 7)) << 4)) = v;
-    }
-    tc::fence_async_smem();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -270,10 +259,10 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
       // tile ahead of PV: two S buffers), and PV_np as soon as P_np is
       // written and V tile np has landed. Neither product waits behind the
       // other's operands.
-      bool ok = true;
+      bool ok = tc::mbar_wait(tc::smem_u32(&ctl.q_ready), 0, abort, kWaitLimitNs);
       int nq = 0, np = 0;
       uint64_t t_idle = 0;
-      while (np < ntiles) {
+      while (ok && np < ntiles) {
         bool progressed = false;
         if (nq < ntiles && nq <= np + 1) {
           const int u = 2 * nq;
@@ -333,6 +322,24 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
     }
   } else {
     // ======================= softmax warpgroup ===============================
+    // Q codes and descales come from the preceding grid (mj_quantize_q) when
+    // it is launched just before: wait for it here only, so that the TMA
+    // producers stream KV meanwhile.
+    tc::grid_dependency_wait();
+    {
+      // Q codes rows r0 .. r0+nr-1 -> Q tile [NQK rows][128 B], K-major,
+      // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); other rows 0.
+      const int xq = tid - kSoftmaxWarp0 * 32;
+      const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
+      for (int i = xq; i < NQK * 8; i += 128) {
+        const int r = i >> 3, c = i & 7;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * kHeadDim + c * 16);
+        *reinterpret_cast<uint4*>(smem + lay.q + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+      }
+      tc::fence_async_smem();
+      tc::mbar_arrive(tc::smem_u32(&ctl.q_ready));
+    }
     const int qd = warp & 3;          // TMEM lane quadrant of this warp
     const int x = qd * 32 + lane;     // key of the tile (S) / channel (O)
     const uint32_t lane_off = uint32_t(qd * 32) << 16;
@@ -360,12 +367,23 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
       ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[j & 1]), uint32_t(j >> 1) & 1u, abort, kWaitLimitNs);
       if (!ok) return;
       tc::tc_fence_after();
-      float ov[NPV];
+      if constexpr (NPV == 16) {
+        float ov[16];  // hi columns 0..NR-1, lo columns NH..NH+NR-1
+        tc::tmem_ld16(tO(j) + lane_off, ov);
+        tc::tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < NPV; c += 16) tc::tmem_ld16(tO(j) + lane_off + c, ov + c);
-      tc::tmem_wait_ld();
+        for (int r = 0; r < NR; ++r) o_acc[r] = fmaf(o_acc[r], alpha_prev[r], ov[r] + ov[NH + r]);
+      } else {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) o_acc[r] = fmaf(o_acc[r], alpha_prev[r], ov[r] + ov[NH + r]);
+        for (int c = 0; c < NR; c += 16) {  // 16 rows at a time: hi and lo columns
+          float hv[16], lv[16];
+          tc::tmem_ld16(tO(j) + lane_off + c, hv);
+          tc::tmem_ld16(tO(j) + lane_off + NH + c, lv);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < 16; ++r) o_acc[c + r] = fmaf(o_acc[c + r], alpha_prev[c + r], hv[r] + lv[r]);
+        }
+      }
     };
 
     for (int i = 0; i < ntiles; ++i) {
@@ -380,12 +398,9 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
       const int tile0 = int(k0) + i * kKvTile;
       const int key = tile0 + x;
       const bool valid = key < int(k1);
-      float t[NR], tmp[NR];
+      float tmp[NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        t[r] = (valid && key <= lim[r]) ? s[r] * scale : -INFINITY;
-        tmp[r] = t[r];
-      }
+      for (int r = 0; r < NR; ++r) tmp[r] = (valid && key <= lim[r]) ? s[r] * scale : -INFINITY;
       const float wmax = rs_reduce<NR, true>(tmp, lane);
       if (lane % kGroup == 0) ctl.red[i & 1][qd][my_row] = wmax;
       __syncwarp();
@@ -410,10 +425,11 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 8 ? 2 : 1))
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         const float m_new = fmaxf(m_run[r], tm[r]);
+        const float tr = (valid && key <= lim[r]) ? s[r] * scale : -INFINITY;
         float pr = 0.f, alpha = 1.f;
         if (m_new != -INFINITY) {
           alpha = fast_exp2(m_run[r] - m_new);  // 0 when m_run = -inf
-          pr = fast_exp2(t[r] - m_new + 8.f);   // <= 256; 0 for masked keys
+          pr = fast_exp2(tr - m_new + 8.f);     // <= 256; 0 for masked keys
         }
         const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(pr, 0.f), __NV_SATFINITE, __NV_E4M3);
         const float hi = e4m3x2_to_float2(hi2).x;
@@ -563,9 +579,17 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
     if (e != cudaSuccess) return e;
     configured = bytes;
   }
-  dim3 grid(p.num_work, p.h_k, p.n_row_tiles);
-  decode_tc_kernel<NQK, NPV, NR><<<grid, kThreadsTc, bytes, stream>>>(mk, mv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_work, p.h_k, p.n_row_tiles);
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = size_t(bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with mj_quantize_q
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR>, mk, mv, p);
 }
 
 }  // namespace

@@ -8,6 +8,10 @@
 // Splits that start at or past seq_lens[b] (a plan made from an upper bound)
 // and rows with no visible key in a split (m = -inf, l = 0) weigh zero; the
 // exponent is never formed from two infinities.
+//
+// One CTA per (request, KV head, query row), one thread per channel: the
+// split weights are computed by as many threads in parallel, and the channel
+// sums read the partials with independent, coalesced loads.
 #include "mj_device.cuh"
 #include "mj_internal.h"
 
@@ -15,8 +19,16 @@ namespace mj {
 
 namespace {
 
-__global__ void __launch_bounds__(kHeadDim) merge_kernel(DecodeParams p) {
-  const int b = blockIdx.x, g = blockIdx.y, c = threadIdx.x;
+constexpr int kMergeThreads = kHeadDim;  // 4 warps
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
+  extern __shared__ float wsh[];  // weights of the live splits
+  __shared__ float red[kMergeThreads / 32];
+  // launched with programmatic stream serialization: the partials are the
+  // preceding decode grid's output
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x, g = blockIdx.y, row = blockIdx.z, c = threadIdx.x;
+  const int warp = c >> 5, lane = c & 31;
   const int ns = min(p.n_splits[b], p.max_splits);
   if (ns <= 1) return;  // single split: the decode kernel wrote the output directly
   const int L = p.seq_lens[b];
@@ -24,37 +36,67 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(DecodeParams p) {
   const int64_t span = int64_t(p.chunk_tiles) * kKvTile;
   const int live = int(min(int64_t(ns), (int64_t(L) + span - 1) / span));  // splits with >= 1 key
 
-  const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
-  for (int row = 0; row < p.n_q; ++row) {
-    float M = -INFINITY;
-    for (int s = 0; s < live; ++s) M = fmaxf(M, p.m_part[part_index(p, b, s, g, row)]);
-    float acc = 0.f, wsum = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < live; ++s) {
-        const int64_t idx = part_index(p, b, s, g, row);
-        const float ms = p.m_part[idx];
-        if (ms == -INFINITY) continue;
-        const float wgt = fast_exp2(ms - M) * p.l_part[idx];
-        acc = fmaf(wgt, p.o_part[idx * kHeadDim + c], acc);
-        wsum += wgt;
-      }
-    }
-    const int tq = row / p.h_r, rr = row % p.h_r, h = g * p.h_r + rr;
-    float val = wsum > 0.f ? acc / wsum * vd : 0.f;
-    if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + c];
-    p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_bf16_bits(val);
-    if (p.lse && c == 0)
-      p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] = wsum > 0.f ? (M + fast_log2(wsum)) * kLn2 : -INFINITY;
+  // max logit over the live splits
+  float mloc = -INFINITY;
+  for (int s = c; s < live; s += kMergeThreads) mloc = fmaxf(mloc, p.m_part[part_index(p, b, s, g, row)]);
+  mloc = warp_max(mloc);
+  if (lane == 0) red[warp] = mloc;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+
+  // split weights
+  float wloc = 0.f;
+  for (int s = c; s < live; s += kMergeThreads) {
+    const int64_t idx = part_index(p, b, s, g, row);
+    const float ms = p.m_part[idx];
+    const float wgt = (M == -INFINITY || ms == -INFINITY) ? 0.f : fast_exp2(ms - M) * p.l_part[idx];
+    wsh[s] = wgt;
+    wloc += wgt;
   }
+  wloc = warp_sum(wloc);
+  if (lane == 0) red[warp] = wloc;
+  __syncthreads();
+  const float wsum = red[0] + red[1] + red[2] + red[3];
+
+  // weighted channel sum
+  const float* op = p.o_part + part_index(p, b, 0, g, row) * kHeadDim + c;
+  const int64_t split_stride = int64_t(p.h_k) * p.n_q * kHeadDim;  // part_index step per split
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int s = 0;
+  for (; s + 4 <= live; s += 4) {
+    a0 = fmaf(wsh[s + 0], op[int64_t(s + 0) * split_stride], a0);
+    a1 = fmaf(wsh[s + 1], op[int64_t(s + 1) * split_stride], a1);
+    a2 = fmaf(wsh[s + 2], op[int64_t(s + 2) * split_stride], a2);
+    a3 = fmaf(wsh[s + 3], op[int64_t(s + 3) * split_stride], a3);
+  }
+  for (; s < live; ++s) a0 = fmaf(wsh[s], op[int64_t(s) * split_stride], a0);
+  const float acc = (a0 + a1) + (a2 + a3);
+
+  const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
+  const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
+  float val = wsum > 0.f ? acc / wsum * vd : 0.f;
+  if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + c];
+  p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_bf16_bits(val);
+  if (p.lse && c == 0)
+    p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] = wsum > 0.f ? (M + fast_log2(wsum)) * kLn2 : -INFINITY;
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   if (!p.with_reduction || p.num_seqs == 0) return cudaSuccess;
-  dim3 grid(p.num_seqs, p.h_k);
-  merge_kernel<<<grid, kHeadDim, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_seqs, p.h_k, p.n_q);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = size_t(p.max_splits) * sizeof(float);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel, p);
 }
 
 }  // namespace mj

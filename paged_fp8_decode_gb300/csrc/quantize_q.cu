@@ -31,6 +31,9 @@ __device__ __forceinline__ float load_x(const QuantParams& p, int b, int g, int 
 }
 
 __global__ void __launch_bounds__(kThreads) quantize_q_kernel(QuantParams p) {
+  // The decode kernel that follows waits for this grid before it reads Q
+  // (griddepcontrol.wait); let it start its KV streaming right away.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   const int g = blockIdx.y;
   const int n = p.q_len * p.h_r * p.d;

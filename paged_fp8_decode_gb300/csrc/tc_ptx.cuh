@@ -89,6 +89,17 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its writes are visible (a no-op without such a grid).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream (launched with programmatic stream
+// serialization) to start before this one completes.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;

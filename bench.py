@@ -51,7 +51,7 @@ DEFAULT_KNOBS = {
     "long_single": (2, 64, 6),
     "spec_verify": (4, 64, 4),
     "spec_verify_noncausal": (4, 64, 4),
-    "fp6_decode": (2, 64, 0),
+    "fp6_decode": (2, 64, 6),
     "tiny": (2, 16, 0),
 }
 

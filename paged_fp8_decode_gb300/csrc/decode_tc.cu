@@ -45,7 +45,9 @@ namespace mj {
 
 namespace {
 
-constexpr int kThreadsTc = 224;
+constexpr int kThreadsTc = 224;      // e4m3 KV: 7 warps
+constexpr int kThreadsTcFp6 = 288;   // packed e2m3 KV: + 2 V-widening warps (7, 8)
+constexpr int kConvWarp0 = 7;
 constexpr int kSoftmaxWarp0 = 2;     // warps 2-5: softmax warpgroup
 constexpr int kVProducerWarp = 6;
 constexpr int kTileBytes = kKvTile * 128;  // 128 keys x 128 bytes
@@ -78,6 +80,7 @@ struct Ctrl {
   uint64_t sum_bar;     // ... their row sums
   uint64_t drain;       // MMA drain after an abort
   uint64_t q_ready;     // the softmax warps have written the Q tile
+  uint64_t vconv[16];   // e2m3 KV: V tile of ring slot s widened to e4m3
   uint32_t tmem_base;
   int abort;
   alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
@@ -118,8 +121,29 @@ __device__ __forceinline__ uint32_t p_byte_offset(int n, int key) {
   return uint32_t(n) * 128u + ((uint32_t((key >> 4) ^ (n & 7))) << 4) + uint32_t(key & 15);
 }
 
-template <int NQK, int NPV, int NR>
-__global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
+// Widen the 16 packed e2m3 codes of a 16-byte shared-memory chunk (12 bytes of
+// little-endian bitstream, 4 bytes of padding, as TMA's 16U6_ALIGN16B type
+// stores them) to 16 e4m3 codes worth 2^-6 times the e2m3 values: per code,
+// the 5 magnitude bits keep their place and the sign moves from bit 5 to bit 7
+// (an e2m3 code read as e4m3 with a zero-extended exponent is exactly 2^-6
+// times its value, subnormals included). Every resulting code is finite.
+__device__ __forceinline__ uint32_t widen4(uint32_t g) {
+  // code k of g sits at bits [6k, 6k + 6): magnitude -> byte k bits 0-4, sign -> bit 7
+  return (g & 0x1Fu) | ((g << 2) & 0x1F80u) | ((g << 4) & 0x1F8000u) | ((g << 6) & 0x1F800000u) |
+         ((g << 8) & 0x80000000u);
+}
+
+__device__ __forceinline__ uint4 widen_chunk(uint4 in) {
+  uint4 o;
+  o.x = widen4(in.x);
+  o.y = widen4(__funnelshift_r(in.x, in.y, 24));
+  o.z = widen4(__funnelshift_r(in.y, in.z, 16));
+  o.w = widen4(in.z >> 8);
+  return o;
+}
+
+template <int NQK, int NPV, int NR, bool FP6>
+__global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 2 : 1))
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
   constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
@@ -171,6 +195,8 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
     tc::mbar_init(tc::smem_u32(&ctl.sum_bar), 4);
     tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
     tc::mbar_init(tc::smem_u32(&ctl.q_ready), 128);
+    if (FP6)
+      for (int s = 0; s < stages; ++s) tc::mbar_init(tc::smem_u32(&ctl.vconv[s]), 64);
     ctl.abort = 0;
     tc::fence_mbar_init();
   }
@@ -205,7 +231,8 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
     const int64_t first_page = k0 / ps;
     const int64_t npages = (k1 + ps - 1) / ps - first_page;
     const int32_t* bt = p.block_table + int64_t(b) * p.bt_stride + first_page;
-    const uint32_t page_bytes = uint32_t(ps) * 128u;
+    const uint32_t page_bytes = uint32_t(ps) * 128u;                 // shared-memory footprint
+    const uint32_t page_tx = uint32_t(ps) * uint32_t(p.row_bytes);  // bytes the copy delivers
     int64_t batch = -1;
     int entry = -1;
     bool ok = true;
@@ -226,7 +253,7 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
       const uint32_t full = tc::smem_u32(&ctl.full[slot]);
       if (lane == 0) {
         ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
-        if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_bytes);
+        if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_tx);
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
       if (ok && lane < nvalid) {
@@ -249,10 +276,28 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
         }
       }
     }
+  } else if (FP6 && warp >= kConvWarp0) {
+    // ======================= V widening (e2m3 KV) ============================
+    // Each V tile is widened in place, chunk by chunk, once its load lands.
+    const int ct = tid - kConvWarp0 * 32;  // 0..63
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const int u = 2 * i + 1;
+      const int slot = u % stages;
+      ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
+      if (!ok) break;
+      uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kTileBytes);
+#pragma unroll 4
+      for (int k = ct; k < kTileBytes / 16; k += 64) tile[k] = widen_chunk(tile[k]);
+      tc::fence_async_smem();
+      tc::mbar_arrive(tc::smem_u32(&ctl.vconv[slot]));
+    }
   } else if (warp == 1) {
     // ======================= MMA issuer ======================================
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false);
+      // K is read as e2m3 straight from the packed TMA layout (kind::f8f6f4
+      // mixes an e2m3 A with the e4m3 Q); V always arrives as e4m3.
+      constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false) | (FP6 ? (3u << 7) : 0u);
       constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, false);
       const uint64_t qdesc = tc::smem_desc(q_addr, 16, 1024, tc::kSwizzle128B);
       // Event loop: issue QK_nq as soon as K tile nq has landed (at most one
@@ -283,8 +328,9 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
         if (np < nq) {
           const int u = 2 * np + 1;
           const int slot = u % stages;
+          const uint32_t vbar = tc::smem_u32(FP6 ? &ctl.vconv[slot] : &ctl.full[slot]);
           if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[np & 1]), uint32_t(np >> 1) & 1u) &&
-              tc::mbar_test_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u)) {
+              tc::mbar_test_wait(vbar, uint32_t(u / stages) & 1u)) {
             tc::tc_fence_after();
             const uint64_t vdesc =
                 tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, kTileBytes, 1024, tc::kSwizzle128B);
@@ -442,8 +488,9 @@ __global__ void __launch_bounds__(kThreadsTc, (NR <= 16 ? 2 : 1))
         pt[p_byte_offset(r, x)] = uint8_t(hi2 & 0xFF);
         pt[p_byte_offset(NH + r, x)] = uint8_t(lo2 & 0xFF);
       }
-      if (tile0 + kKvTile > int(k1)) {
+      if (!FP6 && tile0 + kKvTile > int(k1)) {
         // last, partial tile: zero the V rows past the end before the PV product
+        // (widened e2m3 codes are always finite, so e2m3 needs no zeroing)
         const int u = 2 * i + 1;
         const int slot = u % stages;
         ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
@@ -537,7 +584,7 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
                    bool head_inner) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const int64_t sh_eff = p.h_k == 1 ? (head_inner ? 16 : sp) : sh;
+  const int64_t sh_eff = p.h_k == 1 ? (head_inner ? 32 : sp) : sh;
   cuuint64_t dims[4];
   cuuint64_t strides[3];
   cuuint32_t box[4];
@@ -562,26 +609,31 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   dims[3] = cuuint64_t(p.num_pages);
   strides[2] = cuuint64_t(sp);
   box[3] = 1;
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+  // e4m3: one byte per element. Packed e2m3: 16U6_ALIGN16B keeps 16 codes in
+  // 12 bytes and lands each group in a 16-byte shared-memory chunk (4 bytes of
+  // padding), which tcgen05.mma reads as e2m3; dims[0] counts codes (128).
+  const CUtensorMapDataType dt =
+      p.kv_format == MJ_KV_E2M3 ? CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int NQK, int NPV, int NR>
+template <int NQK, int NPV, int NR, bool FP6>
 cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
   const TcSmem lay = tc_smem_layout(p.kv_stages, NQK, NPV);
   const int bytes = int(lay.total) + 1024;
   static int configured = 0;  // largest dynamic smem size set so far
   if (bytes > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bytes);
     if (e != cudaSuccess) return e;
     configured = bytes;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_work, p.h_k, p.n_row_tiles);
-  cfg.blockDim = dim3(kThreadsTc);
+  cfg.blockDim = dim3(FP6 ? kThreadsTcFp6 : kThreadsTc);
   cfg.dynamicSmemBytes = size_t(bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -589,7 +641,7 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR>, mk, mv, p);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6>, mk, mv, p);
 }
 
 }  // namespace
@@ -597,7 +649,15 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
 int tc_default_stages() { return 6; }
 
 bool tc_supported(const DecodeParams& p) {
-  if (p.kv_format != MJ_KV_E4M3) return false;
+  if (p.kv_format == MJ_KV_E2M3) {
+    // the packed TMA type wants 32-byte aligned strides (and base, checked
+    // by the ABI for e2m3)
+    const int64_t st[] = {p.k_sp, p.k_st, p.k_sh, p.v_sp, p.v_st, p.v_sh};
+    for (int64_t v : st)
+      if (v % 32) return false;
+  } else if (p.kv_format != MJ_KV_E4M3) {
+    return false;
+  }
   if (p.n_q > 32 && p.tw != 32) return false;
   if (p.num_pages > INT32_MAX || p.h_k > 65535) return false;
   const int64_t sm[] = {p.k_sp, p.v_sp};
@@ -630,12 +690,23 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
   }
   if (p.num_work == 0) return cudaSuccess;
   // row tile = the plan's tile width (16 or 32 rows)
-  if (p.tw <= 16) {
-    if (p.n_q <= 4) return launch_tc<16, 16, 4>(mk, mv, p, stream);
-    if (p.n_q <= 8) return launch_tc<16, 16, 8>(mk, mv, p, stream);
-    return launch_tc<16, 32, 16>(mk, mv, p, stream);
+  if (p.kv_format == MJ_KV_E2M3) {
+    // K enters the MMA as true e2m3 values (no 2^-6 widening factor); V is
+    // widened in shared memory and keeps the factor in v_fmt.
+    p.qk_scale_log2 *= 1.0f / 64.0f;
+    if (p.tw <= 16) {
+      if (p.n_q <= 4) return launch_tc<16, 16, 4, true>(mk, mv, p, stream);
+      if (p.n_q <= 8) return launch_tc<16, 16, 8, true>(mk, mv, p, stream);
+      return launch_tc<16, 32, 16, true>(mk, mv, p, stream);
+    }
+    return launch_tc<32, 64, 32, true>(mk, mv, p, stream);
   }
-  return launch_tc<32, 64, 32>(mk, mv, p, stream);
+  if (p.tw <= 16) {
+    if (p.n_q <= 4) return launch_tc<16, 16, 4, false>(mk, mv, p, stream);
+    if (p.n_q <= 8) return launch_tc<16, 16, 8, false>(mk, mv, p, stream);
+    return launch_tc<16, 32, 16, false>(mk, mv, p, stream);
+  }
+  return launch_tc<32, 64, 32, false>(mk, mv, p, stream);
 }
 
 }  // namespace mj

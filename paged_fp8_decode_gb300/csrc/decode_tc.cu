@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
                      DecodeParams p) {
   constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
   static_assert(NH <= NQK && NR <= NH && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
-  constexpr uint32_t kTmemCols = (2 * (NQK + NPV) <= 64) ? 64 : (2 * (NQK + NPV) <= 128 ? 128 : 256);
+  // TMEM: two S buffers (NQK columns each), one O accumulator (NPV columns)
+  constexpr uint32_t kTmemCols = (2 * NQK + NPV <= 64) ? 64 : (2 * NQK + NPV <= 128 ? 128 : 256);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -214,9 +215,9 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort = &ctl.abort;
 
-  // TMEM columns: S buffers at [0, NQK) and [NQK, 2 NQK), O buffers after them
+  // TMEM columns: S buffers at [0, NQK) and [NQK, 2 NQK), the O accumulator after them
   auto tS = [&](int j) { return tmem + uint32_t((j & 1) * NQK); };
-  auto tO = [&](int j) { return tmem + uint32_t(2 * NQK + (j & 1) * NPV); };
+  const uint32_t tO = tmem + uint32_t(2 * NQK);
 
   if (warp == 0 || warp == kVProducerWarp) {
     // ======================= TMA producers ==================================
@@ -298,7 +299,8 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       // K is read as e2m3 straight from the packed TMA layout (kind::f8f6f4
       // mixes an e2m3 A with the e4m3 Q); V always arrives as e4m3.
       constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false) | (FP6 ? (3u << 7) : 0u);
-      constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, false);
+      // PV: A = V tile (MN-major), B = P (MN-major, no swizzle: [key][16 columns] blocks)
+      constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, true);
       const uint64_t qdesc = tc::smem_desc(q_addr, 16, 1024, tc::kSwizzle128B);
       // Event loop: issue QK_nq as soon as K tile nq has landed (at most one
       // tile ahead of PV: two S buffers), and PV_np as soon as P_np is
@@ -334,11 +336,13 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
             tc::tc_fence_after();
             const uint64_t vdesc =
                 tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, kTileBytes, 1024, tc::kSwizzle128B);
-            const uint64_t pdesc = tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(np & 1) * p_stride, 16,
-                                                 1024, tc::kSwizzle128B);
+            // P, MN-major without swizzle: 8-key core groups 128 B apart (LBO),
+            // 16-column blocks 2 KB apart (SBO)
+            const uint64_t pdesc =
+                tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(np & 1) * p_stride, 128, 2048, 0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V)
-              tc::umma_f8f6f4(tO(np), vdesc + uint64_t(256 * k), pdesc + uint64_t(2 * k), idesc_pv, k > 0);
+            for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V, 32 x 16 B of P)
+              tc::umma_f8f6f4(tO, vdesc + uint64_t(256 * k), pdesc + uint64_t(32 * k), idesc_pv, (np > 0 || k > 0));
             tc::umma_commit(tc::smem_u32(&ctl.o_full[np & 1]));
             tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
             ++np;
@@ -397,40 +401,20 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
     for (int r = 0; r < NR; ++r)
       lim[r] = r < nr ? (p.causal ? L - p.q_len + (r0 + r) / p.h_r : INT_MAX) : -1;
 
-    float m_run[NR], l_part[NR], o_acc[NR], alpha_prev[NR];
+    // m_ref: the reference max each row's P is scaled by; it only moves when a
+    // tile's max exceeds it by more than kTau (log2 units), and then O (kept
+    // in TMEM across tiles) is rescaled in place. P = 2^(t - m_ref + 8) stays
+    // <= 2^(8 + kTau) < 448, so both e4m3 terms of P stay finite.
+    constexpr float kTau = 0.6f;
+    float m_ref[NR], l_part[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      m_run[r] = -INFINITY;
+      m_ref[r] = -INFINITY;
       l_part[r] = 0.f;
-      o_acc[r] = 0.f;
-      alpha_prev[r] = 1.f;
     }
     bool ok = true;
     constexpr int kGroup = 32 / NR;  // lanes that share a row after rs_reduce
     const int my_row = lane / kGroup;
-
-    auto absorb = [&](int j) {
-      ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[j & 1]), uint32_t(j >> 1) & 1u, abort, kWaitLimitNs);
-      if (!ok) return;
-      tc::tc_fence_after();
-      if constexpr (NPV == 16) {
-        float ov[16];  // hi columns 0..NR-1, lo columns NH..NH+NR-1
-        tc::tmem_ld16(tO(j) + lane_off, ov);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int r = 0; r < NR; ++r) o_acc[r] = fmaf(o_acc[r], alpha_prev[r], ov[r] + ov[NH + r]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < NR; c += 16) {  // 16 rows at a time: hi and lo columns
-          float hv[16], lv[16];
-          tc::tmem_ld16(tO(j) + lane_off + c, hv);
-          tc::tmem_ld16(tO(j) + lane_off + NH + c, lv);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int r = 0; r < 16; ++r) o_acc[c + r] = fmaf(o_acc[c + r], alpha_prev[c + r], hv[r] + lv[r]);
-        }
-      }
-    };
 
     for (int i = 0; i < ntiles; ++i) {
       ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.s_full[i & 1]), uint32_t(i >> 1) & 1u, abort, kWaitLimitNs);
@@ -454,40 +438,81 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[i & 1]), uint32_t(i >> 1) & 1u, abort, kWaitLimitNs);
       if (!ok) break;
 
-      float tm[NR];
+      // new reference maxima (the same decision in every thread)
+      float alpha[NR];
+      bool rescale = false;
 #pragma unroll
       for (int r = 0; r < NR; r += 4) {
         const float4 a = *reinterpret_cast<const float4*>(&ctl.red[i & 1][0][r]);
         const float4 b4 = *reinterpret_cast<const float4*>(&ctl.red[i & 1][1][r]);
         const float4 c4 = *reinterpret_cast<const float4*>(&ctl.red[i & 1][2][r]);
         const float4 d4 = *reinterpret_cast<const float4*>(&ctl.red[i & 1][3][r]);
-        tm[r + 0] = fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x));
-        tm[r + 1] = fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y));
-        tm[r + 2] = fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z));
-        tm[r + 3] = fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w));
+        const float tm[4] = {fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x)), fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y)),
+                             fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z)), fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w))};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          alpha[r + j] = 1.f;
+          if (tm[j] > m_ref[r + j] + kTau) {  // false for -inf tiles
+            alpha[r + j] = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
+            rescale |= m_ref[r + j] != -INFINITY;
+            m_ref[r + j] = tm[j];
+            l_part[r + j] *= alpha[r + j];
+          }
+        }
       }
-      float alpha_cur[NR];
+      if (rescale) {
+        // O holds the PV sums up to tile i-1, scaled by the old references:
+        // wait for the last of them and rescale O in TMEM before PV_i.
+        ok = tc::mbar_wait(tc::smem_u32(&ctl.o_full[(i - 1) & 1]), uint32_t((i - 1) >> 1) & 1u, abort,
+                           kWaitLimitNs);
+        if (!ok) break;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NPV; c += 16) {
+          float v[16];
+          tc::tmem_ld16(tO + lane_off + c, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c + j;
+            const int r = col < NH ? col : col - NH;  // hi column r, lo column NH + r
+            if (r < NR) v[j] *= alpha[r];
+          }
+          tc::tmem_st16(tO + lane_off + c, v);
+        }
+        tc::tmem_wait_st();
+      }
+
+      // P = 2^(t - m_ref + 8) as hi + lo e4m3 terms; this key's column of
+      // P^T: hi of row r at byte r, lo at byte NH + r of the key's 16-byte
+      // chunk in 16-column block (byte / 16).
+      uint32_t words[NPV / 4];
+#pragma unroll
+      for (int w2 = 0; w2 < NPV / 4; ++w2) words[w2] = 0u;
+#pragma unroll
+      for (int r = 0; r < NR; r += 2) {
+        float pr[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float tr = (valid && key <= lim[r + j]) ? s[r + j] * scale : -INFINITY;
+          pr[j] = m_ref[r + j] == -INFINITY ? 0.f : fast_exp2(tr - m_ref[r + j] + 8.f);
+        }
+        const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(pr[0], pr[1]), __NV_SATFINITE, __NV_E4M3);
+        const float2 hf = e4m3x2_to_float2(hi2);
+        const __nv_fp8x2_storage_t lo2 =
+            __nv_cvt_float2_to_fp8x2(make_float2(pr[0] - hf.x, pr[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
+        const float2 lf = e4m3x2_to_float2(lo2);
+        l_part[r] += hf.x + lf.x;
+        l_part[r + 1] += hf.y + lf.y;
+        words[r / 4] |= uint32_t(hi2) << ((r % 4) * 8);
+        words[(NH + r) / 4] |= uint32_t(lo2) << (((NH + r) % 4) * 8);
+      }
       uint8_t* pt = smem + lay.p0 + (i & 1) * p_stride;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float m_new = fmaxf(m_run[r], tm[r]);
-        const float tr = (valid && key <= lim[r]) ? s[r] * scale : -INFINITY;
-        float pr = 0.f, alpha = 1.f;
-        if (m_new != -INFINITY) {
-          alpha = fast_exp2(m_run[r] - m_new);  // 0 when m_run = -inf
-          pr = fast_exp2(tr - m_new + 8.f);     // <= 256; 0 for masked keys
-        }
-        const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(pr, 0.f), __NV_SATFINITE, __NV_E4M3);
-        const float hi = e4m3x2_to_float2(hi2).x;
-        const __nv_fp8x2_storage_t lo2 =
-            __nv_cvt_float2_to_fp8x2(make_float2(pr - hi, 0.f), __NV_SATFINITE, __NV_E4M3);
-        const float lo = e4m3x2_to_float2(lo2).x;
-        l_part[r] = fmaf(l_part[r], alpha, hi + lo);
-        m_run[r] = m_new;
-        alpha_cur[r] = alpha;
-        pt[p_byte_offset(r, x)] = uint8_t(hi2 & 0xFF);
-        pt[p_byte_offset(NH + r, x)] = uint8_t(lo2 & 0xFF);
-      }
+      for (int bk = 0; bk < NPV / 16; ++bk)
+        *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
+            make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
+
       if (!FP6 && tile0 + kKvTile > int(k1)) {
         // last, partial tile: zero the V rows past the end before the PV product
         // (widened e2m3 codes are always finite, so e2m3 needs no zeroing)
@@ -503,12 +528,29 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       tc::fence_async_smem();
       tc::tc_fence_before();
       tc::mbar_arrive(tc::smem_u32(&ctl.p_full[i & 1]));
-      if (i > 0) absorb(i - 1);
-#pragma unroll
-      for (int r = 0; r < NR; ++r) alpha_prev[r] = alpha_cur[r];
       if (!ok) break;
     }
-    if (ok) absorb(ntiles - 1);
+    // the final O: wait for the last PV product
+    float o_acc[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) o_acc[r] = 0.f;
+    ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[(ntiles - 1) & 1]), uint32_t((ntiles - 1) >> 1) & 1u, abort,
+                             kWaitLimitNs);
+    if (ok) {
+      tc::tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < NPV; c += 16) {
+        float v[16];
+        tc::tmem_ld16(tO + lane_off + c, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c + j;
+          const int r = col < NH ? col : col - NH;
+          if (r < NR) o_acc[r] += v[j];
+        }
+      }
+    }
 
     // ---- epilogue --------------------------------------------------------
     {
@@ -537,12 +579,12 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
           p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + x] = float_to_bf16_bits(val);
           if (p.lse && x == 0)
             p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
-                lr > 0.f ? (m_run[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
+                lr > 0.f ? (m_ref[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
         } else {
           const int64_t idx = part_index(p, b, w.w, g, row);
           p.o_part[idx * kHeadDim + x] = on;
           if (x == 0) {
-            p.m_part[idx] = lr > 0.f ? m_run[r] : -INFINITY;
+            p.m_part[idx] = lr > 0.f ? m_ref[r] : -INFINITY;
             p.l_part[idx] = lr * (1.f / 256.f);
           }
         }

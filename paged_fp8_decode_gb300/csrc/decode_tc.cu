@@ -765,10 +765,16 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
   }
   if (p.kv_stages <= 0) p.kv_stages = tc_default_stages();
   if (p.kv_stages > tc_max_stages()) p.kv_stages = tc_max_stages();
-  // The tile-pair variants (up to 8 query rows) run with an even ring depth
-  // only: an odd depth (5) faulted in two benchmark runs whose cause was not
-  // found (a self-checking build did not reproduce it), so it is not offered.
-  if (p.n_q <= 8 && (p.kv_stages & 1)) p.kv_stages = p.kv_stages > 2 ? p.kv_stages - 1 : 2;
+  // The ring depth is always even, so that K tiles (ring entries u = 2i) and
+  // V tiles (u = 2i + 1) never share a slot. Every waiter on full[slot] must
+  // know that the slot's previous occupant has landed: a phase-parity wait
+  // for the k-th use of a barrier passes wrongly while use k - 1 is still
+  // pending. With K-only and V-only slots the previous occupant of a K (V)
+  // slot is an earlier K (V) tile that the MMA issuer (or the V-widening
+  // warps) has already consumed in order. With an odd depth a K slot's
+  // previous occupant is a V tile, which the issuer's look-ahead QK probe (up
+  // to three tiles ahead of PV) can reach before it has landed.
+  if (p.kv_stages & 1) p.kv_stages = p.kv_stages > 2 ? p.kv_stages - 1 : 2;
   p.tma_head_inner = (p.k_sh < p.k_st) ? 1 : 0;
   if (((p.v_sh < p.v_st) ? 1 : 0) != p.tma_head_inner) {
     *unsupported = true;

@@ -25,9 +25,9 @@
 //   P is scaled by 2^8 (p = 2^(t - m + 8) <= 256) so that its e4m3 terms stay
 //   normal well into the tail of the softmax; the factor cancels in O / l.
 // * Keys at or past the device seq_len are masked by select on S; in a
-//   request's last, partial tile the softmax warps also zero the V rows past
-//   the end before the PV product (page tails may hold NaN codes, and 0 * NaN
-//   would reach O through the MMA).
+//   request's last, partial tile the V producer warp also zeroes the V rows
+//   past the end before the PV product (page tails may hold NaN codes, and
+//   0 * NaN would reach O through the MMA).
 // * Every wait is bounded (2 s); a timeout raises a status bit and the CTA
 //   unwinds, frees its TMEM and returns.
 #include <cuda.h>
@@ -82,6 +82,7 @@ struct Ctrl {
   uint64_t drain;       // MMA drain after an abort
   uint64_t q_ready;     // the softmax warps have written the Q tile
   uint64_t vconv[16];   // e2m3 KV: V tile of ring slot s widened to e4m3
+  uint64_t v_tail;      // e4m3 KV: the last, partial V tile has its rows past the end zeroed
   uint32_t tmem_base;
   int abort;
   alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
@@ -176,6 +177,8 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
   const int nr = min(min(p.tw, p.n_q - r0), NR);
   if (nr <= 0) return;
   const int ntiles = int((k1 - k0 + kKvTile - 1) / kKvTile);
+  // the last tile ends before k0 + ntiles * 128: its V rows past the end get zeroed
+  const bool last_partial = k0 + int64_t(ntiles) * kKvTile > k1;
   const int stages = p.kv_stages;
 
   const TcSmem lay = tc_smem_layout(stages, NQK, NPV, NSB);
@@ -201,6 +204,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
     tc::mbar_init(tc::smem_u32(&ctl.sum_bar), 4);
     tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
     tc::mbar_init(tc::smem_u32(&ctl.q_ready), 128);
+    tc::mbar_init(tc::smem_u32(&ctl.v_tail), 1);
     if (FP6)
       for (int s = 0; s < stages; ++s) tc::mbar_init(tc::smem_u32(&ctl.vconv[s]), 64);
     ctl.abort = 0;
@@ -275,6 +279,25 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       if (ok) ++issued;
       __syncwarp();
     }
+    if (!FP6 && half == 1 && ok && last_partial) {
+      // Last, partial V tile: zero its rows past the end (page tails and
+      // stale ring contents may hold NaN codes, and 0 * NaN would reach O
+      // through the PV product), then release it to the MMA issuer. This warp
+      // may wait on the slot's full barrier: its own wait on the slot's empty
+      // barrier showed that the previous occupant has landed and been consumed.
+      const int u = 2 * (ntiles - 1) + 1;
+      const int slot = u % stages;
+      if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (ok) {
+        const int first_dead = int(k1 - (k0 + int64_t(ntiles - 1) * kKvTile));  // rows >= this are past the end
+        uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kTileBytes);
+        for (int c = first_dead * 8 + lane; c < kKvTile * 8; c += 32) tile[c] = make_uint4(0u, 0u, 0u, 0u);
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.v_tail));
+      }
+    }
     if (!ok && lane == 0) {
       // abort: wait (bounded) for this warp's loads still in flight before the CTA exits
       const uint64_t t0 = tc::globaltimer_ns();
@@ -338,9 +361,12 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
         if (np < nq) {
           const int u = 2 * np + 1;
           const int slot = u % stages;
-          const uint32_t vbar = tc::smem_u32(FP6 ? &ctl.vconv[slot] : &ctl.full[slot]);
-          if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[bs(np)]), bp(np)) &&
-              tc::mbar_test_wait(vbar, uint32_t(u / stages) & 1u)) {
+          // V tile ready: widened (e2m3), tail-zeroed (last partial e4m3 tile, a
+          // one-shot barrier), else landed
+          const bool tail = !FP6 && last_partial && np == ntiles - 1;
+          const uint32_t vbar = tc::smem_u32(FP6 ? &ctl.vconv[slot] : (tail ? &ctl.v_tail : &ctl.full[slot]));
+          const uint32_t vpar = tail ? 0u : uint32_t(u / stages) & 1u;
+          if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[bs(np)]), bp(np)) && tc::mbar_test_wait(vbar, vpar)) {
             tc::tc_fence_after();
             const uint64_t vdesc =
                 tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, kTileBytes, 1024, tc::kSwizzle128B);
@@ -556,19 +582,6 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
           *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
               make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
 
-        const int tile0 = int(k0) + (i + a) * kKvTile;
-        if (!FP6 && tile0 + kKvTile > int(k1)) {
-          // last, partial tile: zero the V rows past the end before the PV product
-          // (widened e2m3 codes are always finite, so e2m3 needs no zeroing)
-          const int u = 2 * (i + a) + 1;
-          const int slot = u % stages;
-          ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
-          if (ok && !valid[a]) {
-            uint4* row = reinterpret_cast<uint4*>(smem + lay.ring + slot * kTileBytes + x * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
       }
       tc::fence_async_smem();
       tc::tc_fence_before();

@@ -36,6 +36,7 @@
 #include <climits>
 #include <cstddef>
 #include <mutex>
+#include <type_traits>
 
 #include "mj_device.cuh"
 #include "mj_internal.h"
@@ -46,7 +47,12 @@ namespace mj {
 namespace {
 
 constexpr int kThreadsTc = 224;      // e4m3 KV: 7 warps
-constexpr int kThreadsTcFp6 = 288;   // packed e2m3 KV: + 2 V-widening warps (7, 8)
+// packed e2m3 KV: + 3 V-widening warps (7-9). With warps 2-5 on the four SM
+// sub-partitions, the widening work then spreads over three of them rather
+// than two (two CTAs per SM keep at most five warps per sub-partition either
+// way, so the register budget is the same).
+constexpr int kThreadsTcFp6 = 320;
+constexpr int kConvThreads = kThreadsTcFp6 - 7 * 32;
 constexpr int kConvWarp0 = 7;
 constexpr int kSoftmaxWarp0 = 2;     // warps 2-5: softmax warpgroup
 constexpr int kVProducerWarp = 6;
@@ -87,6 +93,7 @@ struct Ctrl {
   int abort;
   alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
   alignas(16) float lsum[4][32];    // row sums of the 4 softmax warps
+  float alpha[4][32];               // per softmax warp: the rescale factors of the current tiles
 };
 static_assert(sizeof(Ctrl) <= 3072, "control block");
 static_assert(offsetof(Ctrl, red) % 16 == 0 && offsetof(Ctrl, lsum) % 16 == 0, "float4 access to red/lsum");
@@ -160,8 +167,11 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int g = blockIdx.y;
-  const int4 w = reinterpret_cast<const int4*>(p.work)[blockIdx.x];
+  // CTA x = (work row, KV head) with the head fastest: the CTAs that run
+  // together stream the same requests' pages (with token-major layouts the
+  // heads of a page interleave, so they share DRAM rows)
+  const int g = int(blockIdx.x % unsigned(p.h_k));
+  const int4 w = reinterpret_cast<const int4*>(p.work)[blockIdx.x / unsigned(p.h_k)];
   const int b = w.x;
   if (w.z <= w.y || b < 0 || b >= p.num_seqs) return;
   if (p.with_reduction && (w.w < 0 || w.w >= p.max_splits || b >= p.part_seqs)) {
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
   const int64_t k0 = int64_t(w.y) * kKvTile;
   const int64_t k1 = min(int64_t(w.z) * kKvTile, int64_t(L));
   if (k1 <= k0) return;
-  const int r0 = blockIdx.z * p.tw;
+  const int r0 = blockIdx.y * p.tw;
   const int nr = min(min(p.tw, p.n_q - r0), NR);
   if (nr <= 0) return;
   const int ntiles = int((k1 - k0 + kKvTile - 1) / kKvTile);
@@ -206,7 +216,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
     tc::mbar_init(tc::smem_u32(&ctl.q_ready), 128);
     tc::mbar_init(tc::smem_u32(&ctl.v_tail), 1);
     if (FP6)
-      for (int s = 0; s < stages; ++s) tc::mbar_init(tc::smem_u32(&ctl.vconv[s]), 64);
+      for (int s = 0; s < stages; ++s) tc::mbar_init(tc::smem_u32(&ctl.vconv[s]), kConvThreads);
     ctl.abort = 0;
     tc::fence_mbar_init();
   }
@@ -311,7 +321,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
   } else if (FP6 && warp >= kConvWarp0) {
     // ======================= V widening (e2m3 KV) ============================
     // Each V tile is widened in place, chunk by chunk, once its load lands.
-    const int ct = tid - kConvWarp0 * 32;  // 0..63
+    const int ct = tid - kConvWarp0 * 32;  // 0 .. kConvThreads - 1
     bool ok = true;
     for (int i = 0; i < ntiles && ok; ++i) {
       const int u = 2 * i + 1;
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       if (!ok) break;
       uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kTileBytes);
 #pragma unroll 4
-      for (int k = ct; k < kTileBytes / 16; k += 64) tile[k] = widen_chunk(tile[k]);
+      for (int k = ct; k < kTileBytes / 16; k += kConvThreads) tile[k] = widen_chunk(tile[k]);
       tc::fence_async_smem();
       tc::mbar_arrive(tc::smem_u32(&ctl.vconv[slot]));
     }
@@ -434,6 +444,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
 #pragma unroll
     for (int r = 0; r < NR; ++r)
       lim[r] = r < nr ? (p.causal ? L - p.q_len + (r0 + r) / p.h_r : INT_MAX) : -1;
+    const int lim_min = lim[0];  // the tile's first row has the smallest limit
 
     // m_ref: the reference max each row's P is scaled by; it only moves when a
     // tile's max exceeds it by more than kTau (log2 units), and then O (kept
@@ -456,7 +467,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
     // interleaves.
     for (int i = 0; i < ntiles; i += TP) {
       const int nt = min(TP, ntiles - i);
-      float s[TP][NQK];
+      float s[TP][NR];  // S columns of the real rows only
 #pragma unroll
       for (int a = 0; a < TP; ++a) {
         if (a < nt) {
@@ -468,11 +479,10 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
 #pragma unroll
       for (int a = 0; a < TP; ++a) {
         if (a < nt) {
-#pragma unroll
-          for (int c = 0; c < NQK; c += 16) tc::tmem_ld16(tS(i + a) + lane_off + c, s[a] + c);
+          tc::tmem_ld_cols<NR>(tS(i + a) + lane_off, s[a]);
         } else {
 #pragma unroll
-          for (int c = 0; c < NQK; ++c) s[a][c] = -INFINITY;
+          for (int c = 0; c < NR; ++c) s[a][c] = -INFINITY;
         }
       }
       tc::tmem_wait_ld();
@@ -484,14 +494,30 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
         key[a] = int(k0) + (i + a) * kKvTile + x;
         valid[a] = a < nt && key[a] < int(k1);
       }
+      // Every key of the iteration visible to every row (the common case:
+      // no tile past the end, no causal limit inside): no per-row masks.
+      // Rows past nr then see S = 0 (their Q rows are zero); their P only
+      // reaches O columns that are never written out.
+      const int64_t it_end = k0 + int64_t(i + nt) * kKvTile;  // one past the iteration's last key
+      const bool all_vis = nt == TP && it_end <= k1 && it_end - 1 <= int64_t(lim_min);
       float tmp[NR];
+      if (all_vis) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        float v = -INFINITY;
+        for (int r = 0; r < NR; ++r) {
+          float v = s[0][r] * scale;
 #pragma unroll
-        for (int a = 0; a < TP; ++a)
-          v = fmaxf(v, (valid[a] && key[a] <= lim[r]) ? s[a][r] * scale : -INFINITY);
-        tmp[r] = v;
+          for (int a = 1; a < TP; ++a) v = fmaxf(v, s[a][r] * scale);
+          tmp[r] = v;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          float v = -INFINITY;
+#pragma unroll
+          for (int a = 0; a < TP; ++a)
+            v = fmaxf(v, (valid[a] && key[a] <= lim[r]) ? s[a][r] * scale : -INFINITY);
+          tmp[r] = v;
+        }
       }
       const int xi = i / TP;  // exchange sequence number
       const float wmax = rs_reduce<NR, true>(tmp, lane);
@@ -502,7 +528,6 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       if (!ok) break;
 
       // new reference maxima (the same decision in every thread)
-      float alpha[NR];
       bool rescale = false;
 #pragma unroll
       for (int r = 0; r < NR; r += 4) {
@@ -514,20 +539,74 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
                              fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z)), fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w))};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          alpha[r + j] = 1.f;
+          float alpha = 1.f;
           if (tm[j] > m_ref[r + j] + kTau) {  // false for -inf tiles
-            alpha[r + j] = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
+            alpha = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
             rescale |= m_ref[r + j] != -INFINITY;
             m_ref[r + j] = tm[j];
-            l_part[r + j] *= alpha[r + j];
+            l_part[r + j] *= alpha;
           }
+          // the O rescale below reads the factors back from shared memory
+          if (lane == 0) ctl.alpha[qd][r + j] = alpha;
         }
       }
+      // P = 2^(t - m_ref + 8) as hi + lo e4m3 terms; this key's column of
+      // P^T: hi of row r at byte r, lo at byte NH + r of the key's 16-byte
+      // chunk in 16-column block (byte / 16).
+      // (one body, instantiated masked and unmasked: a select would make
+      // fully visible tiles pay for the masks)
+      auto make_p = [&](auto masked) {
+        float c8[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) c8[r] = 8.f - m_ref[r];
+#pragma unroll
+        for (int a = 0; a < TP; ++a) {
+          if (a >= nt) break;
+          uint32_t words[NPV / 4];
+#pragma unroll
+          for (int w2 = 0; w2 < NPV / 4; ++w2) words[w2] = 0u;
+#pragma unroll
+          for (int r = 0; r < NR; r += 2) {
+            float pr[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              if constexpr (decltype(masked)::value) {
+                const bool vis = valid[a] && key[a] <= lim[r + j] && m_ref[r + j] != -INFINITY;
+                pr[j] = vis ? fast_exp2(fmaf(s[a][r + j], scale, c8[r + j])) : 0.f;
+              } else {
+                pr[j] = fast_exp2(fmaf(s[a][r + j], scale, c8[r + j]));
+              }
+            }
+            const __nv_fp8x2_storage_t hi2 =
+                __nv_cvt_float2_to_fp8x2(make_float2(pr[0], pr[1]), __NV_SATFINITE, __NV_E4M3);
+            const float2 hf = e4m3x2_to_float2(hi2);
+            const __nv_fp8x2_storage_t lo2 =
+                __nv_cvt_float2_to_fp8x2(make_float2(pr[0] - hf.x, pr[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
+            const float2 lf = e4m3x2_to_float2(lo2);
+            l_part[r] += hf.x + lf.x;
+            l_part[r + 1] += hf.y + lf.y;
+            words[r / 4] |= uint32_t(hi2) << ((r % 4) * 8);
+            words[(NH + r) / 4] |= uint32_t(lo2) << (((NH + r) % 4) * 8);
+          }
+          uint8_t* pt = smem + lay.p0 + bs(i + a) * p_stride;
+#pragma unroll
+          for (int bk = 0; bk < NPV / 16; ++bk)
+            *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
+                make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
+        }
+      };
+      if (all_vis)
+        make_p(std::false_type{});
+      else
+        make_p(std::true_type{});
       if (rescale) {
         // O holds the PV sums up to tile i-1, scaled by the old references:
-        // wait for the last of them and rescale O in TMEM before PV_i.
+        // wait for the last of them and rescale O in TMEM before PV_i (which
+        // waits for p_full, signalled below). Done after P is written, when
+        // S no longer occupies registers.
         ok = tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(i - 1)]), bp(i - 1), abort, kWaitLimitNs);
         if (!ok) break;
+        __syncwarp();  // lane 0's factors
         tc::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < NPV; c += 16) {
@@ -538,51 +617,13 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
           for (int j = 0; j < 16; ++j) {
             const int col = c + j;
             const int r = col < NH ? col : col - NH;  // hi column r, lo column NH + r
-            if (r < NR) v[j] *= alpha[r];
+            if (r < NR) v[j] *= ctl.alpha[qd][r];
           }
           tc::tmem_st16(tO + lane_off + c, v);
         }
         tc::tmem_wait_st();
       }
 
-      // P = 2^(t - m_ref + 8) as hi + lo e4m3 terms; this key's column of
-      // P^T: hi of row r at byte r, lo at byte NH + r of the key's 16-byte
-      // chunk in 16-column block (byte / 16).
-      float c8[NR];
-#pragma unroll
-      for (int r = 0; r < NR; ++r) c8[r] = 8.f - m_ref[r];
-#pragma unroll
-      for (int a = 0; a < TP; ++a) {
-        if (a >= nt) break;
-        uint32_t words[NPV / 4];
-#pragma unroll
-        for (int w2 = 0; w2 < NPV / 4; ++w2) words[w2] = 0u;
-#pragma unroll
-        for (int r = 0; r < NR; r += 2) {
-          float pr[2];
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const bool vis = valid[a] && key[a] <= lim[r + j] && m_ref[r + j] != -INFINITY;
-            pr[j] = vis ? fast_exp2(fmaf(s[a][r + j], scale, c8[r + j])) : 0.f;
-          }
-          const __nv_fp8x2_storage_t hi2 =
-              __nv_cvt_float2_to_fp8x2(make_float2(pr[0], pr[1]), __NV_SATFINITE, __NV_E4M3);
-          const float2 hf = e4m3x2_to_float2(hi2);
-          const __nv_fp8x2_storage_t lo2 =
-              __nv_cvt_float2_to_fp8x2(make_float2(pr[0] - hf.x, pr[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
-          const float2 lf = e4m3x2_to_float2(lo2);
-          l_part[r] += hf.x + lf.x;
-          l_part[r + 1] += hf.y + lf.y;
-          words[r / 4] |= uint32_t(hi2) << ((r % 4) * 8);
-          words[(NH + r) / 4] |= uint32_t(lo2) << (((NH + r) % 4) * 8);
-        }
-        uint8_t* pt = smem + lay.p0 + bs(i + a) * p_stride;
-#pragma unroll
-        for (int bk = 0; bk < NPV / 16; ++bk)
-          *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
-              make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
-
-      }
       tc::fence_async_smem();
       tc::tc_fence_before();
 #pragma unroll
@@ -733,7 +774,8 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
     configured = bytes;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_work, p.h_k, p.n_row_tiles);
+  if (int64_t(p.num_work) * p.h_k > INT32_MAX || p.n_row_tiles > 65535) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3(unsigned(p.num_work) * unsigned(p.h_k), unsigned(p.n_row_tiles));
   cfg.blockDim = dim3(FP6 ? kThreadsTcFp6 : kThreadsTc);
   cfg.dynamicSmemBytes = size_t(bytes);
   cfg.stream = stream;

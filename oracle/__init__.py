@@ -24,6 +24,8 @@ Sources (the mjolnir-kernel 0.1.0 pages):
 Modules:
 
 * :mod:`oracle.formats` — OCP e4m3 / e2m3 codecs and the fp6 4-in-3 packing.
+* :mod:`oracle.kvwrite` — the KV-cache write at ``slot_mapping`` (e4m3 with
+  per-tensor / per-head scales, packed e2m3 with per-channel scales).
 * :mod:`oracle.qquant`  — the Q quantization recipe (bit-exact target).
 * :mod:`oracle.plan`    — ``tile_width``, ``slots`` and the split-KV plan
   (bit-exact target).

@@ -22,10 +22,10 @@ Test infrastructure only (see :mod:`oracle`).
 
 Pins (``tests/test_oracle_formats.py``): hand-derived code values from the
 format definitions (``tests/golden/e4m3_codes.txt``,
-``tests/golden/e2m3_codes.txt``), exhaustive decode/encode round trips,
-ties-to-even at every midpoint, saturation, agreement with torch's own
-``float8_e4m3fn`` conversion on random inputs, and hand-packed byte fixtures
-(``tests/golden/fp6_packing.txt``).
+``tests/golden/e2m3_codes.txt``), exhaustive decode/encode round trips of
+both formats, ties-to-even at every midpoint, saturation, agreement with
+torch's own ``float8_e4m3fn`` conversion on random inputs, and hand-packed
+byte fixtures (``tests/golden/fp6_packing.txt``) read in both directions.
 """
 
 from __future__ import annotations
@@ -116,6 +116,38 @@ def e2m3_decode(codes) -> np.ndarray:
     return E2M3_TABLE[np.asarray(codes, dtype=np.uint8) & 0x3F]
 
 
+# Non-negative e2m3 values in code order (codes 0x00..0x1F), strictly
+# increasing: subnormals 0, 1/8 .. 7/8, then 1.0 .. 7.5.
+_E2M3_POS = E2M3_TABLE[:0x20].copy()
+
+
+def e2m3_encode(x) -> np.ndarray:
+    """Round to the nearest e2m3 value, ties to the even code, saturating.
+
+    The same plain definition as :func:`e4m3_encode` over the 32 non-negative
+    e2m3 values: the nearer of the two neighbours, the even code (mantissa
+    LSB 0) at an exact midpoint, magnitudes at or above 7.5 give 7.5 (code
+    0x1F), and the sign bit (bit 5) follows the sign of ``x`` (``-0.0`` and
+    negative values that round to zero give 0x20). The format has no NaN: a
+    NaN input is outside the contract of the cache write.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    vals = _E2M3_POS
+    i = np.searchsorted(vals, a, side="right") - 1  # vals[i] <= a
+    i = np.clip(i, 0, len(vals) - 1)
+    top = i >= len(vals) - 1  # a >= 7.5
+    j = np.minimum(i + 1, len(vals) - 1)
+    lo, hi = vals[i], vals[j]
+    twice = 2.0 * a  # exact: lo, hi and a need few bits
+    mid = lo + hi
+    up = (twice > mid) | ((twice == mid) & (i % 2 == 1))
+    code = np.where(up, j, i)
+    code = np.where(top, 0x1F, code).astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x20, code).astype(np.uint8)
+    return code
+
+
 # ----------------------------------------------------------------------------
 # 4-codes-in-3-bytes little-endian bitstream
 # ----------------------------------------------------------------------------
@@ -139,3 +171,23 @@ def fp6_unpack_rows(packed) -> np.ndarray:
             code |= ((flat[:, bit // 8] >> (bit % 8)) & 1) << k
         out[:, i] = code
     return out.reshape(packed.shape[:-1] + (ncodes,))
+
+
+def fp6_pack_rows(codes) -> np.ndarray:
+    """Codes ``[..., 4*k]`` (6-bit values in uint8) -> packed rows ``[..., 3*k]``.
+
+    The inverse of :func:`fp6_unpack_rows`: bit ``k`` of code ``i`` goes to
+    bit ``6i + k`` of the row's little-endian bitstream. A plain loop over
+    codes and bits.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    ncodes = codes.shape[-1]
+    assert ncodes % 4 == 0, "a packed e2m3 row holds a whole number of 4-code groups"
+    nbytes = ncodes * 6 // 8
+    flat = codes.reshape(-1, ncodes).astype(np.uint32)
+    out = np.zeros((flat.shape[0], nbytes), dtype=np.uint32)
+    for i in range(ncodes):
+        for k in range(6):
+            bit = 6 * i + k
+            out[:, bit // 8] |= ((flat[:, i] >> k) & 1) << (bit % 8)
+    return out.astype(np.uint8).reshape(codes.shape[:-1] + (nbytes,))

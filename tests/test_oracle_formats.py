@@ -126,3 +126,58 @@ def test_fp6_unpack_matches_independent_packer():
     packed = pack_e2m3(codes)
     assert packed.shape == (50, 96)
     assert np.array_equal(F.fp6_unpack_rows(packed), codes)
+
+
+# ----------------------------------------------------------------------------
+# e2m3 encoder (the cache write) and the packing direction of the fixtures
+# ----------------------------------------------------------------------------
+def test_e2m3_roundtrip_all_codes():
+    codes = np.arange(64, dtype=np.uint8)
+    assert np.array_equal(F.e2m3_encode(F.e2m3_decode(codes)), codes)
+
+
+def test_e2m3_midpoints_go_to_even():
+    pos = F.E2M3_TABLE[:0x20]
+    assert np.all(np.diff(pos) > 0)
+    for c in range(0x1F):
+        mid = (pos[c] + pos[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert F.e2m3_encode(mid) == even, hex(c)
+        assert F.e2m3_encode(-mid) == (even | 0x20), hex(c)
+        eps = (pos[c + 1] - pos[c]) * 1e-6
+        assert F.e2m3_encode(mid - eps) == c
+        assert F.e2m3_encode(mid + eps) == c + 1
+
+
+def test_e2m3_hand_values():
+    # worked by hand from the value list of tests/golden/e2m3_codes.txt
+    cases = [
+        (0.0625, 0x00),   # tie 0 | 0.125 -> even code 0
+        (0.1875, 0x02),   # tie 0.125 (1) | 0.25 (2) -> 2
+        (0.9375, 0x08),   # tie 0.875 (7) | 1.0 (8) -> 8: rounds up into the normals
+        (1.0625, 0x08),   # tie 1.0 (8) | 1.125 (9) -> 8
+        (1.9375, 0x10),   # tie 1.875 (15) | 2.0 (16) -> 16
+        (5.5, 0x1B),      # exact: 1.375 * 4
+        (5.75, 0x1C),     # tie 5.5 (27) | 6.0 (28) -> 28
+        (7.4, 0x1F),      # nearer to 7.5 than to 7.0
+        (7.5, 0x1F), (8.0, 0x1F), (1e30, 0x1F),  # saturation
+        (-3.0, 0x34), (-0.0, 0x20), (-0.01, 0x20),
+    ]
+    for x, want in cases:
+        assert F.e2m3_encode(x) == want, (x, hex(int(F.e2m3_encode(x))))
+
+
+def test_fp6_pack_golden(golden):
+    for row in golden("fp6_packing.txt"):
+        codes_s, bytes_s = row.split("|")
+        codes = np.array([int(v) for v in codes_s.split()], dtype=np.uint8)
+        want = np.array([int(v, 16) for v in bytes_s.split()], dtype=np.uint8)
+        assert np.array_equal(F.fp6_pack_rows(codes), want), row
+
+
+def test_fp6_pack_unpack_inverse():
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 64, size=(7, 128), dtype=np.uint8)
+    packed = F.fp6_pack_rows(codes)
+    assert packed.shape == (7, 96)
+    assert np.array_equal(F.fp6_unpack_rows(packed), codes)

@@ -1,0 +1,126 @@
+"""Pins of the oracle's KV-cache write at ``slot_mapping``."""
+
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import kvwrite as W
+
+PS, NP, HK, D = 16, 6, 2, 128
+
+
+def _layout(kind, kv_format):
+    rb = W.row_bytes(D, kv_format)
+    if kind == "HND":  # (page, head, token, row)
+        return (HK * PS * rb, rb, PS * rb)
+    return (PS * HK * rb, HK * rb, rb)  # NHD: (page, token, head, row)
+
+
+def _pools(kv_format):
+    rb = W.row_bytes(D, kv_format)
+    size = NP * PS * HK * rb
+    rng = np.random.default_rng(3)
+    return rng.integers(0, 256, size, dtype=np.uint8), rng.integers(0, 256, size, dtype=np.uint8)
+
+
+def _gather(pool, strides, slot, h, rb):
+    off = (slot // PS) * strides[0] + (slot % PS) * strides[1] + h * strides[2]
+    return pool[off:off + rb]
+
+
+def _scales(kv_format, rng):
+    if kv_format == W.KV_E4M3:
+        return rng.uniform(0.002, 0.05, HK).astype(np.float32), rng.uniform(0.002, 0.05, HK).astype(np.float32)
+    return rng.uniform(0.1, 2.0, (HK, D)).astype(np.float32), rng.uniform(0.1, 2.0, (HK, D)).astype(np.float32)
+
+
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+@pytest.mark.parametrize("kind", ["HND", "NHD"])
+def test_padding_writes_nothing_and_rows_land_at_their_slots(kv_format, kind):
+    rng = np.random.default_rng(11)
+    T = 9
+    key = rng.standard_normal((T, HK, D)).astype(np.float32)
+    val = rng.standard_normal((T, HK, D)).astype(np.float32)
+    slots = np.array([5, -1, 17, 40, -1, 3, 95, 64, 2], dtype=np.int64)
+    ks, vs = _scales(kv_format, rng)
+    kp, vp = _pools(kv_format)
+    kp0, vp0 = kp.copy(), vp.copy()
+    st = _layout(kind, kv_format)
+    W.write_kv(key, val, kp, vp, slots, PS, st, st, kv_format, ks, vs)
+    rb = W.row_bytes(D, kv_format)
+    kq, vq = W.quantize_rows(key, ks, kv_format), W.quantize_rows(val, vs, kv_format)
+    touched = np.zeros(kp.size, dtype=bool)
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        for h in range(HK):
+            assert np.array_equal(_gather(kp, st, s, h, rb), kq[t, h])
+            assert np.array_equal(_gather(vp, st, s, h, rb), vq[t, h])
+            off = (s // PS) * st[0] + (s % PS) * st[1] + h * st[2]
+            touched[off:off + rb] = True
+    # every other byte is as it was
+    assert np.array_equal(kp[~touched], kp0[~touched]) and np.array_equal(vp[~touched], vp0[~touched])
+
+
+def test_e4m3_representable_rows_are_exact():
+    # x = scale * v with power-of-two scales: x / scale is exactly v
+    rng = np.random.default_rng(12)
+    codes = rng.choice([c for c in range(256) if c not in (0x7F, 0xFF)], size=(4, HK, D)).astype(np.uint8)
+    scale = np.array([2.0 ** -6, 2.0 ** 3], dtype=np.float32)
+    x = (F.e4m3_decode(codes) * scale.reshape(1, HK, 1)).astype(np.float32)
+    assert np.array_equal(W.quantize_rows(x, scale, W.KV_E4M3), codes)
+    # per tensor: one scale for every head
+    x1 = (F.e4m3_decode(codes) * np.float32(0.5)).astype(np.float32)
+    assert np.array_equal(W.quantize_rows(x1, np.array([0.5], np.float32), W.KV_E4M3), codes)
+
+
+def test_e2m3_representable_rows_are_exact():
+    rng = np.random.default_rng(13)
+    codes = rng.integers(0, 64, size=(4, HK, D), dtype=np.uint8)
+    s = (2.0 ** rng.integers(-4, 4, size=(HK, D))).astype(np.float32)
+    x = (F.e2m3_decode(codes) * s).astype(np.float32)
+    rows = W.quantize_rows(x, s, W.KV_E2M3)
+    assert rows.shape == (4, HK, 96)
+    assert np.array_equal(F.fp6_unpack_rows(rows), codes)
+
+
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+def test_written_rows_are_within_half_a_step(kv_format):
+    rng = np.random.default_rng(14)
+    x = (rng.standard_normal((64, HK, D)) * 3).astype(np.float32)
+    ks, _ = _scales(kv_format, rng)
+    rows = W.quantize_rows(x, ks, kv_format)
+    if kv_format == W.KV_E4M3:
+        codes, vals = rows, F.E4M3_TABLE[:0x7F]
+        y = x / ks.reshape(1, HK, 1).astype(np.float64)
+        dec = F.e4m3_decode(codes)
+        top = 448.0
+    else:
+        codes, vals = F.fp6_unpack_rows(rows), F.E2M3_TABLE[:0x20]
+        y = x / ks.astype(np.float64)
+        dec = F.e2m3_decode(codes)
+        top = 7.5
+    a = np.minimum(np.abs(y), top)
+    i = np.clip(np.searchsorted(vals, a, side="right") - 1, 0, len(vals) - 2)
+    half_step = (vals[i + 1] - vals[i]) / 2
+    # the quotient is float32: allow its own rounding (relative 2^-24)
+    assert np.all(np.abs(np.abs(dec) - a) <= half_step * (1 + 1e-6) + a * 2.0 ** -23)
+    assert np.all((np.signbit(dec) == np.signbit(y)) | (dec == 0))
+
+
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+def test_token_order_does_not_matter(kv_format):
+    rng = np.random.default_rng(15)
+    T = 12
+    key = rng.standard_normal((T, HK, D)).astype(np.float32)
+    val = rng.standard_normal((T, HK, D)).astype(np.float32)
+    slots = rng.permutation(NP * PS)[:T].astype(np.int64)
+    slots[3] = -1
+    ks, vs = _scales(kv_format, rng)
+    st = _layout("HND", kv_format)
+    a_k, a_v = _pools(kv_format)
+    b_k, b_v = a_k.copy(), a_v.copy()
+    W.write_kv(key, val, a_k, a_v, slots, PS, st, st, kv_format, ks, vs)
+    perm = rng.permutation(T)
+    W.write_kv(key[perm], val[perm], b_k, b_v, slots[perm], PS, st, st, kv_format, ks, vs)
+    assert np.array_equal(a_k, b_k) and np.array_equal(a_v, b_v)

@@ -171,6 +171,69 @@ def cpu_baseline_child(workload: str, budget_s: float):
                       "bytes": nbytes}))
 
 
+def measure_write_kv(w, dev, peak: float) -> dict:
+    """The KV-cache write that precedes a decode step (mj_write_kv), timed on
+    its own: a bulk write of every token of the workload's batch (up to
+    262144), and the decode step's own write of one new token per request.
+    Inputs are generated on the device (a kernel-only figure). Algorithmic
+    bytes: the bf16 K and V rows read, the code rows written and the slots."""
+    import ctypes
+
+    import torch
+
+    import paged_fp8_decode_gb300 as mj
+
+    fmt = mj.MJ_KV_E4M3 if w.kv_format == "fp8" else mj.MJ_KV_E2M3
+    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    lib = mj.load_library()
+    stream = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    out = {"format": w.kv_format}
+    for label, n_tok in (("bulk", int(min(int(w.seq_lens.sum()), 262144))), ("decode_step", int(w.num_seqs))):
+        pages = (n_tok + w.page_size - 1) // w.page_size + 64
+        kv = torch.randn(2, n_tok, w.h_k, w.d, device=dev, generator=gen).to(torch.bfloat16)
+        slots = torch.randperm(pages * w.page_size, device=dev, generator=gen)[:n_tok].to(torch.int64)
+        pool = torch.empty(2, pages * w.page_size * w.h_k * row, dtype=torch.uint8, device=dev)
+        amax = kv.float().abs().amax(dim=1)  # [2, h_k, d]
+        if fmt == mj.MJ_KV_E4M3:
+            scales = (amax.amax(dim=2) / 448.0).contiguous()  # per KV head
+        else:
+            scales = (amax / 7.5).contiguous()  # per (KV head, channel)
+        strides = (w.h_k * w.page_size * row, row, w.page_size * row)  # HND
+        a = mj.mj_write_kv_args()
+        a.num_tokens, a.h_k, a.d = n_tok, w.h_k, w.d
+        a.key, a.value = kv[0].data_ptr(), kv[1].data_ptr()
+        a.key_tok_stride, a.key_head_stride = kv[0].stride(0), kv[0].stride(1)
+        a.value_tok_stride, a.value_head_stride = kv[1].stride(0), kv[1].stride(1)
+        a.slot_mapping = slots.data_ptr()
+        a.kv_format, a.page_size, a.num_pages = fmt, w.page_size, pages
+        a.k_cache, a.v_cache = pool[0].data_ptr(), pool[1].data_ptr()
+        a.k_stride_page, a.k_stride_token, a.k_stride_head = strides
+        a.v_stride_page, a.v_stride_token, a.v_stride_head = strides
+        a.k_scale, a.v_scale, a.scale_per_head = scales[0].data_ptr(), scales[1].data_ptr(), 1
+        ref, st = ctypes.byref(a), stream.cuda_stream
+        for _ in range(3):
+            assert lib.mj_write_kv(ref, st) == 0
+        reps = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            lib.mj_write_kv(ref, st)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        nbytes = 2 * n_tok * w.h_k * w.d * 2 + 2 * n_tok * w.h_k * row + n_tok * 8
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[label] = {"tokens": n_tok, "us": round(us, 3), "bytes": nbytes, "gbs": round(gbs, 1)}
+        if label == "bulk":
+            out[label]["roofline"] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                      "frac": round(gbs / peak, 4)}
+        del kv, slots, pool
+    return out
+
+
 def run_cpu_baseline(workload: str, budget_s: float = 12.0):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -343,6 +406,9 @@ def main_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
 
+    # the KV-cache write before the step (its own measurement, outside the timed step)
+    write_kv = measure_write_kv(w, dev, _peaks()[0]) if rank == 0 else None
+
     # plan host time alone
     t0 = time.perf_counter()
     for _ in range(50):
@@ -393,6 +459,7 @@ def main_ours(args):
                      "decode_us": round(dec_avg_ms * 1e3, 3)},
         "cpu_baseline": cpu_base,
         "device_status": status,
+        "write_kv": write_kv,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -11,6 +11,10 @@
  *                                online softmax, P.V
  *   mj_merge_lse        (device) merge split-KV partials by log-sum-exp
  *
+ * and, before the step, the cache write of the new tokens:
+ *
+ *   mj_write_kv         (device) quantize K/V rows into the paged caches
+ *
  * Conventions (all calls):
  *  - Every call returns an mj_status; 0 is success, negative is an error.
  *    Nothing throws, aborts or prints.
@@ -283,6 +287,57 @@ MJ_API int mj_merge_lse(const mj_decode_args* args, void* stream);
  * ---------------------------------------------------------------------- */
 #define MJ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 MJ_API int mj_decode_attention_noalloc(const mj_decode_args* args, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mj_write_kv — the KV-cache write that precedes a decode step: quantize the
+ * new tokens' K and V rows and scatter them into the paged caches at
+ * slot_mapping. Source: MjolnirImpl.do_kv_cache_update / _write_kv on the
+ * mjolnir/backend.py page (the e4m3 write takes the layer's k/v scale; the
+ * packed e2m3 write takes the per-(KV head, channel) scales that
+ * _install_fp6_scales says "quantize the cache write").
+ *
+ * For token t and KV head g with s = slot_mapping[t] >= 0, the row goes to
+ * page s / page_size, row s % page_size of the cache (the decode call's
+ * layout and strides):
+ *   e4m3: code[c] = e4m3(x[c] / scale)      scale = k_scale[0] (per tensor)
+ *                                           or k_scale[g] (scale_per_head)
+ *   e2m3: code[c] = e2m3(x[c] / k_scale[g*d + c]), packed 4 codes per 3 bytes
+ * x is the bf16 input widened to float32; the division is IEEE float32 and
+ * the rounding to the cache format is to nearest, ties to even, saturating
+ * (448 / 7.5). Likewise for V with v_scale. A negative slot marks a padding
+ * token: nothing is written for it. A slot at or past num_pages*page_size is
+ * skipped and, if status != NULL, bit 1 of *status is set.
+ *
+ * Alignment: key/value 16-byte aligned with token/head strides that are
+ * multiples of 8 elements; cache bases 16-byte aligned with byte strides that
+ * are multiples of 16. The caches are written in place; every byte outside
+ * the written rows keeps its value. The call enqueues one kernel on `stream`.
+ * ---------------------------------------------------------------------- */
+typedef struct mj_write_kv_args {
+  int num_tokens;             /* rows in key / value (0: nothing to do) */
+  int h_k, d;                 /* KV heads; head size (128) */
+  const void* key;            /* device bf16; (t, g, c) at key[t*key_tok_stride + g*key_head_stride + c] */
+  const void* value;          /* device bf16; likewise with the value strides */
+  int64_t key_tok_stride, key_head_stride;      /* elements */
+  int64_t value_tok_stride, value_head_stride;  /* elements */
+  const int64_t* slot_mapping;  /* device [num_tokens] */
+
+  int kv_format;              /* mj_kv_format */
+  int page_size;              /* tokens per page: 16, 32, 64 or 128 */
+  int64_t num_pages;
+  void* k_cache;
+  void* v_cache;
+  int64_t k_stride_page, k_stride_token, k_stride_head;  /* bytes */
+  int64_t v_stride_page, v_stride_token, v_stride_head;  /* bytes */
+
+  const float* k_scale;       /* device float32: e4m3 [1] or [h_k]; e2m3 [h_k][d] */
+  const float* v_scale;
+  int scale_per_head;         /* e4m3 only: 1 = one scale per KV head, 0 = per tensor */
+
+  uint32_t* status;           /* nullable device word (see above) */
+} mj_write_kv_args;
+
+MJ_API int mj_write_kv(const mj_write_kv_args* args, void* stream);
 
 #ifdef __cplusplus
 }

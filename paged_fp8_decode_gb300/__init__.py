@@ -40,7 +40,7 @@ KV_TILE = 128
 EXPORTS = (
     "mj_status_string", "mj_version", "mj_tile_width", "mj_slots", "mj_plan_split_kv",
     "mj_quantize_q", "mj_workspace_size", "mj_workspace_init", "mj_workspace_status",
-    "mj_decode_attention", "mj_merge_lse", "mj_decode_attention_noalloc",
+    "mj_decode_attention", "mj_merge_lse", "mj_decode_attention_noalloc", "mj_write_kv",
 )
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -77,6 +77,24 @@ class mj_decode_args(ctypes.Structure):
     ]
 
 
+class mj_write_kv_args(ctypes.Structure):
+    """ctypes mirror of ``struct mj_write_kv_args`` (include/mj.h)."""
+
+    _fields_ = [
+        ("num_tokens", ctypes.c_int), ("h_k", ctypes.c_int), ("d", ctypes.c_int),
+        ("key", ctypes.c_void_p), ("value", ctypes.c_void_p),
+        ("key_tok_stride", ctypes.c_int64), ("key_head_stride", ctypes.c_int64),
+        ("value_tok_stride", ctypes.c_int64), ("value_head_stride", ctypes.c_int64),
+        ("slot_mapping", ctypes.c_void_p),
+        ("kv_format", ctypes.c_int), ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int64),
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("k_stride_page", ctypes.c_int64), ("k_stride_token", ctypes.c_int64), ("k_stride_head", ctypes.c_int64),
+        ("v_stride_page", ctypes.c_int64), ("v_stride_token", ctypes.c_int64), ("v_stride_head", ctypes.c_int64),
+        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("scale_per_head", ctypes.c_int),
+        ("status", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -104,6 +122,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mj_decode_attention.argtypes = [ctypes.POINTER(mj_decode_args), vp]
     lib.mj_merge_lse.argtypes = [ctypes.POINTER(mj_decode_args), vp]
     lib.mj_decode_attention_noalloc.argtypes = [ctypes.POINTER(mj_decode_args), vp]
+    lib.mj_write_kv.argtypes = [ctypes.POINTER(mj_write_kv_args), vp]
     _lib = lib
     return lib
 
@@ -218,6 +237,33 @@ def mj_decode_attention_noalloc(args: mj_decode_args, stream=None):
     include/mj.h)."""
     _check("mj_decode_attention_noalloc",
            load_library().mj_decode_attention_noalloc(ctypes.byref(args), _stream(stream)))
+
+
+def mj_write_kv(key, value, slot_mapping, k_cache, v_cache, kv_strides, page_size: int, num_pages: int,
+                kv_format: int, k_scale, v_scale, scale_per_head: bool = False, status=None, stream=None):
+    """Quantize K/V rows into the paged caches at ``slot_mapping``.
+
+    ``key`` / ``value``: bf16 ``[T, h_k, d]`` (any token/head strides, channel
+    stride 1). ``slot_mapping``: int64 ``[T]`` (negative = padding).
+    ``k_cache`` / ``v_cache``: uint8 pools; ``kv_strides``: byte strides
+    ``(page, token, head)`` shared by both. ``k_scale`` / ``v_scale``:
+    float32 -- e4m3 ``[1]`` or ``[h_k]`` (``scale_per_head``), e2m3
+    ``[h_k, d]``. ``status``: optional int32/uint32 device word."""
+    assert key.stride(2) == 1 and value.stride(2) == 1
+    a = mj_write_kv_args()
+    a.num_tokens, a.h_k, a.d = int(key.shape[0]), int(key.shape[1]), int(key.shape[2])
+    a.key, a.value = _ptr(key), _ptr(value)
+    a.key_tok_stride, a.key_head_stride = key.stride(0), key.stride(1)
+    a.value_tok_stride, a.value_head_stride = value.stride(0), value.stride(1)
+    a.slot_mapping = _ptr(slot_mapping)
+    a.kv_format, a.page_size, a.num_pages = int(kv_format), int(page_size), int(num_pages)
+    a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
+    a.k_stride_page, a.k_stride_token, a.k_stride_head = (int(x) for x in kv_strides)
+    a.v_stride_page, a.v_stride_token, a.v_stride_head = (int(x) for x in kv_strides)
+    a.k_scale, a.v_scale = _ptr(k_scale), _ptr(v_scale)
+    a.scale_per_head = 1 if scale_per_head else 0
+    a.status = _ptr(status)
+    _check("mj_write_kv", load_library().mj_write_kv(ctypes.byref(a), _stream(stream)))
 
 
 from .step import DecodeStep  # noqa: E402,F401

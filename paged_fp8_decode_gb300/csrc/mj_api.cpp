@@ -265,6 +265,35 @@ int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, in
   return status_of(mj::launch_quantize_q(p, static_cast<cudaStream_t>(stream)));
 }
 
+int mj_write_kv(const mj_write_kv_args* a, void* stream) {
+  if (!a) return MJ_ERR_INVALID_ARG;
+  if (a->num_tokens < 0 || a->h_k < 1 || a->num_pages < 0) return MJ_ERR_INVALID_ARG;
+  if (a->d != mj::kHeadDim) return MJ_ERR_UNSUPPORTED;
+  if (a->kv_format != MJ_KV_E4M3 && a->kv_format != MJ_KV_E2M3) return MJ_ERR_UNSUPPORTED;
+  if (a->page_size != 16 && a->page_size != 32 && a->page_size != 64 && a->page_size != 128)
+    return MJ_ERR_UNSUPPORTED;
+  if (a->num_tokens == 0) return MJ_OK;
+  if (int64_t(a->num_tokens) * a->h_k >= (int64_t(1) << 31)) return MJ_ERR_INVALID_ARG;
+  if (!a->key || !a->value || !a->slot_mapping || !a->k_cache || !a->v_cache || !a->k_scale || !a->v_scale)
+    return MJ_ERR_INVALID_ARG;
+  const int64_t el[] = {a->key_tok_stride, a->key_head_stride, a->value_tok_stride, a->value_head_stride};
+  const int64_t by[] = {a->k_stride_page, a->k_stride_token, a->k_stride_head,
+                        a->v_stride_page, a->v_stride_token, a->v_stride_head};
+  for (int64_t v : el)
+    if (v < 0) return MJ_ERR_INVALID_ARG;
+  for (int64_t v : by)
+    if (v < 0) return MJ_ERR_INVALID_ARG;
+  for (int64_t v : el)
+    if (v % 8) return MJ_ERR_ALIGNMENT;
+  for (int64_t v : by)
+    if (v % 16) return MJ_ERR_ALIGNMENT;
+  if (!aligned(a->key, 16) || !aligned(a->value, 16) || !aligned(a->slot_mapping, 8) || !aligned(a->k_cache, 16) ||
+      !aligned(a->v_cache, 16) || !aligned(a->k_scale, 16) || !aligned(a->v_scale, 16) ||
+      (a->status && !aligned(a->status, 4)))
+    return MJ_ERR_ALIGNMENT;
+  return status_of(mj::launch_write_kv(*a, static_cast<cudaStream_t>(stream)));
+}
+
 int mj_workspace_size(int part_seqs, int max_splits, int max_q_len, int h_q, int h_k, int d, size_t* bytes) {
   if (!bytes || part_seqs < 0 || max_splits < 1 || max_q_len < 1 || h_k < 1 || h_q < 1 || h_q % h_k)
     return MJ_ERR_INVALID_ARG;

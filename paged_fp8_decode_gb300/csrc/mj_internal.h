@@ -88,6 +88,7 @@ struct QuantParams {
 cudaError_t launch_quantize_q(const QuantParams& p, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_write_kv(const mj_write_kv_args& a, cudaStream_t stream);
 // Tensor-core kernel; sets *unsupported (and launches nothing) when the
 // arguments are outside its envelope.
 cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsupported);

@@ -332,3 +332,69 @@ WORKLOADS = {
     "spec_verify_noncausal": lambda seed=1004: spec_verify(False, seed),
     "fp6_decode": fp6_decode,
 }
+
+
+# ----------------------------------------------------------------------------
+# inputs of the KV-cache write (mj_write_kv)
+# ----------------------------------------------------------------------------
+@dataclass
+class WriteCase:
+    name: str
+    key_bf16: np.ndarray    # uint16 bf16 bits [T, h_k, d]
+    value_bf16: np.ndarray
+    key: np.ndarray         # float32 values of the bf16 inputs (exact)
+    value: np.ndarray
+    slots: np.ndarray       # int64 [T]; -1 = padding token
+    k_pool: np.ndarray      # uint8, pre-filled with random bytes (written in place)
+    v_pool: np.ndarray
+    kv_strides: tuple       # byte strides (page, token, head)
+    page_size: int
+    num_pages: int
+    kv_format: str          # "fp8" | "e2m3"
+    k_scale: np.ndarray     # float32: [1] / [h_k] (fp8) or [h_k, d] (e2m3)
+    v_scale: np.ndarray
+    scale_per_head: bool
+
+
+def kv_write_case(*, name="write", num_tokens, h_k=8, d=128, page_size=16, num_pages, layout="HND",
+                  kv_format="fp8", scale_mode="head", pad_every=0, outlier_channels=0, seed=0) -> WriteCase:
+    """New K/V rows (N(0,1), rounded to bf16, optional x10 outlier channels),
+    a slot for each token (distinct, random over the pool; every
+    ``pad_every``-th token is padding, slot -1), pools pre-filled with random
+    bytes, and scales: fp8 ``amax/448`` per tensor or per KV head, e2m3
+    ``amax/7.5`` per (KV head, channel)."""
+    import torch
+
+    rng = _rng(seed, 20)
+    x = rng.standard_normal((2, num_tokens, h_k, d), dtype=np.float32)
+    if outlier_channels:
+        for s in range(2):
+            for g in range(h_k):
+                ch = rng.choice(d, outlier_channels, replace=False)
+                x[s, :, g, ch] *= 10.0
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xf = (bits.astype(np.uint32) << 16).view(np.float32)  # exact float32 of the bf16 values
+    cap = num_pages * page_size
+    assert num_tokens <= cap
+    slots = rng.permutation(cap)[:num_tokens].astype(np.int64)
+    if pad_every:
+        slots[pad_every - 1::pad_every] = -1
+    rb = d if kv_format == "fp8" else d * 3 // 4
+    strides = (h_k * page_size * rb, rb, page_size * rb) if layout == "HND" else (page_size * h_k * rb, h_k * rb, rb)
+    size = num_pages * page_size * h_k * rb
+    k_pool = rng.integers(0, 256, size, dtype=np.uint8)
+    v_pool = rng.integers(0, 256, size, dtype=np.uint8)
+    live = slots >= 0
+    scales = []
+    for s in range(2):
+        v = np.abs(xf[s][live]) if live.any() else np.ones((1, h_k, d), np.float32)
+        if kv_format == "e2m3":
+            scales.append(np.maximum(v.max(axis=0), 1e-6).astype(np.float32) / np.float32(7.5))
+        elif scale_mode == "head":
+            scales.append(np.maximum(v.max(axis=(0, 2)), 1e-6).astype(np.float32) / np.float32(448.0))
+        else:
+            scales.append(np.array([max(float(v.max()), 1e-6) / 448.0], dtype=np.float32))
+    return WriteCase(name=name, key_bf16=bits[0], value_bf16=bits[1], key=xf[0], value=xf[1], slots=slots,
+                     k_pool=k_pool, v_pool=v_pool, kv_strides=strides, page_size=page_size, num_pages=num_pages,
+                     kv_format=kv_format, k_scale=scales[0], v_scale=scales[1],
+                     scale_per_head=(kv_format == "fp8" and scale_mode == "head"))

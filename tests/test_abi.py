@@ -158,3 +158,51 @@ def test_quantize_rejections(lib):
     assert f(None, 4096, 128, 2, 1, 32, 8, 128, None, base, base, None) == mj.MJ_ERR_INVALID_ARG
     assert f(base + 2, 4096, 128, 2, 1, 32, 8, 128, None, base, base, None) == mj.MJ_ERR_ALIGNMENT
     assert f(base, 4096, 128, 0, 1, 32, 8, 128, None, None, None, None) == mj.MJ_OK  # empty batch: no-op
+
+
+# ----------------------------------------------------------------------------
+# mj_write_kv: host-side validation (every case is rejected before a launch)
+# ----------------------------------------------------------------------------
+def _valid_write_args():
+    base = 1 << 40  # never dereferenced: every case below fails validation first
+    a = mj.mj_write_kv_args()
+    a.num_tokens, a.h_k, a.d = 4, 2, 128
+    a.key, a.value = base, base + 0x1000
+    a.key_tok_stride, a.key_head_stride = 256, 128
+    a.value_tok_stride, a.value_head_stride = 256, 128
+    a.slot_mapping = base + 0x2000
+    a.kv_format, a.page_size, a.num_pages = 0, 16, 4
+    a.k_cache, a.v_cache = base + 0x10000, base + 0x20000
+    a.k_stride_page, a.k_stride_token, a.k_stride_head = 4096, 128, 2048
+    a.v_stride_page, a.v_stride_token, a.v_stride_head = 4096, 128, 2048
+    a.k_scale, a.v_scale, a.scale_per_head = base + 0x3000, base + 0x3100, 1
+    return a
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("d", 64, mj.MJ_ERR_UNSUPPORTED),
+    ("kv_format", 3, mj.MJ_ERR_UNSUPPORTED),
+    ("page_size", 48, mj.MJ_ERR_UNSUPPORTED),
+    ("num_tokens", -1, mj.MJ_ERR_INVALID_ARG),
+    ("h_k", 0, mj.MJ_ERR_INVALID_ARG),
+    ("key", None, mj.MJ_ERR_INVALID_ARG),
+    ("slot_mapping", None, mj.MJ_ERR_INVALID_ARG),
+    ("v_scale", None, mj.MJ_ERR_INVALID_ARG),
+    ("key", (1 << 40) + 8, mj.MJ_ERR_ALIGNMENT),
+    ("slot_mapping", (1 << 40) + 0x2004, mj.MJ_ERR_ALIGNMENT),
+    ("key_head_stride", 132, mj.MJ_ERR_ALIGNMENT),
+    ("k_stride_token", 120, mj.MJ_ERR_ALIGNMENT),
+    ("v_stride_page", -16, mj.MJ_ERR_INVALID_ARG),
+    ("k_scale", (1 << 40) + 0x3004, mj.MJ_ERR_ALIGNMENT),
+])
+def test_write_kv_args_rejected_on_host(lib, field, value, status):
+    a = _valid_write_args()
+    setattr(a, field, value)
+    assert lib.mj_write_kv(ctypes.byref(a), None) == status
+
+
+def test_write_kv_nothing_to_do(lib):
+    a = _valid_write_args()
+    a.num_tokens = 0
+    a.key = a.value = a.slot_mapping = None  # nothing is read when there are no tokens
+    assert lib.mj_write_kv(ctypes.byref(a), None) == mj.MJ_OK

@@ -66,6 +66,9 @@ typedef enum mj_kv_format {
   MJ_KV_E2M3 = 1   /* packed e2m3: 4 codes per 3 bytes, little-endian bitstream; row = d*3/4 bytes */
 } mj_kv_format;
 
+/* Element type of the decode output (T5DecodeRunner's out_dtype: bf16 or fp16). */
+typedef enum mj_out_dtype { MJ_OUT_BF16 = 0, MJ_OUT_F16 = 1 } mj_out_dtype;
+
 /* Kernel variant of mj_decode_attention. AUTO picks the tensor-core kernel
  * whenever its preconditions hold, else the CUDA-core kernel. */
 typedef enum mj_impl { MJ_IMPL_AUTO = 0, MJ_IMPL_SIMT = 1, MJ_IMPL_TCGEN05 = 2 } mj_impl;
@@ -198,7 +201,7 @@ typedef struct mj_decode_args {
 
   /* output */
   const float* o_mul;           /* nullable device float32 [h_q][d]: O *= o_mul last */
-  void* out;                    /* device bf16; (b*q_len+t, h, c) at
+  void* out;                    /* device bf16 (or fp16, see out_dtype); (b*q_len+t, h, c) at
                                    out[(b*q_len+t)*out_tok_stride + h*out_head_stride + c] */
   int64_t out_tok_stride, out_head_stride;  /* elements, multiples of 8 */
   float* lse;                   /* nullable device float32 [num_seqs][h_k][q_len*h_r]:
@@ -212,6 +215,8 @@ typedef struct mj_decode_args {
   int impl;          /* mj_impl */
   int kv_stages;     /* KV ring depth of the tensor-core kernel */
   int evict_first;   /* 1 = L2 evict-first hint on KV loads (KV is read once) */
+
+  int out_dtype;     /* mj_out_dtype of `out` (0 = bf16); rounding to nearest even */
 } mj_decode_args;
 
 /* ------------------------------------------------------------------------

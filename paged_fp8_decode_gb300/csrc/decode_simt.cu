@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
       const int tq = row / p.h_r, rr = row % p.h_r, h = g * p.h_r + rr;
       float val = on * vd;
       if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + c];
-      p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_bf16_bits(val);
+      p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_out_bits(val, p.out_f16);
       if (p.lse && c == 0)
         p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] = Lt > 0.f ? (M + fast_log2(Lt)) * kLn2 : -INFINITY;
     } else {

@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
           const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
           float val = on * vd;
           if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + x];
-          p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + x] = float_to_bf16_bits(val);
+          p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + x] = float_to_out_bits(val, p.out_f16);
           if (p.lse && x == 0)
             p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
                 lr > 0.f ? (m_ref[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;

@@ -64,6 +64,7 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   if (a->out_tok_stride < 0 || a->out_head_stride < 0 || a->descale_seq_stride < 0 || a->descale_head_stride < 0)
     return MJ_ERR_INVALID_ARG;
   if (a->out_tok_stride % 8 || a->out_head_stride % 8) return MJ_ERR_ALIGNMENT;
+  if (a->out_dtype != MJ_OUT_BF16 && a->out_dtype != MJ_OUT_F16) return MJ_ERR_UNSUPPORTED;
 
   const int h_r = a->h_q / a->h_k;
   const int n_q = a->q_len * h_r;
@@ -123,6 +124,7 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   q.v_fmt = fmt;
   q.o_mul = a->o_mul;
   q.out = static_cast<uint16_t*>(a->out);
+  q.out_f16 = a->out_dtype == MJ_OUT_F16 ? 1 : 0;
   q.out_ts = a->out_tok_stride;
   q.out_hs = a->out_head_stride;
   q.lse = a->lse;

@@ -80,6 +80,13 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
   return u;
 }
 
+__device__ __forceinline__ uint16_t float_to_f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+// the decode output element: bf16 or fp16, rounded to nearest even
+__device__ __forceinline__ uint16_t float_to_out_bits(float x, int f16) {
+  return f16 ? float_to_f16_bits(x) : float_to_bf16_bits(x);
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
   return __uint_as_float(uint32_t(u) << 16);
 }

@@ -52,7 +52,8 @@ struct DecodeParams {
   float v_fmt;          // format factor of V (64 for widened e2m3, else 1)
 
   const float* o_mul;
-  uint16_t* out;  // bf16 bits
+  uint16_t* out;  // bf16 (or fp16) bits
+  int out_f16;    // 1: out holds fp16
   int64_t out_ts, out_hs;
   float* lse;
 

@@ -114,7 +114,9 @@ class DecodeStep:
         a.with_reduction = 1 if info["with_reduction"] else 0
         a.chunk_tiles, a.max_splits, a.part_seqs = info["chunk_tiles"], self.max_splits, self.slots
         a.o_mul = kv.o_mul.data_ptr() if kv.o_mul is not None else None
+        assert out.dtype in (torch.bfloat16, torch.float16), "the decode output is bf16 or fp16"
         a.out = out.data_ptr()
+        a.out_dtype = 1 if out.dtype == torch.float16 else 0
         a.out_tok_stride, a.out_head_stride = out.stride(0), out.stride(1)
         a.lse = self.lse.data_ptr() if self.lse is not None else None
         a.workspace, a.workspace_bytes = self.workspace.data_ptr(), self.ws_bytes

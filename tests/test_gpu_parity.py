@@ -187,3 +187,33 @@ def test_tcgen05_rejects_what_it_cannot_run():
     with pytest.raises(mj.MjError) as e:
         run_gpu(w, impl=2)
     assert e.value.status == mj.MJ_ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------------------------------
+# fp16 output (T5DecodeRunner's out_dtype is bf16 or fp16)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["ragged_hnd", "spec_causal", "fp6_small"])
+def test_fp16_output(impl, name):
+    import torch
+
+    w = _case(name)
+    got = run_gpu(w, impl=impl, out_dtype=torch.float16)
+    ref, lse, _, _ = run_oracle(w)
+    compare(w, got["out"], ref, all_units(w), name + " fp16")
+    real = w.seq_lens > 0
+    np.testing.assert_allclose(got["lse"][real], lse[real], atol=2e-3, rtol=1e-4)
+    assert got["status"] == 0
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_fp16_output_split(impl):
+    """The split plan: the merge kernel writes the fp16 output."""
+    import torch
+
+    w = _case("split_nhd")
+    got = run_gpu(w, impl=impl, max_splits=16, out_dtype=torch.float16)
+    assert got["info"]["with_reduction"]
+    ref, _, _, _ = run_oracle(w)
+    compare(w, got["out"], ref, all_units(w), "split fp16")
+    assert got["status"] == 0

@@ -171,6 +171,36 @@ def cpu_baseline_child(workload: str, budget_s: float):
                       "bytes": nbytes}))
 
 
+# ----------------------------------------------------------------------------
+# replicas (one process per GPU under torchrun; weak scaling)
+# ----------------------------------------------------------------------------
+def replica_workload(name: str, rank: int):
+    """Rank r's batch: the Qwen3-8B decode batch is drawn with its own seed
+    per rank (independent replicas); the other workloads are the same batch
+    on every rank."""
+    import synth
+
+    if name == "qwen3_8b_decode":
+        return synth.WORKLOADS[name](seed=1002 + 17 * rank)
+    return synth.WORKLOADS[name]()
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The job's time is its slowest rank's: all-reduce MAX (a no-op alone)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(kv_bytes_per_rank: int, world: int, seconds_per_step: float) -> float:
+    """Whole-job throughput: the KV bytes every rank streamed per step over the step time."""
+    return kv_bytes_per_rank * world / seconds_per_step / 1e9
+
+
 def measure_write_kv(w, dev, peak: float) -> dict:
     """The KV-cache write that precedes a decode step (mj_write_kv), timed on
     its own: a bulk write of every token of the workload's batch (up to
@@ -306,8 +336,7 @@ def main_ours(args):
         cpu_base = run_cpu_baseline(args.workload)
 
     build()
-    w = synth.WORKLOADS[args.workload](seed=1002 + 17 * rank) if args.workload == "qwen3_8b_decode" else \
-        synth.WORKLOADS[args.workload]()
+    w = replica_workload(args.workload, rank)
     cps, msplit, stages = DEFAULT_KNOBS.get(args.workload, (2, 64, 0))
     cps = args.ctas_per_sm or cps
     msplit = args.max_splits or msplit
@@ -359,11 +388,7 @@ def main_ours(args):
         torch.cuda.synchronize(dev)
         if dist is not None:
             dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
 
     # ---- the decode kernel alone (roofline), CUDA events around each launch
     n_dec = max(10, min(args.steps, 200))
@@ -400,11 +425,7 @@ def main_ours(args):
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
 
     # the KV-cache write before the step (its own measurement, outside the timed step)
     write_kv = measure_write_kv(w, dev, _peaks()[0]) if rank == 0 else None
@@ -422,7 +443,7 @@ def main_ours(args):
         return
 
     ms_per_step = elapsed_ms / args.steps
-    value = kv_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(kv_bytes, world, ms_per_step * 1e-3)
     peak, peak_kind = _peaks()
     dec_avg_ms = sum(decode_ms) / len(decode_ms)
     achieved = kv_bytes / (dec_avg_ms * 1e-3) / 1e9
@@ -449,7 +470,7 @@ def main_ours(args):
         "tokens_per_s": round(tokens * world / (ms_per_step * 1e-3), 1),
         "plan_host_us": round(plan_us, 2),
         "clocks": clocks,
-        "e2e": {"value": round(kv_bytes * world / (e2e_s / e2e_steps) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(kv_bytes, world, e2e_s / e2e_steps), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
                 "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)},
         "gpu_launches": launches_per_step * args.steps,

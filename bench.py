@@ -283,6 +283,44 @@ def _cpu_children(workload: str, budget_s: float, n: int):
     return res
 
 
+def measure_bf16_q(w, kv, dev, peak: float, cps: int, msplit: int) -> dict | None:
+    """The decode step with bf16 Q as is (T5DecodeRunner's q_mode="bf16"):
+    decode (+ merge) only, timed on its own. e4m3 KV only."""
+    if w.kv_format != "fp8":
+        return None
+    import numpy as np
+    import torch
+
+    from paged_fp8_decode_gb300 import DecodeStep, mj_decode_attention, mj_merge_lse
+    from paged_fp8_decode_gb300.step import q_from_workload
+
+    q = q_from_workload(w, dev)
+    out = torch.empty(w.num_seqs * w.q_len, w.h_q, w.d, dtype=torch.bfloat16, device=dev)
+    step = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d, ctas_per_sm=cps,
+                      max_splits=msplit, causal=w.causal, device=dev, q_mode="bf16")
+    stream = torch.cuda.current_stream(dev)
+    step.plan(w.seq_lens, w.num_seqs, stream)
+    a = step.args(kv, out, w.num_seqs, w.softmax_scale, q=q)
+    for _ in range(3):
+        mj_decode_attention(a, stream)
+        mj_merge_lse(a, stream)
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(reps):
+        mj_decode_attention(a, stream)
+        mj_merge_lse(a, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.h_k * 2 * w.d
+    gbs = kv_bytes / (us * 1e-6) / 1e9
+    return {"kernel": "decode_simt", "us": round(us, 2), "gbs": round(gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4)}}
+
+
 def run_cpu_baseline(workload: str, budget_s: float = 10.0):
     """The oracle as it stands on the host cores: one single-threaded process
     per core at once (the aggregate rate), and one process alone."""
@@ -455,6 +493,7 @@ def main_ours(args):
 
     # the KV-cache write before the step (its own measurement, outside the timed step)
     write_kv = measure_write_kv(w, dev, _peaks()[0]) if rank == 0 else None
+    bf16_q = measure_bf16_q(w, kv, dev, _peaks()[0], cps, msplit) if rank == 0 else None
 
     # plan host time alone
     t0 = time.perf_counter()
@@ -507,6 +546,7 @@ def main_ours(args):
         "cpu_baseline": cpu_base,
         "device_status": status,
         "write_kv": write_kv,
+        "bf16_q": bf16_q,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

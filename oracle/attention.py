@@ -114,8 +114,10 @@ def visible_mask(L: int, q_len: int, h_r: int, causal: bool) -> np.ndarray:
     return j[None, :] <= (L - q_len + t)[:, None]
 
 
-def unit_logits(qcodes_bg, qdesc: float, kcodes, kdesc: float, kv_format: str, softmax_scale: float):
-    q = e4m3_decode(qcodes_bg) * float(qdesc)  # [n_q, d]
+def unit_logits(qcodes_bg, qdesc: float, kcodes, kdesc: float, kv_format: str, softmax_scale: float,
+                q_values=False):
+    """``q_values``: the rows are query values (bf16 mode), not e4m3 codes."""
+    q = np.asarray(qcodes_bg, dtype=np.float64) if q_values else e4m3_decode(qcodes_bg) * float(qdesc)  # [n_q, d]
     k = decode_codes(kcodes, kv_format) * float(kdesc)  # [L, d]
     return softmax_scale * (q @ k.T)  # [n_q, L]
 
@@ -132,8 +134,12 @@ def softmax_rows(s, vis):
 def decode_attention(q_codes, q_descale, k_logical, v_logical, k_descale, v_descale, block_table,
                      seq_lens, *, num_seqs: int, q_len: int, h_q: int, h_k: int, d: int,
                      page_size: int, kv_format: str, softmax_scale: float, causal: bool,
-                     o_mul=None, units=None):
+                     o_mul=None, units=None, q_values=False):
     """Full decode step.
+
+    ``q_values`` (the runner's bf16 Q mode, "Q as is"): ``q_codes`` holds the
+    query values in the packed row order (:func:`oracle.qquant.pack_q_rows`)
+    and ``q_descale`` is not used.
 
     Returns ``(out float64 [B*q_len, h_q, d], lse float64 [B, h_k, n_q])``;
     rows of requests with ``seq_len == 0`` (and of units not in ``units``
@@ -150,8 +156,8 @@ def decode_attention(q_codes, q_descale, k_logical, v_logical, k_descale, v_desc
         if L <= 0:
             continue
         kc, vc = gather_unit(k_logical, v_logical, block_table, b, g, L, page_size, kv_format)
-        s = unit_logits(q_codes[b, g], q_descale[b, g], kc, descale_at(k_descale, b, g), kv_format,
-                        softmax_scale)
+        s = unit_logits(q_codes[b, g], None if q_values else q_descale[b, g], kc, descale_at(k_descale, b, g),
+                        kv_format, softmax_scale, q_values=q_values)
         vis = visible_mask(L, q_len, h_r, causal)
         m, l, p = softmax_rows(s, vis)
         v = decode_codes(vc, kv_format) * descale_at(v_descale, b, g)

@@ -58,3 +58,15 @@ def quantize_q(q_f32, num_seqs: int, q_len: int, h_q: int, h_k: int, d: int, q_m
     codes = e4m3_encode(y)  # [B, ql, h_k, h_r, d]
     codes = codes.transpose(0, 2, 1, 3, 4).reshape(num_seqs, h_k, q_len * h_r, d)
     return np.ascontiguousarray(codes), scale
+
+
+def pack_q_rows(q_f32, num_seqs: int, q_len: int, h_q: int, h_k: int, d: int) -> np.ndarray:
+    """The bf16-Q mode (``q_mode="bf16"`` of ``T5DecodeRunner``: "Q as is"):
+    the query values themselves, in the same packed row order as the codes
+    (``[B, h_k, q_len*h_r, d]``, row ``t*h_r + r``), as float64."""
+    q = np.asarray(q_f32, dtype=np.float64)[: num_seqs * q_len]
+    assert q.shape == (num_seqs * q_len, h_q, d)
+    h_r = h_q // h_k
+    x = q.reshape(num_seqs, q_len, h_k, h_r, d).transpose(0, 2, 1, 3, 4)
+    return np.ascontiguousarray(x.reshape(num_seqs, h_k, q_len * h_r, d))
+

@@ -30,6 +30,9 @@ MJ_KV_E4M3 = 0
 MJ_KV_E2M3 = 1
 KV_FORMATS = {"fp8": MJ_KV_E4M3, "e2m3": MJ_KV_E2M3}
 
+MJ_Q_FP8 = 0
+MJ_Q_BF16 = 1
+
 MJ_OUT_BF16 = 0
 MJ_OUT_F16 = 1
 
@@ -78,6 +81,8 @@ class mj_decode_args(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("impl", ctypes.c_int), ("kv_stages", ctypes.c_int), ("evict_first", ctypes.c_int),
         ("out_dtype", ctypes.c_int),
+        ("q_mode", ctypes.c_int), ("q_bf16", ctypes.c_void_p),
+        ("q_tok_stride", ctypes.c_int64), ("q_head_stride", ctypes.c_int64),
     ]
 
 

@@ -10,7 +10,8 @@
 // into the result.
 //
 // This is the generic path: any row tile up to 32, any strides, e4m3 or
-// packed e2m3. The tensor-core kernel is the fast path.
+// packed e2m3, e4m3 Q codes or bf16 Q as is. The tensor-core kernel is the
+// fast path.
 #include "mj_device.cuh"
 #include "mj_internal.h"
 
@@ -81,18 +82,33 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // Q codes of this row tile -> shared floats (rows >= nr are zero).
+  // Q of this row tile -> shared floats (rows >= nr are zero): the e4m3
+  // codes (row t*h_r + r of the packed tile), or the bf16 Q as is (token t,
+  // query head g*h_r + r).
   const uint8_t* qrow = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
   for (int i = tid; i < NR * kHeadDim / 4; i += kThreads) {
     const int row = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
     float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (row < nr) e4m3x4_to_float(reinterpret_cast<const uint32_t*>(qrow + row * kHeadDim)[c4], v);
+    if (row < nr) {
+      if (p.q_bf16_mode) {
+        const int rr = r0 + row, tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
+        const uint2 u = *reinterpret_cast<const uint2*>(p.q_bf16 + int64_t(b * p.q_len + tq) * p.q_ts +
+                                                        int64_t(h) * p.q_hs + 4 * c4);
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+      } else {
+        e4m3x4_to_float(reinterpret_cast<const uint32_t*>(qrow + row * kHeadDim)[c4], v);
+      }
+    }
     *reinterpret_cast<float4*>(&qs[row][4 * c4]) = make_float4(v[0], v[1], v[2], v[3]);
   }
   __syncthreads();
 
   const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
-  const float scale = p.q_descale[int64_t(b) * p.h_k + g] * kd * p.qk_scale_log2;
+  const float qd = p.q_bf16_mode ? 1.f : p.q_descale[int64_t(b) * p.h_k + g];
+  const float scale = qd * kd * p.qk_scale_log2;
   const int64_t causal_base = int64_t(L) - p.q_len;  // query t sees key j iff j <= L - q_len + t
 
   float m[NR], l[NR], o[NR][4];

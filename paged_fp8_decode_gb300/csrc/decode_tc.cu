@@ -792,6 +792,7 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
 int tc_default_stages() { return 6; }
 
 bool tc_supported(const DecodeParams& p) {
+  if (p.q_bf16_mode) return false;  // the tensor-core kernel takes e4m3 Q codes
   if (p.kv_format == MJ_KV_E2M3) {
     // the packed TMA type wants 32-byte aligned strides (and base, checked
     // by the ABI for e2m3)

@@ -43,12 +43,21 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   if (a->num_pages < 1 || a->num_work < 0 || a->block_table_stride < 0) return MJ_ERR_INVALID_ARG;
   if (a->impl < MJ_IMPL_AUTO || a->impl > MJ_IMPL_TCGEN05) return MJ_ERR_INVALID_ARG;
   if (!(a->softmax_scale > 0.f) || !std::isfinite(a->softmax_scale)) return MJ_ERR_INVALID_ARG;
-  const void* need[] = {a->q_codes, a->q_descale, a->k_cache,  a->v_cache, a->k_descale, a->v_descale,
+  if (a->q_mode != MJ_Q_FP8 && a->q_mode != MJ_Q_BF16) return MJ_ERR_UNSUPPORTED;
+  const bool bf16_q = a->q_mode == MJ_Q_BF16;
+  if (bf16_q && a->kv_format != MJ_KV_E4M3) return MJ_ERR_UNSUPPORTED;  // e2m3 KV is fp8-Q only
+  const void* q0 = bf16_q ? a->q_bf16 : a->q_codes;
+  const void* q1 = bf16_q ? a->q_bf16 : a->q_descale;
+  const void* need[] = {q0, q1, a->k_cache,  a->v_cache, a->k_descale, a->v_descale,
                         a->block_table, a->seq_lens, a->work, a->n_splits, a->out, a->workspace};
   for (const void* ptr : need)
     if (!ptr) return MJ_ERR_INVALID_ARG;
+  if (bf16_q) {
+    if (a->q_tok_stride < 0 || a->q_head_stride < 0) return MJ_ERR_INVALID_ARG;
+    if (a->q_tok_stride % 8 || a->q_head_stride % 8) return MJ_ERR_ALIGNMENT;
+  }
   const uintptr_t kv_align = a->kv_format == MJ_KV_E2M3 ? 32 : 16;
-  const void* a16[] = {a->q_codes, a->q_descale, a->block_table, a->seq_lens, a->work,
+  const void* a16[] = {q0, q1, a->block_table, a->seq_lens, a->work,
                        a->n_splits, a->out, a->workspace};
   for (const void* ptr : a16)
     if (!aligned(ptr, 16)) return MJ_ERR_ALIGNMENT;
@@ -96,6 +105,10 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   q.n_row_tiles = n_row_tiles(n_q);
   q.q_codes = a->q_codes;
   q.q_descale = a->q_descale;
+  q.q_bf16_mode = a->q_mode == MJ_Q_BF16 ? 1 : 0;
+  q.q_bf16 = static_cast<const uint16_t*>(a->q_bf16);
+  q.q_ts = a->q_tok_stride;
+  q.q_hs = a->q_head_stride;
   q.k_cache = static_cast<const uint8_t*>(a->k_cache);
   q.v_cache = static_cast<const uint8_t*>(a->v_cache);
   q.k_sp = a->k_stride_page;

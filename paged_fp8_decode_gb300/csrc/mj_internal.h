@@ -32,6 +32,9 @@ struct DecodeParams {
 
   const uint8_t* q_codes;
   const float* q_descale;
+  int q_bf16_mode;          // 1: Q is q_bf16 as is (no codes, no descale)
+  const uint16_t* q_bf16;
+  int64_t q_ts, q_hs;       // element strides of q_bf16
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   int64_t k_sp, k_st, k_sh, v_sp, v_st, v_sh;  // byte strides (page, token, head)

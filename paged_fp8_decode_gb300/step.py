@@ -44,7 +44,11 @@ class DecodeStep:
     def __init__(self, *, max_num_seqs: int, q_len: int, h_q: int, h_k: int, d: int = 128,
                  sm_count: int | None = None, ctas_per_sm: int = 2, max_splits: int = 16,
                  margin: int = 0, causal: bool = True, impl: int = MJ_IMPL_AUTO, kv_stages: int = 0,
-                 evict_first: bool = True, device="cuda", with_lse: bool = False):
+                 evict_first: bool = True, device="cuda", with_lse: bool = False, q_mode: str = "fp8"):
+        """``q_mode``: "fp8" (dynamic e4m3 Q, mj_quantize_q in the step) or
+        "bf16" (Q as is; the step is decode + merge)."""
+        assert q_mode in ("fp8", "bf16")
+        self.q_mode = q_mode
         self.device = torch.device(device)
         if sm_count is None:
             sm_count = torch.cuda.get_device_properties(self.device).multi_processor_count
@@ -94,9 +98,15 @@ class DecodeStep:
         return info
 
     # ------------------------------------------------------------- the calls
-    def args(self, kv: PagedKV, out: torch.Tensor, num_seqs: int, softmax_scale: float) -> mj_decode_args:
+    def args(self, kv: PagedKV, out: torch.Tensor, num_seqs: int, softmax_scale: float,
+             q: torch.Tensor | None = None) -> mj_decode_args:
+        """The decode call's arguments; ``q`` (bf16 mode): the bf16 Q it reads."""
         info = self.plan_info
         a = mj_decode_args()
+        if self.q_mode == "bf16":
+            assert q is not None and q.dtype == torch.bfloat16 and q.stride(2) == 1
+            a.q_mode, a.q_bf16 = 1, q.data_ptr()
+            a.q_tok_stride, a.q_head_stride = q.stride(0), q.stride(1)
         a.num_seqs, a.q_len, a.h_q, a.h_k, a.d = num_seqs, self.q_len, self.h_q, self.h_k, self.d
         a.causal = 1 if self.causal else 0
         a.softmax_scale = softmax_scale
@@ -125,10 +135,11 @@ class DecodeStep:
 
     def run(self, q: torch.Tensor, out: torch.Tensor, kv: PagedKV, num_seqs: int, softmax_scale: float,
             stream=None, args: mj_decode_args | None = None):
-        """Quantize Q, decode, merge: the device part of one step."""
-        mj_quantize_q(q, num_seqs, self.q_len, self.h_k, self.q_codes, self.q_descale, q_mul=kv.q_mul,
-                      stream=stream)
-        a = args if args is not None else self.args(kv, out, num_seqs, softmax_scale)
+        """Quantize Q (fp8 mode), decode, merge: the device part of one step."""
+        if self.q_mode == "fp8":
+            mj_quantize_q(q, num_seqs, self.q_len, self.h_k, self.q_codes, self.q_descale, q_mul=kv.q_mul,
+                          stream=stream)
+        a = args if args is not None else self.args(kv, out, num_seqs, softmax_scale, q=q)
         mj_decode_attention(a, stream)
         mj_merge_lse(a, stream)
         return out

@@ -15,7 +15,7 @@ ATOL_MEAN = 2e-3  # mean |err| <= 2e-3 * max|V|
 
 
 def run_gpu(w, *, impl=0, ctas_per_sm=2, max_splits=16, margin=0, plan_lens=None, sm_count=None,
-            kv_stages=0, out_strided=False, descale_per_seq=False, steps=1, out_dtype=None):
+            kv_stages=0, out_strided=False, descale_per_seq=False, steps=1, out_dtype=None, q_mode="fp8"):
     import torch
 
     from paged_fp8_decode_gb300 import DecodeStep, mj_workspace_status
@@ -31,7 +31,7 @@ def run_gpu(w, *, impl=0, ctas_per_sm=2, max_splits=16, margin=0, plan_lens=None
     q = q_from_workload(w)
     step = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
                       sm_count=sm_count, ctas_per_sm=ctas_per_sm, max_splits=max_splits, margin=margin,
-                      causal=w.causal, impl=impl, kv_stages=kv_stages, with_lse=True)
+                      causal=w.causal, impl=impl, kv_stages=kv_stages, with_lse=True, q_mode=q_mode)
     odt = torch.bfloat16 if out_dtype is None else out_dtype
     if out_strided:  # O rows inside a wider buffer (like a fused QKV/O layout)
         big = torch.full((w.num_seqs * w.q_len, w.h_q + 8, w.d + 64), SENTINEL, dtype=odt, device="cuda")
@@ -56,13 +56,18 @@ def run_gpu(w, *, impl=0, ctas_per_sm=2, max_splits=16, margin=0, plan_lens=None
     }
 
 
-def run_oracle(w, units=None):
+def run_oracle(w, units=None, q_mode="fp8"):
     codes, desc = oracle_quantize_q(w.q_f32, w.num_seqs, w.q_len, w.h_q, w.h_k, w.d, w.q_mul)
-    out, lse = OA.decode_attention(codes, desc, w.logical("k"), w.logical("v"), w.k_scale, w.v_scale,
+    qin = codes
+    if q_mode == "bf16":  # the values as is, in the same packed row order
+        from oracle.qquant import pack_q_rows
+
+        qin = pack_q_rows(w.q_f32, w.num_seqs, w.q_len, w.h_q, w.h_k, w.d)
+    out, lse = OA.decode_attention(qin, desc, w.logical("k"), w.logical("v"), w.k_scale, w.v_scale,
                                    w.block_table, w.seq_lens, num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q,
                                    h_k=w.h_k, d=w.d, page_size=w.page_size, kv_format=w.kv_format,
                                    softmax_scale=w.softmax_scale, causal=w.causal, o_mul=w.o_mul,
-                                   units=units)
+                                   units=units, q_values=(q_mode == "bf16"))
     return out, lse, codes, desc
 
 

@@ -120,6 +120,7 @@ def _valid_args():
     ("workspace_bytes", 16, mj.MJ_ERR_CAPACITY),
     ("impl", 9, mj.MJ_ERR_INVALID_ARG),
     ("out_dtype", 2, mj.MJ_ERR_UNSUPPORTED),
+    ("q_mode", 2, mj.MJ_ERR_UNSUPPORTED),
 ])
 def test_decode_args_rejected_on_host(lib, field, value, status):
     a = _valid_args()
@@ -207,3 +208,14 @@ def test_write_kv_nothing_to_do(lib):
     a.num_tokens = 0
     a.key = a.value = a.slot_mapping = None  # nothing is read when there are no tokens
     assert lib.mj_write_kv(ctypes.byref(a), None) == mj.MJ_OK
+
+
+def test_bf16_q_mode_host_checks(lib):
+    a = _valid_args()
+    a.q_mode, a.q_bf16 = mj.MJ_Q_BF16, None
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_INVALID_ARG
+    a.q_bf16, a.q_tok_stride, a.q_head_stride = (1 << 40) + 0x9000, 4096, 132
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_ALIGNMENT
+    a.q_head_stride = 128
+    a.kv_format = mj.MJ_KV_E2M3  # e2m3 KV is fp8-Q only
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_UNSUPPORTED

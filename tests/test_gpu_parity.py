@@ -217,3 +217,43 @@ def test_fp16_output_split(impl):
     ref, _, _, _ = run_oracle(w)
     compare(w, got["out"], ref, all_units(w), "split fp16")
     assert got["status"] == 0
+
+
+# ----------------------------------------------------------------------------
+# bf16 Q as is (T5DecodeRunner's q_mode="bf16"; e4m3 KV only)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("impl", [0, 1])  # AUTO (the CUDA-core kernel takes it) and SIMT
+@pytest.mark.parametrize("name", ["ragged_hnd", "spec_causal", "spec_noncausal"])
+def test_bf16_q(impl, name):
+    w = _case(name)
+    got = run_gpu(w, impl=impl, q_mode="bf16")
+    ref, lse, _, _ = run_oracle(w, q_mode="bf16")
+    compare(w, got["out"], ref, all_units(w), name + " bf16 Q")
+    real = w.seq_lens > 0
+    np.testing.assert_allclose(got["lse"][real], lse[real], atol=2e-3, rtol=1e-4)
+    assert got["status"] == 0
+
+
+def test_bf16_q_split_and_full_size():
+    w = _case("split_nhd")
+    got = run_gpu(w, impl=0, max_splits=16, q_mode="bf16")
+    assert got["info"]["with_reduction"]
+    ref, _, _, _ = run_oracle(w, q_mode="bf16")
+    compare(w, got["out"], ref, all_units(w), "split bf16 Q")
+    w = synth.WORKLOADS["qwen3_8b_decode"]()
+    got = run_gpu(w, impl=0, ctas_per_sm=2, max_splits=64, q_mode="bf16")
+    units = sorted(set(sample_units(w, 6, seed=5)) | {(w.num_seqs - 1, w.h_k - 1)})
+    ref, _, _, _ = run_oracle(w, units=units, q_mode="bf16")
+    compare(w, got["out"], ref, units, "qwen3 bf16 Q")
+    assert got["status"] == 0
+
+
+def test_bf16_q_rejections():
+    import paged_fp8_decode_gb300 as mj
+
+    with pytest.raises(mj.MjError) as e:  # the tensor-core kernel takes e4m3 Q codes only
+        run_gpu(_case("ragged_hnd"), impl=2, q_mode="bf16")
+    assert e.value.status == mj.MJ_ERR_UNSUPPORTED
+    with pytest.raises(mj.MjError) as e:  # packed e2m3 KV is fp8-Q only
+        run_gpu(_case("fp6_small"), impl=0, q_mode="bf16")
+    assert e.value.status == mj.MJ_ERR_UNSUPPORTED

@@ -188,3 +188,75 @@ def test_bf16_rounding():
     x = np.random.default_rng(0).standard_normal(10000).astype(np.float32)
     ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
     np.testing.assert_array_equal(A.to_bf16(x.astype(np.float64)), ref)
+
+
+# ----------------------------------------------------------------------------
+# the bf16-Q mode ("Q as is")
+# ----------------------------------------------------------------------------
+def _run_bf16(w, units=None):
+    from oracle.qquant import pack_q_rows
+
+    qv = pack_q_rows(w.q_f32, w.num_seqs, w.q_len, w.h_q, w.h_k, w.d)
+    return A.decode_attention(
+        qv, None, w.logical("k"), w.logical("v"), w.k_scale, w.v_scale, w.block_table,
+        w.seq_lens, num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
+        page_size=w.page_size, kv_format=w.kv_format, softmax_scale=w.softmax_scale,
+        causal=w.causal, o_mul=w.o_mul, units=units, q_values=True)
+
+
+def test_bf16_q_row_order():
+    from oracle.qquant import pack_q_rows
+
+    B, ql, hq, hk, d = 2, 3, 6, 2, 4
+    q = np.zeros((B * ql, hq, d))
+    for tok in range(B * ql):
+        for h in range(hq):
+            q[tok, h] = 1000 * tok + 10 * h + np.arange(d) * 0.1  # the value names its place
+    packed = pack_q_rows(q, B, ql, hq, hk, d)
+    hr = hq // hk
+    for b in range(B):
+        for g in range(hk):
+            for t in range(ql):
+                for r in range(hr):
+                    assert np.array_equal(packed[b, g, t * hr + r], q[b * ql + t, g * hr + r])
+
+
+def test_bf16_q_mode_equals_fp8_mode_on_representable_q():
+    # Q set to its own dequantised e4m3 codes: both modes see the same values
+    w = _small(q_len=2, seq_lens=[7, 40, 19])
+    codes, desc = quantize_q(w.q_f32, w.num_seqs, w.q_len, w.h_q, w.h_k, w.d, w.q_mul)
+    deq = F.e4m3_decode(codes) * desc[:, :, None, None]  # [B, h_k, n_q, d]
+    hr = w.h_r
+    q = np.zeros_like(w.q_f32, dtype=np.float64)
+    for b in range(w.num_seqs):
+        for g in range(w.h_k):
+            for row in range(w.n_q):
+                t, r = divmod(row, hr)
+                q[b * w.q_len + t, g * hr + r] = deq[b, g, row]
+    w.q_f32 = q
+    out_fp8 = _run(w)[2]
+    out_bf16, _ = _run_bf16(w)
+    np.testing.assert_allclose(out_bf16, out_fp8, rtol=1e-12, atol=1e-14)
+
+
+def test_bf16_q_mode_matches_brute_force():
+    w = _small(q_len=2, seq_lens=[6, 30, 11], causal=True)
+    out, _ = _run_bf16(w)
+    for b in range(w.num_seqs):
+        L = int(w.seq_lens[b])
+        for g in range(w.h_k):
+            kc, vc = A.gather_unit(w.logical("k"), w.logical("v"), w.block_table, b, g, L, w.page_size)
+            k = F.e4m3_decode(kc) * A.descale_at(w.k_scale, b, g)
+            v = F.e4m3_decode(vc) * A.descale_at(w.v_scale, b, g)
+            for t in range(w.q_len):
+                for r in range(w.h_r):
+                    qrow = np.asarray(w.q_f32[b * w.q_len + t, g * w.h_r + r], dtype=np.float64)
+                    logits, vals = [], []
+                    for j in range(L):
+                        if j <= L - w.q_len + t:  # causal
+                            logits.append(w.softmax_scale * float(qrow @ k[j]))
+                            vals.append(v[j])
+                    mx = max(logits)
+                    wts = [math.exp(s - mx) for s in logits]
+                    want = sum(wt * vv for wt, vv in zip(wts, vals)) / sum(wts)
+                    np.testing.assert_allclose(out[b * w.q_len + t, g * w.h_r + r], want, rtol=1e-10, atol=1e-12)

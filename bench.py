@@ -285,7 +285,8 @@ def _cpu_children(workload: str, budget_s: float, n: int):
 
 def measure_bf16_q(w, kv, dev, peak: float, cps: int, msplit: int) -> dict | None:
     """The decode step with bf16 Q as is (T5DecodeRunner's q_mode="bf16"):
-    decode (+ merge) only, timed on its own. e4m3 KV only."""
+    decode (+ merge) only, timed on its own. e4m3 KV only. The tensor-core
+    kernel carries each Q value as two e4m3 terms."""
     if w.kv_format != "fp8":
         return None
     import numpy as np
@@ -316,7 +317,7 @@ def measure_bf16_q(w, kv, dev, peak: float, cps: int, msplit: int) -> dict | Non
     us = e0.elapsed_time(e1) * 1e3 / reps
     kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.h_k * 2 * w.d
     gbs = kv_bytes / (us * 1e-6) / 1e9
-    return {"kernel": "decode_simt", "us": round(us, 2), "gbs": round(gbs, 1),
+    return {"kernel": "decode_tc (Q as two e4m3 terms)", "us": round(us, 2), "gbs": round(gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4)}}
 

@@ -94,6 +94,7 @@ struct Ctrl {
   alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
   alignas(16) float lsum[4][32];    // row sums of the 4 softmax warps
   float alpha[4][32];               // per softmax warp: the rescale factors of the current tiles
+  float qamax[2][4];                // bf16 Q: per softmax warp, |x| max and |residual| max
 };
 static_assert(sizeof(Ctrl) <= 3072, "control block");
 static_assert(offsetof(Ctrl, red) % 16 == 0 && offsetof(Ctrl, lsum) % 16 == 0, "float4 access to red/lsum");
@@ -151,12 +152,15 @@ __device__ __forceinline__ uint4 widen_chunk(uint4 in) {
   return o;
 }
 
-template <int NQK, int NPV, int NR, bool FP6>
+// BQ: bf16 Q as is, represented as two e4m3 terms per value (see the Q
+// staging in the softmax warps).
+template <int NQK, int NPV, int NR, bool FP6, bool BQ = false>
 __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 2 : 1))
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
   constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
   static_assert(NH <= NQK && NR <= NH && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
+  static_assert(!BQ || (!FP6 && 2 * NR <= NQK), "bf16 Q: e4m3 KV, hi and lo rows in the Q tile");
   // TP tiles per softmax iteration; NSB S and P buffers let QK run up to
   // NSB - 1 tiles ahead of PV.
   constexpr int TP = NR <= 8 ? 2 : 1;
@@ -420,10 +424,11 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
     // it is launched just before: wait for it here only, so that the TMA
     // producers stream KV meanwhile.
     tc::grid_dependency_wait();
-    {
+    const int xq = tid - kSoftmaxWarp0 * 32;
+    float sc_hi = 0.f, sc_lo = 0.f;  // bf16 Q: logit scales of its hi and lo terms
+    if constexpr (!BQ) {
       // Q codes rows r0 .. r0+nr-1 -> Q tile [NQK rows][128 B], K-major,
       // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); other rows 0.
-      const int xq = tid - kSoftmaxWarp0 * 32;
       const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
       for (int i = xq; i < NQK * 8; i += 128) {
         const int r = i >> 3, c = i & 7;
@@ -431,14 +436,90 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
         if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * kHeadDim + c * 16);
         *reinterpret_cast<uint4*>(smem + lay.q + r * 128 + ((c ^ (r & 7)) << 4)) = v;
       }
-      tc::fence_async_smem();
-      tc::mbar_arrive(tc::smem_u32(&ctl.q_ready));
+    } else {
+      // bf16 Q as two e4m3 terms: hi = e4m3(x / s_hi) with s_hi = amax/448,
+      // lo = e4m3((x - hi*s_hi) / s_lo) with s_lo = (max |residual|)/448.
+      // hi fills rows 0 .. NR-1 of the Q tile and lo rows NR .. 2NR-1, so one
+      // QK product gives both terms; the logit is s_hi*S_hi + s_lo*S_lo.
+      // Thread xq owns NR consecutive channels of one row (NR x 128 values
+      // over 128 threads).
+      constexpr int EPT = NR;
+      const int row = (xq * EPT) / kHeadDim, c0 = (xq * EPT) % kHeadDim;
+      float xv[EPT];
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) xv[e] = 0.f;
+      if (row < nr) {
+        const int rr = r0 + row, tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
+        const uint16_t* src = p.q_bf16 + int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c0;
+#pragma unroll
+        for (int e = 0; e < EPT; e += 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(src + e);
+          xv[e] = __uint_as_float(u.x << 16);
+          xv[e + 1] = __uint_as_float(u.x & 0xFFFF0000u);
+          xv[e + 2] = __uint_as_float(u.y << 16);
+          xv[e + 3] = __uint_as_float(u.y & 0xFFFF0000u);
+        }
+      }
+      // max over the 128 softmax threads (the four softmax warps always reach this barrier)
+      auto block_max = [&](float v, int slot) {
+        v = warp_max(v);
+        if (lane == 0) ctl.qamax[slot][warp & 3] = v;
+        tc::named_bar_sync(1, 128);
+        return fmaxf(fmaxf(ctl.qamax[slot][0], ctl.qamax[slot][1]), fmaxf(ctl.qamax[slot][2], ctl.qamax[slot][3]));
+      };
+      float am = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) am = fmaxf(am, fabsf(xv[e]));
+      const float s_hi = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.f);
+      uint32_t hw[EPT / 4];
+      float rm = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPT; e += 2) {
+        const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(xv[e], s_hi), __fdiv_rn(xv[e + 1], s_hi)), __NV_SATFINITE, __NV_E4M3);
+        const float2 hv = e4m3x2_to_float2(h2);
+        xv[e] -= hv.x * s_hi;  // the residual
+        xv[e + 1] -= hv.y * s_hi;
+        rm = fmaxf(rm, fmaxf(fabsf(xv[e]), fabsf(xv[e + 1])));
+        if ((e & 3) == 0)
+          hw[e / 4] = uint32_t(h2);
+        else
+          hw[e / 4] |= uint32_t(h2) << 16;
+      }
+      const float rmax = block_max(rm, 1);
+      const float s_lo = rmax > 0.f ? __fdiv_rn(rmax, 448.f) : 1.f;
+      uint32_t lw[EPT / 4];
+#pragma unroll
+      for (int e = 0; e < EPT; e += 2) {
+        const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(xv[e], s_lo), __fdiv_rn(xv[e + 1], s_lo)), __NV_SATFINITE, __NV_E4M3);
+        if ((e & 3) == 0)
+          lw[e / 4] = uint32_t(l2);
+        else
+          lw[e / 4] |= uint32_t(l2) << 16;
+      }
+      // 4 codes per word; byte (c & 15) of 16-byte chunk (c >> 4) ^ (row & 7)
+#pragma unroll
+      for (int e = 0; e < EPT; e += 4) {
+        const int c = c0 + e;
+        const int r_hi = row, r_lo = NR + row;
+        *reinterpret_cast<uint32_t*>(smem + lay.q + r_hi * 128 + (((c >> 4) ^ (r_hi & 7)) << 4) + (c & 15)) = hw[e / 4];
+        *reinterpret_cast<uint32_t*>(smem + lay.q + r_lo * 128 + (((c >> 4) ^ (r_lo & 7)) << 4) + (c & 15)) = lw[e / 4];
+      }
+      for (int i = xq; i < (NQK - 2 * NR) * 8; i += 128)  // the rows past the two terms
+        *reinterpret_cast<uint4*>(smem + lay.q + 2 * NR * 128 + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+      const float kq = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g) * p.qk_scale_log2;
+      sc_hi = s_hi * kq;
+      sc_lo = s_lo * kq;
     }
+    tc::fence_async_smem();
+    tc::mbar_arrive(tc::smem_u32(&ctl.q_ready));
     const int qd = warp & 3;          // TMEM lane quadrant of this warp
     const int x = qd * 32 + lane;     // key of the tile (S) / channel (O)
     const uint32_t lane_off = uint32_t(qd * 32) << 16;
     const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
-    const float scale = p.q_descale[int64_t(b) * p.h_k + g] * kd * p.qk_scale_log2;
+    // bf16 Q: the logits are formed when S is read (scale 1 below)
+    const float scale = BQ ? 1.f : p.q_descale[int64_t(b) * p.h_k + g] * kd * p.qk_scale_log2;
     // last visible key of each row (query token t sees keys j <= L - q_len + t)
     int lim[NR];
 #pragma unroll
@@ -476,16 +557,29 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       }
       if (!ok) break;
       tc::tc_fence_after();
+      if constexpr (!BQ) {
 #pragma unroll
-      for (int a = 0; a < TP; ++a) {
-        if (a < nt) {
-          tc::tmem_ld_cols<NR>(tS(i + a) + lane_off, s[a]);
-        } else {
+        for (int a = 0; a < TP; ++a) {
+          if (a < nt) {
+            tc::tmem_ld_cols<NR>(tS(i + a) + lane_off, s[a]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < NR; ++c) s[a][c] = -INFINITY;
+            for (int c = 0; c < NR; ++c) s[a][c] = -INFINITY;
+          }
         }
+        tc::tmem_wait_ld();
+      } else {
+        // columns 0 .. NR-1: the hi term's products, NR .. 2NR-1: the lo term's
+        float s2[TP][2 * NR];
+#pragma unroll
+        for (int a = 0; a < TP; ++a)
+          if (a < nt) tc::tmem_ld_cols<2 * NR>(tS(i + a) + lane_off, s2[a]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int a = 0; a < TP; ++a)
+#pragma unroll
+          for (int c = 0; c < NR; ++c) s[a][c] = a < nt ? fmaf(s2[a][NR + c], sc_lo, s2[a][c] * sc_hi) : -INFINITY;
       }
-      tc::tmem_wait_ld();
 
       int key[TP];
       bool valid[TP];
@@ -762,13 +856,13 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   return r == CUDA_SUCCESS;
 }
 
-template <int NQK, int NPV, int NR, bool FP6>
+template <int NQK, int NPV, int NR, bool FP6, bool BQ = false>
 cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
   const TcSmem lay = tc_smem_layout(p.kv_stages, NQK, NPV, NR <= 8 ? 4 : 2);
   const int bytes = int(lay.total) + 1024;
   static int configured = 0;  // largest dynamic smem size set so far
   if (bytes > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6, BQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bytes);
     if (e != cudaSuccess) return e;
     configured = bytes;
@@ -784,7 +878,7 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6>, mk, mv, p);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6, BQ>, mk, mv, p);
 }
 
 }  // namespace
@@ -792,7 +886,7 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
 int tc_default_stages() { return 6; }
 
 bool tc_supported(const DecodeParams& p) {
-  if (p.q_bf16_mode) return false;  // the tensor-core kernel takes e4m3 Q codes
+  if (p.q_bf16_mode && p.kv_format != MJ_KV_E4M3) return false;
   if (p.kv_format == MJ_KV_E2M3) {
     // the packed TMA type wants 32-byte aligned strides (and base, checked
     // by the ABI for e2m3)
@@ -854,6 +948,14 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
       return launch_tc<16, 32, 16, true>(mk, mv, p, stream);
     }
     return launch_tc<32, 64, 32, true>(mk, mv, p, stream);
+  }
+  if (p.q_bf16_mode) {  // the Q tile holds two rows (hi, lo) per query row
+    if (p.tw <= 16) {
+      if (p.n_q <= 4) return launch_tc<16, 16, 4, false, true>(mk, mv, p, stream);
+      if (p.n_q <= 8) return launch_tc<16, 16, 8, false, true>(mk, mv, p, stream);
+      return launch_tc<32, 32, 16, false, true>(mk, mv, p, stream);
+    }
+    return launch_tc<64, 64, 32, false, true>(mk, mv, p, stream);
   }
   if (p.tw <= 16) {
     if (p.n_q <= 4) return launch_tc<16, 16, 4, false>(mk, mv, p, stream);

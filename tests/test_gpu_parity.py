@@ -222,38 +222,47 @@ def test_fp16_output_split(impl):
 # ----------------------------------------------------------------------------
 # bf16 Q as is (T5DecodeRunner's q_mode="bf16"; e4m3 KV only)
 # ----------------------------------------------------------------------------
-@pytest.mark.parametrize("impl", [0, 1])  # AUTO (the CUDA-core kernel takes it) and SIMT
-@pytest.mark.parametrize("name", ["ragged_hnd", "spec_causal", "spec_noncausal"])
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["ragged_hnd", "spec_causal", "spec_noncausal", "wide_rows"])
 def test_bf16_q(impl, name):
-    w = _case(name)
+    """The CUDA-core kernel uses Q exactly; the tensor-core kernel carries each
+    value as two e4m3 terms (hi + lo, per-(request, KV head) scales)."""
+    if name == "wide_rows":  # 32 query rows per (request, KV head): the widest row tile
+        w = synth.make_case(name=name, num_seqs=3, q_len=4, h_q=64, h_k=8, page_size=32, seq_lens=[50, 700, 129],
+                            layout="HND", scale_mode="head", seed=26)
+    else:
+        w = _case(name)
     got = run_gpu(w, impl=impl, q_mode="bf16")
     ref, lse, _, _ = run_oracle(w, q_mode="bf16")
     compare(w, got["out"], ref, all_units(w), name + " bf16 Q")
     real = w.seq_lens > 0
-    np.testing.assert_allclose(got["lse"][real], lse[real], atol=2e-3, rtol=1e-4)
-    assert got["status"] == 0
+    # Two e4m3 terms carry each Q value to ~2^-8 relative (bf16's own step),
+    # so the tensor-core kernel's logits, and the LSE, move by up to about
+    # 2^-8 * |q| |k| * softmax_scale (~4e-3 here); the CUDA-core kernel uses Q exactly.
+    np.testing.assert_allclose(got["lse"][real], lse[real], atol=1e-2 if impl == 2 else 2e-3, rtol=1e-4)
+    assert got["status"] == 0, f"device status {got['status']}"
 
 
-def test_bf16_q_split_and_full_size():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_bf16_q_split_and_full_size(impl):
     w = _case("split_nhd")
-    got = run_gpu(w, impl=0, max_splits=16, q_mode="bf16")
+    got = run_gpu(w, impl=impl, max_splits=16, q_mode="bf16")
     assert got["info"]["with_reduction"]
     ref, _, _, _ = run_oracle(w, q_mode="bf16")
     compare(w, got["out"], ref, all_units(w), "split bf16 Q")
     w = synth.WORKLOADS["qwen3_8b_decode"]()
-    got = run_gpu(w, impl=0, ctas_per_sm=2, max_splits=64, q_mode="bf16")
+    got = run_gpu(w, impl=impl, ctas_per_sm=2, max_splits=64, kv_stages=6, q_mode="bf16")
     units = sorted(set(sample_units(w, 6, seed=5)) | {(w.num_seqs - 1, w.h_k - 1)})
     ref, _, _, _ = run_oracle(w, units=units, q_mode="bf16")
     compare(w, got["out"], ref, units, "qwen3 bf16 Q")
+    real_rows = np.repeat(w.seq_lens > 0, w.q_len)
+    assert np.all(np.isfinite(got["out"][real_rows]))
     assert got["status"] == 0
 
 
 def test_bf16_q_rejections():
     import paged_fp8_decode_gb300 as mj
 
-    with pytest.raises(mj.MjError) as e:  # the tensor-core kernel takes e4m3 Q codes only
-        run_gpu(_case("ragged_hnd"), impl=2, q_mode="bf16")
-    assert e.value.status == mj.MJ_ERR_UNSUPPORTED
     with pytest.raises(mj.MjError) as e:  # packed e2m3 KV is fp8-Q only
         run_gpu(_case("fp6_small"), impl=0, q_mode="bf16")
     assert e.value.status == mj.MJ_ERR_UNSUPPORTED

@@ -413,18 +413,20 @@ def main_ours(args):
     q = q_from_workload(w, dev)
     out = torch.empty(w.num_seqs * w.q_len, w.h_q, w.d, dtype=torch.bfloat16, device=dev)
     step = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d, ctas_per_sm=cps,
-                      max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages, device=dev)
+                      max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages, device=dev,
+                      q_mode=args.q_mode)
     stream = torch.cuda.current_stream(dev)
     info = step.plan(w.seq_lens, w.num_seqs, stream)
-    a = step.args(kv, out, w.num_seqs, w.softmax_scale)
+    a = step.args(kv, out, w.num_seqs, w.softmax_scale, q=q)
     row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
     kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.h_k * 2 * row
     tokens = int((w.seq_lens > 0).sum()) * w.q_len
-    launches_per_step = 2 + (1 if info["with_reduction"] else 0)
+    launches_per_step = (1 if args.q_mode == "fp8" else 0) + 1 + (1 if info["with_reduction"] else 0)
 
     def device_step(ev=None):
-        mj_quantize_q(q, w.num_seqs, w.q_len, w.h_k, step.q_codes, step.q_descale, q_mul=kv.q_mul,
-                      stream=stream)
+        if args.q_mode == "fp8":  # otherwise the decode kernel quantizes Q itself (or takes it as is)
+            mj_quantize_q(q, w.num_seqs, w.q_len, w.h_k, step.q_codes, step.q_descale, q_mul=kv.q_mul,
+                          stream=stream)
         if ev is not None:
             ev[0].record(stream)
         mj_decode_attention(a, stream)
@@ -492,6 +494,35 @@ def main_ours(args):
         e2e_step()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
 
+    # the same step with the separate quantize launch, for comparison
+    unfused = None
+    if args.q_mode == "fp8_fused" and rank == 0:
+        step_u = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
+                            ctas_per_sm=cps, max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages,
+                            device=dev)
+        step_u.plan(w.seq_lens, w.num_seqs, stream)
+        a_u = step_u.args(kv, out, w.num_seqs, w.softmax_scale)
+        n_u = max(10, min(args.steps, 500))
+
+        def step_unfused():
+            mj_quantize_q(q, w.num_seqs, w.q_len, w.h_k, step_u.q_codes, step_u.q_descale, q_mul=kv.q_mul,
+                          stream=stream)
+            mj_decode_attention(a_u, stream)
+            mj_merge_lse(a_u, stream)
+
+        for _ in range(3):
+            step_unfused()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n_u):
+            step_unfused()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_u = e0.elapsed_time(e1) / n_u
+        unfused = {"ms_per_step": round(ms_u, 5), "value": round(whole_job_gbs(kv_bytes, 1, ms_u * 1e-3), 2),
+                   "unit": "GB/s", "steps": n_u, "note": "mj_quantize_q as its own launch before the decode"}
+
     # the KV-cache write before the step (its own measurement, outside the timed step)
     write_kv = measure_write_kv(w, dev, _peaks()[0]) if rank == 0 else None
     bf16_q = measure_bf16_q(w, kv, dev, _peaks()[0], cps, msplit) if rank == 0 else None
@@ -527,6 +558,7 @@ def main_ours(args):
             "kv_format": w.kv_format, "causal": w.causal, "parallelism": f"replicas{world}",
             "l2": f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step vs 129 MB L2, no flush",
             "ctas_per_sm": cps, "max_splits": msplit, "kv_stages": stages, "variant": args.variant,
+            "q_mode": args.q_mode,
             "with_reduction": info["with_reduction"], "chunk_tiles": info["chunk_tiles"],
             "num_work": info["num_work"],
         },
@@ -547,6 +579,7 @@ def main_ours(args):
         "cpu_baseline": cpu_base,
         "device_status": status,
         "write_kv": write_kv,
+        "unfused_step": unfused,
         "bf16_q": bf16_q,
     }
     print(json.dumps(line), flush=True)
@@ -562,6 +595,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_decode")
     ap.add_argument("--variant", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--q-mode", default="fp8_fused", choices=["fp8", "fp8_fused", "bf16"],
+                    help="fp8: mj_quantize_q then decode; fp8_fused: the same quantization inside the "
+                         "decode kernel (bit-identical output); bf16: Q as is")
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--max-splits", type=int, default=0)
     ap.add_argument("--kv-stages", type=int, default=None)

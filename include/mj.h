@@ -66,11 +66,15 @@ typedef enum mj_kv_format {
   MJ_KV_E2M3 = 1   /* packed e2m3: 4 codes per 3 bytes, little-endian bitstream; row = d*3/4 bytes */
 } mj_kv_format;
 
-/* How the decode call takes Q (T5DecodeRunner's q_mode): MJ_Q_FP8 — the
- * e4m3 codes and per-(request, KV head) descales mj_quantize_q wrote;
- * MJ_Q_BF16 — the bf16 Q as is (e4m3 KV only, as on the runner page: packed
- * e2m3 is "fp8 Q only"). */
-typedef enum mj_q_mode { MJ_Q_FP8 = 0, MJ_Q_BF16 = 1 } mj_q_mode;
+/* How the decode call takes Q (T5DecodeRunner's q_mode):
+ *   MJ_Q_FP8       — the e4m3 codes and per-(request, KV head) descales
+ *                    mj_quantize_q wrote;
+ *   MJ_Q_BF16      — the bf16 Q as is (e4m3 KV only, as on the runner page:
+ *                    packed e2m3 is "fp8 Q only");
+ *   MJ_Q_FP8_FUSED — the bf16 Q, quantized by the decode kernel itself with
+ *                    mj_quantize_q's recipe (same codes, same descales), so
+ *                    the step needs no separate quantize launch. */
+typedef enum mj_q_mode { MJ_Q_FP8 = 0, MJ_Q_BF16 = 1, MJ_Q_FP8_FUSED = 2 } mj_q_mode;
 
 /* Element type of the decode output (T5DecodeRunner's out_dtype: bf16 or fp16). */
 typedef enum mj_out_dtype { MJ_OUT_BF16 = 0, MJ_OUT_F16 = 1 } mj_out_dtype;
@@ -224,12 +228,13 @@ typedef struct mj_decode_args {
 
   int out_dtype;     /* mj_out_dtype of `out` (0 = bf16); rounding to nearest even */
 
-  /* Q as is (q_mode MJ_Q_BF16): device bf16, (b*q_len+t, h, c) at
-     q_bf16[(b*q_len+t)*q_tok_stride + h*q_head_stride + c]; strides in
+  /* bf16 Q (q_mode MJ_Q_BF16 / MJ_Q_FP8_FUSED): device bf16, (b*q_len+t, h, c)
+     at q_bf16[(b*q_len+t)*q_tok_stride + h*q_head_stride + c]; strides in
      elements, multiples of 8. The step is then decode (+ merge) only. */
   int q_mode;        /* mj_q_mode (0 = the fp8 codes above) */
   const void* q_bf16;
   int64_t q_tok_stride, q_head_stride;
+  const float* q_mul;  /* MJ_Q_FP8_FUSED: nullable device float32 [h_q][d], as in mj_quantize_q */
 } mj_decode_args;
 
 /* ------------------------------------------------------------------------

@@ -32,6 +32,7 @@ KV_FORMATS = {"fp8": MJ_KV_E4M3, "e2m3": MJ_KV_E2M3}
 
 MJ_Q_FP8 = 0
 MJ_Q_BF16 = 1
+MJ_Q_FP8_FUSED = 2
 
 MJ_OUT_BF16 = 0
 MJ_OUT_F16 = 1
@@ -82,7 +83,7 @@ class mj_decode_args(ctypes.Structure):
         ("impl", ctypes.c_int), ("kv_stages", ctypes.c_int), ("evict_first", ctypes.c_int),
         ("out_dtype", ctypes.c_int),
         ("q_mode", ctypes.c_int), ("q_bf16", ctypes.c_void_p),
-        ("q_tok_stride", ctypes.c_int64), ("q_head_stride", ctypes.c_int64),
+        ("q_tok_stride", ctypes.c_int64), ("q_head_stride", ctypes.c_int64), ("q_mul", ctypes.c_void_p),
     ]
 
 

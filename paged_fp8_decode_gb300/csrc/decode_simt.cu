@@ -12,6 +12,8 @@
 // This is the generic path: any row tile up to 32, any strides, e4m3 or
 // packed e2m3, e4m3 Q codes or bf16 Q as is. The tensor-core kernel is the
 // fast path.
+#include <cuda_fp8.h>
+
 #include "mj_device.cuh"
 #include "mj_internal.h"
 
@@ -83,31 +85,69 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // Q of this row tile -> shared floats (rows >= nr are zero): the e4m3
-  // codes (row t*h_r + r of the packed tile), or the bf16 Q as is (token t,
-  // query head g*h_r + r).
+  // codes (row t*h_r + r of the packed tile), the bf16 Q as is (token t,
+  // query head g*h_r + r), or that bf16 Q quantized here with mj_quantize_q's
+  // recipe (q_mul, amax over all q_len*h_r rows of (b, g), amax/448, e4m3
+  // round-to-nearest-even satfinite; IEEE float32 steps throughout).
+  float qd = 1.f;  // descale of the staged Q values
   const uint8_t* qrow = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
-  for (int i = tid; i < NR * kHeadDim / 4; i += kThreads) {
-    const int row = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (row < nr) {
-      if (p.q_bf16_mode) {
-        const int rr = r0 + row, tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
-        const uint2 u = *reinterpret_cast<const uint2*>(p.q_bf16 + int64_t(b * p.q_len + tq) * p.q_ts +
-                                                        int64_t(h) * p.q_hs + 4 * c4);
-        v[0] = __uint_as_float(u.x << 16);
-        v[1] = __uint_as_float(u.x & 0xFFFF0000u);
-        v[2] = __uint_as_float(u.y << 16);
-        v[3] = __uint_as_float(u.y & 0xFFFF0000u);
-      } else {
-        e4m3x4_to_float(reinterpret_cast<const uint32_t*>(qrow + row * kHeadDim)[c4], v);
+  auto q_in = [&](int rr, int c) {  // bf16 Q of packed row rr, channel c (times q_mul)
+    const int tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
+    float x = bf16_bits_to_float(p.q_bf16[int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c]);
+    if (p.q_mul) x = __fmul_rn(x, p.q_mul[int64_t(h) * kHeadDim + c]);
+    return x;
+  };
+  if (p.q_mode == MJ_Q_FP8_FUSED) {
+    const int c = tid;  // 128 threads, one channel each
+    // the tile's rows once, into registers; the rows of (b, g) outside the
+    // tile only count towards the amax
+    float xr[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) xr[r] = r < nr ? q_in(r0 + r, c) : 0.f;
+    float am = 0.f;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[r]));
+    for (int rr = 0; rr < p.n_q; ++rr)
+      if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr, c)));
+    am = warp_max(am);
+    if (lane == 0) red_m[warp][0] = am;
+    __syncthreads();
+    am = fmaxf(fmaxf(red_m[0][0], red_m[1][0]), fmaxf(red_m[2][0], red_m[3][0]));
+    qd = __fdiv_rn(fmaxf(am, 1e-6f), 448.0f);
+#pragma unroll
+    for (int row = 0; row < NR; ++row) {
+      float v = 0.f;
+      if (row < nr) {
+        __nv_fp8_e4m3 code;
+        code.__x = __nv_cvt_float_to_fp8(__fdiv_rn(xr[row], qd), __NV_SATFINITE, __NV_E4M3);
+        v = float(code);
       }
+      qs[row][c] = v;
     }
-    *reinterpret_cast<float4*>(&qs[row][4 * c4]) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    for (int i = tid; i < NR * kHeadDim / 4; i += kThreads) {
+      const int row = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (row < nr) {
+        if (p.q_mode == MJ_Q_BF16) {
+          const int rr = r0 + row, tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
+          const uint2 u = *reinterpret_cast<const uint2*>(p.q_bf16 + int64_t(b * p.q_len + tq) * p.q_ts +
+                                                          int64_t(h) * p.q_hs + 4 * c4);
+          v[0] = __uint_as_float(u.x << 16);
+          v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+          v[2] = __uint_as_float(u.y << 16);
+          v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+          e4m3x4_to_float(reinterpret_cast<const uint32_t*>(qrow + row * kHeadDim)[c4], v);
+        }
+      }
+      *reinterpret_cast<float4*>(&qs[row][4 * c4]) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    if (p.q_mode == MJ_Q_FP8) qd = p.q_descale[int64_t(b) * p.h_k + g];
   }
   __syncthreads();
 
   const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
-  const float qd = p.q_bf16_mode ? 1.f : p.q_descale[int64_t(b) * p.h_k + g];
   const float scale = qd * kd * p.qk_scale_log2;
   const int64_t causal_base = int64_t(L) - p.q_len;  // query t sees key j iff j <= L - q_len + t
 

@@ -152,15 +152,16 @@ __device__ __forceinline__ uint4 widen_chunk(uint4 in) {
   return o;
 }
 
-// BQ: bf16 Q as is, represented as two e4m3 terms per value (see the Q
-// staging in the softmax warps).
-template <int NQK, int NPV, int NR, bool FP6, bool BQ = false>
+// QM, how Q arrives (mj_q_mode): 0 e4m3 codes from mj_quantize_q; 1 bf16 Q
+// as is, represented as two e4m3 terms per value; 2 bf16 Q quantized here
+// with mj_quantize_q's recipe (see the Q staging in the softmax warps).
+template <int NQK, int NPV, int NR, bool FP6, int QM = 0>
 __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 2 : 1))
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
   constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
   static_assert(NH <= NQK && NR <= NH && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
-  static_assert(!BQ || (!FP6 && 2 * NR <= NQK), "bf16 Q: e4m3 KV, hi and lo rows in the Q tile");
+  static_assert(QM != 1 || (!FP6 && 2 * NR <= NQK), "bf16 Q: e4m3 KV, hi and lo rows in the Q tile");
   // TP tiles per softmax iteration; NSB S and P buffers let QK run up to
   // NSB - 1 tiles ahead of PV.
   constexpr int TP = NR <= 8 ? 2 : 1;
@@ -426,7 +427,15 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
     tc::grid_dependency_wait();
     const int xq = tid - kSoftmaxWarp0 * 32;
     float sc_hi = 0.f, sc_lo = 0.f;  // bf16 Q: logit scales of its hi and lo terms
-    if constexpr (!BQ) {
+    float sq = 1.f;                  // Q quantized here: its descale
+    // max over the 128 softmax threads (the four softmax warps always reach this barrier)
+    auto block_max = [&](float v, int slot) {
+      v = warp_max(v);
+      if (lane == 0) ctl.qamax[slot][warp & 3] = v;
+      tc::named_bar_sync(1, 128);
+      return fmaxf(fmaxf(ctl.qamax[slot][0], ctl.qamax[slot][1]), fmaxf(ctl.qamax[slot][2], ctl.qamax[slot][3]));
+    };
+    if constexpr (QM == 0) {
       // Q codes rows r0 .. r0+nr-1 -> Q tile [NQK rows][128 B], K-major,
       // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); other rows 0.
       const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
@@ -436,6 +445,38 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
         if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * kHeadDim + c * 16);
         *reinterpret_cast<uint4*>(smem + lay.q + r * 128 + ((c ^ (r & 7)) << 4)) = v;
       }
+    } else if constexpr (QM == 2) {
+      // mj_quantize_q's recipe, in the kernel: x = bf16 Q (times q_mul), the
+      // scale from the amax over all q_len*h_r rows of (b, g), then e4m3
+      // round-to-nearest-even satfinite, every step an IEEE float32 operation,
+      // so the codes and the descale are the ones that call writes. Thread xq
+      // takes channel xq of every row.
+      const int c = xq;
+      auto q_in = [&](int rr) {
+        const int tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
+        float v = bf16_bits_to_float(p.q_bf16[int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c]);
+        if (p.q_mul) v = __fmul_rn(v, p.q_mul[int64_t(h) * kHeadDim + c]);
+        return v;
+      };
+      // the tile's rows once, into registers (independent loads); the rows of
+      // (b, g) outside the tile only count towards the amax
+      float xr[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) xr[r] = r < nr ? q_in(r0 + r) : 0.f;
+      float am = 0.f;
+#pragma unroll
+      for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[r]));
+      for (int rr = 0; rr < p.n_q; ++rr)
+        if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr)));
+      sq = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.0f);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        uint8_t code = 0;
+        if (r < nr) code = __nv_cvt_float_to_fp8(__fdiv_rn(xr[r], sq), __NV_SATFINITE, __NV_E4M3);
+        smem[lay.q + r * 128 + (((c >> 4) ^ (r & 7)) << 4) + (c & 15)] = code;
+      }
+      for (int i = xq; i < (NQK - NR) * 8; i += 128)  // the rows past the tile
+        *reinterpret_cast<uint4*>(smem + lay.q + NR * 128 + i * 16) = make_uint4(0u, 0u, 0u, 0u);
     } else {
       // bf16 Q as two e4m3 terms: hi = e4m3(x / s_hi) with s_hi = amax/448,
       // lo = e4m3((x - hi*s_hi) / s_lo) with s_lo = (max |residual|)/448.
@@ -460,13 +501,6 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
           xv[e + 3] = __uint_as_float(u.y & 0xFFFF0000u);
         }
       }
-      // max over the 128 softmax threads (the four softmax warps always reach this barrier)
-      auto block_max = [&](float v, int slot) {
-        v = warp_max(v);
-        if (lane == 0) ctl.qamax[slot][warp & 3] = v;
-        tc::named_bar_sync(1, 128);
-        return fmaxf(fmaxf(ctl.qamax[slot][0], ctl.qamax[slot][1]), fmaxf(ctl.qamax[slot][2], ctl.qamax[slot][3]));
-      };
       float am = 0.f;
 #pragma unroll
       for (int e = 0; e < EPT; ++e) am = fmaxf(am, fabsf(xv[e]));
@@ -518,8 +552,9 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
     const int x = qd * 32 + lane;     // key of the tile (S) / channel (O)
     const uint32_t lane_off = uint32_t(qd * 32) << 16;
     const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
-    // bf16 Q: the logits are formed when S is read (scale 1 below)
-    const float scale = BQ ? 1.f : p.q_descale[int64_t(b) * p.h_k + g] * kd * p.qk_scale_log2;
+    // bf16 Q as two terms: the logits are formed when S is read (scale 1 below)
+    const float scale =
+        QM == 1 ? 1.f : (QM == 2 ? sq : p.q_descale[int64_t(b) * p.h_k + g]) * kd * p.qk_scale_log2;
     // last visible key of each row (query token t sees keys j <= L - q_len + t)
     int lim[NR];
 #pragma unroll
@@ -557,7 +592,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       }
       if (!ok) break;
       tc::tc_fence_after();
-      if constexpr (!BQ) {
+      if constexpr (QM != 1) {
 #pragma unroll
         for (int a = 0; a < TP; ++a) {
           if (a < nt) {
@@ -856,13 +891,13 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   return r == CUDA_SUCCESS;
 }
 
-template <int NQK, int NPV, int NR, bool FP6, bool BQ = false>
+template <int NQK, int NPV, int NR, bool FP6, int QM = 0>
 cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
   const TcSmem lay = tc_smem_layout(p.kv_stages, NQK, NPV, NR <= 8 ? 4 : 2);
   const int bytes = int(lay.total) + 1024;
   static int configured = 0;  // largest dynamic smem size set so far
   if (bytes > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6, BQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          bytes);
     if (e != cudaSuccess) return e;
     configured = bytes;
@@ -878,7 +913,21 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6, BQ>, mk, mv, p);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6, QM>, mk, mv, p);
+}
+
+// The kernel instance for the row tile (the plan's tile width, 16 or 32
+// rows; fewer rows take the 4- or 8-row variants). With bf16 Q as two terms
+// the Q tile holds two rows (hi, lo) per query row.
+template <bool FP6, int QM>
+cudaError_t launch_rows(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
+  constexpr int K = QM == 1 ? 2 : 1;
+  if (p.tw <= 16) {
+    if (p.n_q <= 4) return launch_tc<16, 16, 4, FP6, QM>(mk, mv, p, stream);
+    if (p.n_q <= 8) return launch_tc<16, 16, 8, FP6, QM>(mk, mv, p, stream);
+    return launch_tc<16 * K, 32, 16, FP6, QM>(mk, mv, p, stream);
+  }
+  return launch_tc<32 * K, 64, 32, FP6, QM>(mk, mv, p, stream);
 }
 
 }  // namespace
@@ -886,7 +935,7 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
 int tc_default_stages() { return 6; }
 
 bool tc_supported(const DecodeParams& p) {
-  if (p.q_bf16_mode && p.kv_format != MJ_KV_E4M3) return false;
+  if (p.q_mode == MJ_Q_BF16 && p.kv_format != MJ_KV_E4M3) return false;
   if (p.kv_format == MJ_KV_E2M3) {
     // the packed TMA type wants 32-byte aligned strides (and base, checked
     // by the ABI for e2m3)
@@ -942,27 +991,13 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
     // K enters the MMA as true e2m3 values (no 2^-6 widening factor); V is
     // widened in shared memory and keeps the factor in v_fmt.
     p.qk_scale_log2 *= 1.0f / 64.0f;
-    if (p.tw <= 16) {
-      if (p.n_q <= 4) return launch_tc<16, 16, 4, true>(mk, mv, p, stream);
-      if (p.n_q <= 8) return launch_tc<16, 16, 8, true>(mk, mv, p, stream);
-      return launch_tc<16, 32, 16, true>(mk, mv, p, stream);
-    }
-    return launch_tc<32, 64, 32, true>(mk, mv, p, stream);
+    // packed e2m3 KV takes fp8 Q only: codes, or quantized here
+    return p.q_mode == MJ_Q_FP8_FUSED ? launch_rows<true, 2>(mk, mv, p, stream)
+                                      : launch_rows<true, 0>(mk, mv, p, stream);
   }
-  if (p.q_bf16_mode) {  // the Q tile holds two rows (hi, lo) per query row
-    if (p.tw <= 16) {
-      if (p.n_q <= 4) return launch_tc<16, 16, 4, false, true>(mk, mv, p, stream);
-      if (p.n_q <= 8) return launch_tc<16, 16, 8, false, true>(mk, mv, p, stream);
-      return launch_tc<32, 32, 16, false, true>(mk, mv, p, stream);
-    }
-    return launch_tc<64, 64, 32, false, true>(mk, mv, p, stream);
-  }
-  if (p.tw <= 16) {
-    if (p.n_q <= 4) return launch_tc<16, 16, 4, false>(mk, mv, p, stream);
-    if (p.n_q <= 8) return launch_tc<16, 16, 8, false>(mk, mv, p, stream);
-    return launch_tc<16, 32, 16, false>(mk, mv, p, stream);
-  }
-  return launch_tc<32, 64, 32, false>(mk, mv, p, stream);
+  if (p.q_mode == MJ_Q_BF16) return launch_rows<false, 1>(mk, mv, p, stream);
+  if (p.q_mode == MJ_Q_FP8_FUSED) return launch_rows<false, 2>(mk, mv, p, stream);
+  return launch_rows<false, 0>(mk, mv, p, stream);
 }
 
 }  // namespace mj

@@ -43,9 +43,10 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   if (a->num_pages < 1 || a->num_work < 0 || a->block_table_stride < 0) return MJ_ERR_INVALID_ARG;
   if (a->impl < MJ_IMPL_AUTO || a->impl > MJ_IMPL_TCGEN05) return MJ_ERR_INVALID_ARG;
   if (!(a->softmax_scale > 0.f) || !std::isfinite(a->softmax_scale)) return MJ_ERR_INVALID_ARG;
-  if (a->q_mode != MJ_Q_FP8 && a->q_mode != MJ_Q_BF16) return MJ_ERR_UNSUPPORTED;
-  const bool bf16_q = a->q_mode == MJ_Q_BF16;
-  if (bf16_q && a->kv_format != MJ_KV_E4M3) return MJ_ERR_UNSUPPORTED;  // e2m3 KV is fp8-Q only
+  if (a->q_mode != MJ_Q_FP8 && a->q_mode != MJ_Q_BF16 && a->q_mode != MJ_Q_FP8_FUSED) return MJ_ERR_UNSUPPORTED;
+  const bool bf16_q = a->q_mode != MJ_Q_FP8;  // the call reads bf16 Q
+  if (a->q_mode == MJ_Q_BF16 && a->kv_format != MJ_KV_E4M3) return MJ_ERR_UNSUPPORTED;  // e2m3 KV is fp8-Q only
+  if (a->q_mul && !aligned(a->q_mul, 16)) return MJ_ERR_ALIGNMENT;
   const void* q0 = bf16_q ? a->q_bf16 : a->q_codes;
   const void* q1 = bf16_q ? a->q_bf16 : a->q_descale;
   const void* need[] = {q0, q1, a->k_cache,  a->v_cache, a->k_descale, a->v_descale,
@@ -105,7 +106,8 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   q.n_row_tiles = n_row_tiles(n_q);
   q.q_codes = a->q_codes;
   q.q_descale = a->q_descale;
-  q.q_bf16_mode = a->q_mode == MJ_Q_BF16 ? 1 : 0;
+  q.q_mode = a->q_mode;
+  q.q_mul = a->q_mode == MJ_Q_FP8_FUSED ? a->q_mul : nullptr;
   q.q_bf16 = static_cast<const uint16_t*>(a->q_bf16);
   q.q_ts = a->q_tok_stride;
   q.q_hs = a->q_head_stride;

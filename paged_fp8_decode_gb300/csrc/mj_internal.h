@@ -32,9 +32,10 @@ struct DecodeParams {
 
   const uint8_t* q_codes;
   const float* q_descale;
-  int q_bf16_mode;          // 1: Q is q_bf16 as is (no codes, no descale)
+  int q_mode;               // mj_q_mode: 0 codes, 1 bf16 as is, 2 bf16 quantized in the kernel
   const uint16_t* q_bf16;
   int64_t q_ts, q_hs;       // element strides of q_bf16
+  const float* q_mul;       // q_mode 2: nullable [h_q][d]
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   int64_t k_sp, k_st, k_sh, v_sp, v_st, v_sh;  // byte strides (page, token, head)

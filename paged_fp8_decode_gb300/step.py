@@ -45,9 +45,10 @@ class DecodeStep:
                  sm_count: int | None = None, ctas_per_sm: int = 2, max_splits: int = 16,
                  margin: int = 0, causal: bool = True, impl: int = MJ_IMPL_AUTO, kv_stages: int = 0,
                  evict_first: bool = True, device="cuda", with_lse: bool = False, q_mode: str = "fp8"):
-        """``q_mode``: "fp8" (dynamic e4m3 Q, mj_quantize_q in the step) or
-        "bf16" (Q as is; the step is decode + merge)."""
-        assert q_mode in ("fp8", "bf16")
+        """``q_mode``: "fp8" (dynamic e4m3 Q, mj_quantize_q in the step),
+        "fp8_fused" (the same quantization done by the decode kernel; the
+        step is decode + merge) or "bf16" (Q as is; decode + merge)."""
+        assert q_mode in ("fp8", "fp8_fused", "bf16")
         self.q_mode = q_mode
         self.device = torch.device(device)
         if sm_count is None:
@@ -103,10 +104,12 @@ class DecodeStep:
         """The decode call's arguments; ``q`` (bf16 mode): the bf16 Q it reads."""
         info = self.plan_info
         a = mj_decode_args()
-        if self.q_mode == "bf16":
+        if self.q_mode in ("bf16", "fp8_fused"):
             assert q is not None and q.dtype == torch.bfloat16 and q.stride(2) == 1
-            a.q_mode, a.q_bf16 = 1, q.data_ptr()
+            a.q_mode, a.q_bf16 = (1 if self.q_mode == "bf16" else 2), q.data_ptr()
             a.q_tok_stride, a.q_head_stride = q.stride(0), q.stride(1)
+            if self.q_mode == "fp8_fused" and kv.q_mul is not None:
+                a.q_mul = kv.q_mul.data_ptr()
         a.num_seqs, a.q_len, a.h_q, a.h_k, a.d = num_seqs, self.q_len, self.h_q, self.h_k, self.d
         a.causal = 1 if self.causal else 0
         a.softmax_scale = softmax_scale

@@ -120,7 +120,7 @@ def _valid_args():
     ("workspace_bytes", 16, mj.MJ_ERR_CAPACITY),
     ("impl", 9, mj.MJ_ERR_INVALID_ARG),
     ("out_dtype", 2, mj.MJ_ERR_UNSUPPORTED),
-    ("q_mode", 2, mj.MJ_ERR_UNSUPPORTED),
+    ("q_mode", 3, mj.MJ_ERR_UNSUPPORTED),
 ])
 def test_decode_args_rejected_on_host(lib, field, value, status):
     a = _valid_args()

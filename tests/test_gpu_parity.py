@@ -266,3 +266,36 @@ def test_bf16_q_rejections():
     with pytest.raises(mj.MjError) as e:  # packed e2m3 KV is fp8-Q only
         run_gpu(_case("fp6_small"), impl=0, q_mode="bf16")
     assert e.value.status == mj.MJ_ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------------------------------
+# Q quantized inside the decode kernel (q_mode MJ_Q_FP8_FUSED): the same codes
+# and descales as mj_quantize_q (which is pinned to the oracle), so the whole
+# step's output is bit-identical to the step with the separate quantize call
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["ragged_hnd", "spec_causal", "fp6_small", "fp6_nhd_spec", "split", "wide_rows"])
+def test_fused_quantize_is_bit_identical(impl, name):
+    kw = {}
+    if name == "split":
+        w, kw = _case("split_nhd"), dict(max_splits=16)
+    elif name == "wide_rows":  # 64 query rows per (request, KV head): two row tiles share one amax
+        w = synth.make_case(name=name, num_seqs=3, q_len=8, h_q=64, h_k=8, page_size=32, seq_lens=[50, 700, 129],
+                            layout="HND", scale_mode="head", seed=27)
+    else:
+        w = _case(name)
+    a = run_gpu(w, impl=impl, **kw)
+    b = run_gpu(w, impl=impl, q_mode="fp8_fused", **kw)
+    assert a["status"] == 0 and b["status"] == 0
+    real_rows = np.repeat(w.seq_lens > 0, w.q_len)
+    assert np.array_equal(a["out"][real_rows], b["out"][real_rows])
+    real = w.seq_lens > 0
+    assert np.array_equal(a["lse"][real], b["lse"][real])
+    assert np.all(b["out"][~real_rows] == SENTINEL)
+
+
+def test_fused_quantize_full_size():
+    w = synth.WORKLOADS["qwen3_8b_decode"]()
+    a = run_gpu(w, impl=2, **FULL["qwen3_8b_decode"])
+    b = run_gpu(w, impl=2, q_mode="fp8_fused", **FULL["qwen3_8b_decode"])
+    assert np.array_equal(a["out"], b["out"]) and b["status"] == 0

@@ -52,6 +52,7 @@ DEFAULT_KNOBS = {
     "spec_verify": (4, 64, 4),
     "spec_verify_noncausal": (4, 64, 4),
     "fp6_decode": (2, 64, 6),
+    "d256_decode": (2, 64, 2),
     "tiny": (2, 16, 0),
 }
 

@@ -148,8 +148,9 @@ MJ_API int mj_plan_split_kv(const int32_t* seq_lens_host, int num_seqs, int q_le
  * q_codes    device uint8 [num_seqs][h_k][q_len*h_r][d], row t*h_r + r
  *            (h_r = h_q/h_k), written.
  * q_descale  device float32 [num_seqs][h_k], written.
- * d must be 128. Padding requests are quantized too (harmless: the decode
- * call never reads them).
+ * d is 128 or 256 (T5DecodeRunner asserts head_size % 128 == 0; the library
+ * is built for these two), else MJ_ERR_UNSUPPORTED. Padding requests are
+ * quantized too (harmless: the decode call never reads them).
  * ---------------------------------------------------------------------- */
 MJ_API int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, int num_seqs,
                   int q_len, int h_q, int h_k, int d, const float* q_mul, uint8_t* q_codes,
@@ -167,7 +168,7 @@ typedef struct mj_decode_args {
   int num_seqs;   /* requests in the batch (real + trailing padding) */
   int q_len;      /* query tokens per request (1 = decode; 1+k = speculative verify) */
   int h_q, h_k;   /* query heads, KV heads; h_q % h_k == 0 */
-  int d;          /* head size; 128 */
+  int d;          /* head size: 128 or 256 (packed e2m3 at 256: CUDA-core kernel only) */
   int causal;     /* 1: query t sees key j iff j <= seq_len - q_len + t;
                      0: every query token sees every key (README "What it does") */
   float softmax_scale;
@@ -223,7 +224,9 @@ typedef struct mj_decode_args {
 
   /* tuning knobs (0 = library default) */
   int impl;          /* mj_impl */
-  int kv_stages;     /* KV ring depth of the tensor-core kernel */
+  int kv_stages;     /* KV ring depth of the tensor-core kernel, in K or V tiles (made even,
+                        at most 13, and lowered to what shared memory holds); 0 = 6 at
+                        d = 128, 2 at d = 256 (a tile of 256-byte rows is 32 KB) */
   int evict_first;   /* 1 = L2 evict-first hint on KV loads (KV is read once) */
 
   int out_dtype;     /* mj_out_dtype of `out` (0 = bf16); rounding to nearest even */
@@ -338,7 +341,7 @@ MJ_API int mj_decode_attention_noalloc(const mj_decode_args* args, void* stream)
  * ---------------------------------------------------------------------- */
 typedef struct mj_write_kv_args {
   int num_tokens;             /* rows in key / value (0: nothing to do) */
-  int h_k, d;                 /* KV heads; head size (128) */
+  int h_k, d;                 /* KV heads; head size (128 or 256) */
   const void* key;            /* device bf16; (t, g, c) at key[t*key_tok_stride + g*key_head_stride + c] */
   const void* value;          /* device bf16; likewise with the value strides */
   int64_t key_tok_stride, key_head_stride;      /* elements */

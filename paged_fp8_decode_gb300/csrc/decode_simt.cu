@@ -3,15 +3,16 @@
 // One CTA (4 warps) per (work row, KV head, query-row tile). Each warp walks
 // 32-key blocks of the work row's key range; lane j owns key j of the block
 // for S = Q.K^T (the whole K row through 16-byte loads) and channels
-// 4*lane .. 4*lane+3 for O += P.V (coalesced 128-byte V reads per key). The
+// 128*h + 4*lane .. 128*h + 4*lane+3 of each 128-channel half h for
+// O += P.V (coalesced 128-byte V reads per key and half). The
 // online softmax runs per warp in the log2 domain; the four warps' (m, l, O)
 // are merged in shared memory at the end. Keys at or past the request's
 // device seq_len are never read, so stale or poisoned page tails cannot leak
 // into the result.
 //
-// This is the generic path: any row tile up to 32, any strides, e4m3 or
-// packed e2m3, e4m3 Q codes or bf16 Q as is. The tensor-core kernel is the
-// fast path.
+// This is the generic path: any row tile up to 32 (16 with D = 256), any
+// strides, e4m3 or packed e2m3, D = 128 or 256, e4m3 Q codes or bf16 Q as is.
+// The tensor-core kernel is the fast path.
 #include <cuda_fp8.h>
 
 #include "mj_device.cuh"
@@ -47,20 +48,21 @@ __device__ __forceinline__ void load_k16(const uint8_t* row, int kv_format, int 
   }
 }
 
-// Channels 4*lane .. 4*lane+3 of one V row.
-__device__ __forceinline__ void load_v4(const uint8_t* row, int kv_format, int lane, float v[4]) {
+// Channels 4*j .. 4*j+3 of one V row.
+__device__ __forceinline__ void load_v4(const uint8_t* row, int kv_format, int j, float v[4]) {
   if (kv_format == MJ_KV_E4M3) {
-    e4m3x4_to_float(__ldg(reinterpret_cast<const uint32_t*>(row) + lane), v);
+    e4m3x4_to_float(__ldg(reinterpret_cast<const uint32_t*>(row) + j), v);
   } else {
-    const uint8_t* p = row + 3 * lane;
+    const uint8_t* p = row + 3 * j;
     const uint32_t g = uint32_t(__ldg(p)) | (uint32_t(__ldg(p + 1)) << 8) | (uint32_t(__ldg(p + 2)) << 16);
     e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g)), v);
   }
 }
 
-template <int NR>
+template <int NR, int D>
 __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
-  __shared__ __align__(16) float qs[NR][kHeadDim];  // Q rows, later the O accumulator
+  constexpr int DH = D / 128;  // 128-channel halves; thread / lane work repeats per half
+  __shared__ __align__(16) float qs[NR][D];  // Q rows, later the O accumulator
   __shared__ float ps[kWarps][32][NR];              // P of each warp's 32-key block
   __shared__ float red_m[kWarps][NR], red_l[kWarps][NR];
   __shared__ int page_of[kWarps][32];
@@ -90,43 +92,49 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
   // recipe (q_mul, amax over all q_len*h_r rows of (b, g), amax/448, e4m3
   // round-to-nearest-even satfinite; IEEE float32 steps throughout).
   float qd = 1.f;  // descale of the staged Q values
-  const uint8_t* qrow = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
+  const uint8_t* qrow = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * D;
   auto q_in = [&](int rr, int c) {  // bf16 Q of packed row rr, channel c (times q_mul)
     const int tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
     float x = bf16_bits_to_float(p.q_bf16[int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c]);
-    if (p.q_mul) x = __fmul_rn(x, p.q_mul[int64_t(h) * kHeadDim + c]);
+    if (p.q_mul) x = __fmul_rn(x, p.q_mul[int64_t(h) * D + c]);
     return x;
   };
   if (p.q_mode == MJ_Q_FP8_FUSED) {
-    const int c = tid;  // 128 threads, one channel each
-    // the tile's rows once, into registers; the rows of (b, g) outside the
-    // tile only count towards the amax
-    float xr[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) xr[r] = r < nr ? q_in(r0 + r, c) : 0.f;
+    // 128 threads, channels tid + 128*h; the tile's rows once, into
+    // registers; the rows of (b, g) outside the tile only count towards the amax
+    float xr[DH][NR];
     float am = 0.f;
 #pragma unroll
-    for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[r]));
-    for (int rr = 0; rr < p.n_q; ++rr)
-      if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr, c)));
+    for (int hh = 0; hh < DH; ++hh) {
+      const int c = tid + 128 * hh;
+#pragma unroll
+      for (int r = 0; r < NR; ++r) xr[hh][r] = r < nr ? q_in(r0 + r, c) : 0.f;
+#pragma unroll
+      for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[hh][r]));
+      for (int rr = 0; rr < p.n_q; ++rr)
+        if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr, c)));
+    }
     am = warp_max(am);
     if (lane == 0) red_m[warp][0] = am;
     __syncthreads();
     am = fmaxf(fmaxf(red_m[0][0], red_m[1][0]), fmaxf(red_m[2][0], red_m[3][0]));
     qd = __fdiv_rn(fmaxf(am, 1e-6f), 448.0f);
 #pragma unroll
-    for (int row = 0; row < NR; ++row) {
-      float v = 0.f;
-      if (row < nr) {
-        __nv_fp8_e4m3 code;
-        code.__x = __nv_cvt_float_to_fp8(__fdiv_rn(xr[row], qd), __NV_SATFINITE, __NV_E4M3);
-        v = float(code);
+    for (int hh = 0; hh < DH; ++hh) {
+#pragma unroll
+      for (int row = 0; row < NR; ++row) {
+        float v = 0.f;
+        if (row < nr) {
+          __nv_fp8_e4m3 code;
+          code.__x = __nv_cvt_float_to_fp8(__fdiv_rn(xr[hh][row], qd), __NV_SATFINITE, __NV_E4M3);
+          v = float(code);
+        }
+        qs[row][tid + 128 * hh] = v;
       }
-      qs[row][c] = v;
     }
   } else {
-    for (int i = tid; i < NR * kHeadDim / 4; i += kThreads) {
-      const int row = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+    for (int i = tid; i < NR * D / 4; i += kThreads) {
+      const int row = i / (D / 4), c4 = i % (D / 4);
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       if (row < nr) {
         if (p.q_mode == MJ_Q_BF16) {
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
           v[2] = __uint_as_float(u.y << 16);
           v[3] = __uint_as_float(u.y & 0xFFFF0000u);
         } else {
-          e4m3x4_to_float(reinterpret_cast<const uint32_t*>(qrow + row * kHeadDim)[c4], v);
+          e4m3x4_to_float(reinterpret_cast<const uint32_t*>(qrow + row * D)[c4], v);
         }
       }
       *reinterpret_cast<float4*>(&qs[row][4 * c4]) = make_float4(v[0], v[1], v[2], v[3]);
@@ -151,12 +159,13 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
   const float scale = qd * kd * p.qk_scale_log2;
   const int64_t causal_base = int64_t(L) - p.q_len;  // query t sees key j iff j <= L - q_len + t
 
-  float m[NR], l[NR], o[NR][4];
+  float m[NR], l[NR], o[NR][4 * DH];  // o[r][4h + e]: channel 128h + 4*lane + e
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     m[r] = -INFINITY;
     l[r] = 0.f;
-    o[r][0] = o[r][1] = o[r][2] = o[r][3] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4 * DH; ++e) o[r][e] = 0.f;
   }
 
   const int64_t kbase_head = int64_t(g) * p.k_sh;
@@ -183,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
 #pragma unroll
       for (int r = 0; r < NR; ++r) acc[r] = 0.f;
 #pragma unroll 1
-      for (int i = 0; i < kHeadDim / 16; ++i) {
+      for (int i = 0; i < D / 16; ++i) {
         float kf[16];
         load_k16(krow, p.kv_format, i, kf);
 #pragma unroll
@@ -223,10 +232,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
       }
       m[r] = m_new;
       l[r] = l[r] * alpha + pr;
-      o[r][0] *= alpha;
-      o[r][1] *= alpha;
-      o[r][2] *= alpha;
-      o[r][3] *= alpha;
+#pragma unroll
+      for (int e = 0; e < 4 * DH; ++e) o[r][e] *= alpha;
       ps[warp][lane][r] = pr;
     }
     __syncwarp();
@@ -237,15 +244,14 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
       if (pg < 0) continue;
       const int slot = int((kb + kk) % p.page_size);
       const uint8_t* vrow = p.v_cache + int64_t(pg) * p.v_sp + int64_t(slot) * p.v_st + vbase_head;
-      float v[4];
-      load_v4(vrow, p.kv_format, lane, v);
+      float v[4 * DH];
+#pragma unroll
+      for (int hh = 0; hh < DH; ++hh) load_v4(vrow, p.kv_format, 32 * hh + lane, v + 4 * hh);
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         const float pr = ps[warp][kk][r];
-        o[r][0] = fmaf(pr, v[0], o[r][0]);
-        o[r][1] = fmaf(pr, v[1], o[r][1]);
-        o[r][2] = fmaf(pr, v[2], o[r][2]);
-        o[r][3] = fmaf(pr, v[3], o[r][3]);
+#pragma unroll
+        for (int e = 0; e < 4 * DH; ++e) o[r][e] = fmaf(pr, v[e], o[r][e]);
       }
     }
     __syncwarp();
@@ -274,13 +280,16 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
     if (warp == w2) {
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
-        float4* dst = reinterpret_cast<float4*>(&qs[r][4 * lane]);
-        float4 cur = (w2 == 0) ? make_float4(0.f, 0.f, 0.f, 0.f) : *dst;
-        cur.x = fmaf(o[r][0], f[r], cur.x);
-        cur.y = fmaf(o[r][1], f[r], cur.y);
-        cur.z = fmaf(o[r][2], f[r], cur.z);
-        cur.w = fmaf(o[r][3], f[r], cur.w);
-        *dst = cur;
+#pragma unroll
+        for (int hh = 0; hh < DH; ++hh) {
+          float4* dst = reinterpret_cast<float4*>(&qs[r][128 * hh + 4 * lane]);
+          float4 cur = (w2 == 0) ? make_float4(0.f, 0.f, 0.f, 0.f) : *dst;
+          cur.x = fmaf(o[r][4 * hh + 0], f[r], cur.x);
+          cur.y = fmaf(o[r][4 * hh + 1], f[r], cur.y);
+          cur.z = fmaf(o[r][4 * hh + 2], f[r], cur.z);
+          cur.w = fmaf(o[r][4 * hh + 3], f[r], cur.w);
+          *dst = cur;
+        }
       }
     }
     __syncthreads();
@@ -288,7 +297,6 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
 
   const bool direct = !p.with_reduction || p.n_splits[b] <= 1;
   const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
-  const int c = tid;  // 128 threads = 128 channels
   for (int r = 0; r < nr; ++r) {
     float M = red_m[0][r];
     for (int w2 = 1; w2 < kWarps; ++w2) M = fmaxf(M, red_m[w2][r]);
@@ -296,39 +304,58 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeParams p) {
     if (M != -INFINITY)
       for (int w2 = 0; w2 < kWarps; ++w2)
         if (red_m[w2][r] != -INFINITY) Lt += red_l[w2][r] * fast_exp2(red_m[w2][r] - M);
-    const float on = Lt > 0.f ? qs[r][c] / Lt : 0.f;
     const int row = r0 + r;
-    if (direct) {
-      const int tq = row / p.h_r, rr = row % p.h_r, h = g * p.h_r + rr;
-      float val = on * vd;
-      if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + c];
-      p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_out_bits(val, p.out_f16);
-      if (p.lse && c == 0)
-        p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] = Lt > 0.f ? (M + fast_log2(Lt)) * kLn2 : -INFINITY;
-    } else {
-      const int64_t idx = part_index(p, b, w.w, g, row);
-      p.o_part[idx * kHeadDim + c] = on;
-      if (c == 0) {
-        p.m_part[idx] = Lt > 0.f ? M : -INFINITY;
-        p.l_part[idx] = Lt;
+#pragma unroll
+    for (int hh = 0; hh < DH; ++hh) {
+      const int c = tid + 128 * hh;  // 128 threads, channels c
+      const float on = Lt > 0.f ? qs[r][c] / Lt : 0.f;
+      if (direct) {
+        const int tq = row / p.h_r, rr = row % p.h_r, h = g * p.h_r + rr;
+        float val = on * vd;
+        if (p.o_mul) val *= p.o_mul[int64_t(h) * D + c];
+        p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_out_bits(val, p.out_f16);
+        if (p.lse && c == 0)
+          p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] = Lt > 0.f ? (M + fast_log2(Lt)) * kLn2 : -INFINITY;
+      } else {
+        const int64_t idx = part_index(p, b, w.w, g, row);
+        p.o_part[idx * D + c] = on;
+        if (c == 0) {
+          p.m_part[idx] = Lt > 0.f ? M : -INFINITY;
+          p.l_part[idx] = Lt;
+        }
       }
     }
   }
 }
 
+template <int D>
+void launch_rows_simt(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  if (p.tw <= 4)
+    decode_simt_kernel<4, D><<<grid, kThreads, 0, stream>>>(p);
+  else if (p.tw <= 8)
+    decode_simt_kernel<8, D><<<grid, kThreads, 0, stream>>>(p);
+  else if (p.tw <= 16)
+    decode_simt_kernel<16, D><<<grid, kThreads, 0, stream>>>(p);
+  else if constexpr (D == 128)
+    decode_simt_kernel<32, D><<<grid, kThreads, 0, stream>>>(p);
+}
+
 }  // namespace
 
-cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
-  if (p.num_work == 0) return cudaSuccess;
+cudaError_t launch_decode_simt(const DecodeParams& p0, cudaStream_t stream) {
+  if (p0.num_work == 0) return cudaSuccess;
+  DecodeParams p = p0;
+  if (p.d == 256 && p.tw > 16) {
+    // D = 256 keeps 16 rows per CTA (the O accumulator stays in registers):
+    // a 32-row tile of the plan becomes two CTAs' worth of rows
+    p.tw = 16;
+    p.n_row_tiles = (p.n_q + 15) / 16;
+  }
   dim3 grid(p.num_work, p.h_k, p.n_row_tiles);
-  if (p.tw <= 4)
-    decode_simt_kernel<4><<<grid, kThreads, 0, stream>>>(p);
-  else if (p.tw <= 8)
-    decode_simt_kernel<8><<<grid, kThreads, 0, stream>>>(p);
-  else if (p.tw <= 16)
-    decode_simt_kernel<16><<<grid, kThreads, 0, stream>>>(p);
+  if (p.d == 256)
+    launch_rows_simt<256>(p, grid, stream);
   else
-    decode_simt_kernel<32><<<grid, kThreads, 0, stream>>>(p);
+    launch_rows_simt<128>(p, grid, stream);
   return cudaGetLastError();
 }
 

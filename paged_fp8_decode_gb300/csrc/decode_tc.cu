@@ -7,14 +7,19 @@
 // L2 evict-first hint, tcgen05 MMAs accumulating S and O in TMEM, softmax
 // warpgroups. This kernel is written for GB300 from that description:
 //
-// * One CTA per (work row, KV head, query-row tile); 6 warps:
-//     warp 0     TMA producer: block-table lookups (32 entries per warp load),
-//                one 4-D tensor-map load per (page, head) into the ring;
+// * One CTA per (work row, KV head, query-row tile); 7 warps (10 with packed
+//   e2m3 KV):
+//     warps 0, 6 TMA producers of the K and the V tiles: block-table lookups
+//                (32 entries per warp load), one 4-D tensor-map load per
+//                (page, head, 128-channel sub-tile) into the ring;
 //     warp 1     TMEM allocation and the single-thread MMA issuer;
 //     warps 2-5  softmax warpgroup: thread x owns TMEM lane x, i.e. key x of a
-//                128-key tile for S and channel x for O.
-// * The ring alternates K and V tiles of 128 keys x 128 bytes, 128-byte
-//   swizzled by the TMA so that tcgen05.mma reads them directly.
+//                128-key tile for S and channel x (of each 128-channel half)
+//                for O;
+//     warps 7-9  packed e2m3 KV only: widen each landed V tile to e4m3.
+// * The ring alternates K and V tiles of 128 keys x D bytes (D / 128 sub-tiles
+//   of 128 keys x 128 bytes), 128-byte swizzled by the TMA so that
+//   tcgen05.mma reads them directly.
 // * Both products are issued "keys as M" so that M = 128 fills the tensor
 //   core even for a handful of query rows:
 //     S^T[key][row] = K[key][:] . Q[row][:]       A = K tile (K-major), B = Q tile
@@ -64,12 +69,17 @@ struct TcSmem {
   uint32_t ring, q, p0, p1, ctrl, total;
 };
 
-// nsb: S / P buffers in flight (P buffer j at p0 + j * (p1 - p0))
-__host__ __device__ inline TcSmem tc_smem_layout(int stages, int nqk, int npv, int nsb) {
+// Shared-memory bytes of one 128-channel sub-tile of the Q tile (nqk rows).
+__host__ __device__ constexpr uint32_t q_sub_bytes(int nqk) { return uint32_t((nqk * 128 + 1023) / 1024) * 1024u; }
+
+// nsb: S / P buffers in flight (P buffer j at p0 + j * (p1 - p0)); dh: 128-channel
+// sub-tiles per row (D / 128): a ring entry holds dh 16 KB sub-tiles, the Q
+// tile dh sub-tiles of q_sub_bytes(nqk).
+__host__ __device__ inline TcSmem tc_smem_layout(int stages, int nqk, int npv, int nsb, int dh) {
   TcSmem s;
   s.ring = 0;
-  s.q = stages * kTileBytes;
-  s.p0 = s.q + ((nqk * 128 + 1023) / 1024) * 1024;
+  s.q = stages * dh * kTileBytes;
+  s.p0 = s.q + dh * q_sub_bytes(nqk);
   s.p1 = s.p0 + ((npv * 128 + 1023) / 1024) * 1024;
   s.ctrl = s.p0 + nsb * (s.p1 - s.p0);
   s.total = s.ctrl + 3072;
@@ -155,19 +165,28 @@ __device__ __forceinline__ uint4 widen_chunk(uint4 in) {
 // QM, how Q arrives (mj_q_mode): 0 e4m3 codes from mj_quantize_q; 1 bf16 Q
 // as is, represented as two e4m3 terms per value; 2 bf16 Q quantized here
 // with mj_quantize_q's recipe (see the Q staging in the softmax warps).
-template <int NQK, int NPV, int NR, bool FP6, int QM = 0>
+// D, the head size (128 or 256): a K or V row of D channels is DH = D / 128
+// sub-tiles of 128 bytes; QK accumulates over the sub-tiles and PV runs once
+// per sub-tile into its own O accumulator (channel 128 * dh + lane).
+template <int NQK, int NPV, int NR, bool FP6, int QM = 0, int D = 128>
 __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 2 : 1))
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
   constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
+  constexpr int DH = D / 128;
+  constexpr uint32_t kEntry = DH * kTileBytes;  // one ring entry: a K or V tile
+  constexpr uint32_t kQSub = q_sub_bytes(NQK);
   static_assert(NH <= NQK && NR <= NH && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
   static_assert(QM != 1 || (!FP6 && 2 * NR <= NQK), "bf16 Q: e4m3 KV, hi and lo rows in the Q tile");
+  static_assert((D == 128 || D == 256) && (!FP6 || D == 128), "head size (packed e2m3: 128)");
   // TP tiles per softmax iteration; NSB S and P buffers let QK run up to
   // NSB - 1 tiles ahead of PV.
   constexpr int TP = NR <= 8 ? 2 : 1;
   constexpr int NSB = 2 * TP;
-  // TMEM: NSB S buffers (NQK columns each), one O accumulator (NPV columns)
-  constexpr uint32_t kTmemCols = (NSB * NQK + NPV <= 64) ? 64 : (NSB * NQK + NPV <= 128 ? 128 : 256);
+  // TMEM: NSB S buffers (NQK columns each), DH O accumulators (NPV columns each)
+  constexpr int kCols = NSB * NQK + DH * NPV;
+  static_assert(kCols <= 256, "TMEM columns");
+  constexpr uint32_t kTmemCols = kCols <= 64 ? 64 : (kCols <= 128 ? 128 : 256);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -196,7 +215,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
   const bool last_partial = k0 + int64_t(ntiles) * kKvTile > k1;
   const int stages = p.kv_stages;
 
-  const TcSmem lay = tc_smem_layout(stages, NQK, NPV, NSB);
+  const TcSmem lay = tc_smem_layout(stages, NQK, NPV, NSB, DH);
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + lay.ctrl);
   const uint32_t ring_addr = tc::smem_u32(smem + lay.ring);
   const uint32_t q_addr = tc::smem_u32(smem + lay.q);
@@ -239,7 +258,8 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort = &ctl.abort;
 
-  // TMEM columns: S buffer j % NSB at [(j % NSB) NQK, ...), the O accumulator after them
+  // TMEM columns: S buffer j % NSB at [(j % NSB) NQK, ...), the O accumulators
+  // after them (sub-tile dh at tO + dh * NPV)
   auto tS = [&](int j) { return tmem + uint32_t((j % NSB) * NQK); };
   const uint32_t tO = tmem + uint32_t(NSB * NQK);
   // barrier slot and phase parity of tile j's S / P / O events
@@ -285,11 +305,15 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
       if (ok && lane < nvalid) {
-        const uint32_t dst = ring_addr + uint32_t(slot) * kTileBytes + uint32_t(lane) * page_bytes;
-        if (p.tma_head_inner)
-          tc::tma_load_4d(dst, map, full, 0, g, 0, pg, pol);
-        else
-          tc::tma_load_4d(dst, map, full, 0, 0, g, pg, pol);
+        // sub-tile dh: channels 128 dh .. 128 dh + 127 (x = 128 dh bytes, 16-byte aligned)
+#pragma unroll
+        for (int dh = 0; dh < DH; ++dh) {
+          const uint32_t dst = ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes + uint32_t(lane) * page_bytes;
+          if (p.tma_head_inner)
+            tc::tma_load_4d(dst, map, full, 128 * dh, g, 0, pg, pol);
+          else
+            tc::tma_load_4d(dst, map, full, 128 * dh, 0, g, pg, pol);
+        }
       }
       if (ok) ++issued;
       __syncwarp();
@@ -306,8 +330,11 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
       if (ok) {
         const int first_dead = int(k1 - (k0 + int64_t(ntiles - 1) * kKvTile));  // rows >= this are past the end
-        uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kTileBytes);
-        for (int c = first_dead * 8 + lane; c < kKvTile * 8; c += 32) tile[c] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int dh = 0; dh < DH; ++dh) {
+          uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry + dh * kTileBytes);
+          for (int c = first_dead * 8 + lane; c < kKvTile * 8; c += 32) tile[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
         tc::fence_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.v_tail));
@@ -333,7 +360,7 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       const int slot = u % stages;
       ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
       if (!ok) break;
-      uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kTileBytes);
+      uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry);
 #pragma unroll 4
       for (int k = ct; k < kTileBytes / 16; k += kConvThreads) tile[k] = widen_chunk(tile[k]);
       tc::fence_async_smem();
@@ -362,11 +389,15 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
           const int slot = u % stages;
           if (tc::mbar_test_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u)) {
             tc::tc_fence_after();
-            const uint64_t kdesc =
-                tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, 16, 1024, tc::kSwizzle128B);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // K = 128 channels in steps of 32 bytes
-              tc::umma_f8f6f4(tS(nq), kdesc + uint64_t(2 * k), qdesc + uint64_t(2 * k), idesc_qk, k > 0);
+            for (int dh = 0; dh < DH; ++dh) {
+              const uint64_t kdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes, 16,
+                                                   1024, tc::kSwizzle128B);
+              const uint64_t qd = qdesc + uint64_t((uint32_t(dh) * kQSub) >> 4);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)  // 128 channels of the sub-tile in steps of 32 bytes
+                tc::umma_f8f6f4(tS(nq), kdesc + uint64_t(2 * k), qd + uint64_t(2 * k), idesc_qk, dh > 0 || k > 0);
+            }
             tc::umma_commit(tc::smem_u32(&ctl.s_full[bs(nq)]));
             tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
             ++nq;
@@ -383,15 +414,19 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
           const uint32_t vpar = tail ? 0u : uint32_t(u / stages) & 1u;
           if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[bs(np)]), bp(np)) && tc::mbar_test_wait(vbar, vpar)) {
             tc::tc_fence_after();
-            const uint64_t vdesc =
-                tc::smem_desc(ring_addr + uint32_t(slot) * kTileBytes, kTileBytes, 1024, tc::kSwizzle128B);
             // P, MN-major without swizzle: 8-key core groups 128 B apart (LBO),
             // 16-column blocks 2 KB apart (SBO)
             const uint64_t pdesc =
                 tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(bs(np)) * p_stride, 128, 2048, 0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V, 32 x 16 B of P)
-              tc::umma_f8f6f4(tO, vdesc + uint64_t(256 * k), pdesc + uint64_t(32 * k), idesc_pv, (np > 0 || k > 0));
+            for (int dh = 0; dh < DH; ++dh) {
+              const uint64_t vdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes,
+                                                   kTileBytes, 1024, tc::kSwizzle128B);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V, 32 x 16 B of P)
+                tc::umma_f8f6f4(tO + uint32_t(dh * NPV), vdesc + uint64_t(256 * k), pdesc + uint64_t(32 * k), idesc_pv,
+                                (np > 0 || k > 0));
+            }
             tc::umma_commit(tc::smem_u32(&ctl.o_full[bs(np)]));
             tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
             ++np;
@@ -435,57 +470,74 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       tc::named_bar_sync(1, 128);
       return fmaxf(fmaxf(ctl.qamax[slot][0], ctl.qamax[slot][1]), fmaxf(ctl.qamax[slot][2], ctl.qamax[slot][3]));
     };
+    // Q tile: DH sub-tiles (channels 128 dh ..) of [NQK rows][128 B], K-major,
+    // 128-byte swizzle: byte c of row r in sub-tile c >> 7, 16-byte chunk
+    // ((c & 127) >> 4) ^ (r & 7)
+    auto q_off = [&](int r, int c) {
+      return lay.q + uint32_t(c >> 7) * kQSub + uint32_t(r * 128 + ((((c & 127) >> 4) ^ (r & 7)) << 4) + (c & 15));
+    };
+    // zero rows r_from .. NQK-1 of every sub-tile
+    auto zero_rows = [&](int r_from) {
+      for (int i = xq; i < (NQK - r_from) * 8 * DH; i += 128) {
+        const int dh = i / ((NQK - r_from) * 8), j = i % ((NQK - r_from) * 8);
+        *reinterpret_cast<uint4*>(smem + lay.q + dh * kQSub + r_from * 128 + j * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
     if constexpr (QM == 0) {
-      // Q codes rows r0 .. r0+nr-1 -> Q tile [NQK rows][128 B], K-major,
-      // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); other rows 0.
-      const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * kHeadDim;
-      for (int i = xq; i < NQK * 8; i += 128) {
-        const int r = i >> 3, c = i & 7;
+      // Q codes rows r0 .. r0+nr-1 into the Q tile; other rows 0
+      const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * D;
+      for (int i = xq; i < NQK * 8 * DH; i += 128) {
+        const int r = i / (8 * DH), c = (i % (8 * DH)) * 16;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * kHeadDim + c * 16);
-        *reinterpret_cast<uint4*>(smem + lay.q + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * D + c);
+        *reinterpret_cast<uint4*>(smem + q_off(r, c)) = v;
       }
     } else if constexpr (QM == 2) {
       // mj_quantize_q's recipe, in the kernel: x = bf16 Q (times q_mul), the
       // scale from the amax over all q_len*h_r rows of (b, g), then e4m3
       // round-to-nearest-even satfinite, every step an IEEE float32 operation,
       // so the codes and the descale are the ones that call writes. Thread xq
-      // takes channel xq of every row.
-      const int c = xq;
-      auto q_in = [&](int rr) {
+      // takes channels xq + 128 dh of every row.
+      auto q_in = [&](int rr, int c) {
         const int tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
         float v = bf16_bits_to_float(p.q_bf16[int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c]);
-        if (p.q_mul) v = __fmul_rn(v, p.q_mul[int64_t(h) * kHeadDim + c]);
+        if (p.q_mul) v = __fmul_rn(v, p.q_mul[int64_t(h) * D + c]);
         return v;
       };
       // the tile's rows once, into registers (independent loads); the rows of
       // (b, g) outside the tile only count towards the amax
-      float xr[NR];
-#pragma unroll
-      for (int r = 0; r < NR; ++r) xr[r] = r < nr ? q_in(r0 + r) : 0.f;
+      float xr[DH][NR];
       float am = 0.f;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[r]));
-      for (int rr = 0; rr < p.n_q; ++rr)
-        if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr)));
+      for (int dh = 0; dh < DH; ++dh) {
+        const int c = xq + 128 * dh;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) xr[dh][r] = r < nr ? q_in(r0 + r, c) : 0.f;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[dh][r]));
+        for (int rr = 0; rr < p.n_q; ++rr)
+          if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr, c)));
+      }
       sq = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.0f);
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        uint8_t code = 0;
-        if (r < nr) code = __nv_cvt_float_to_fp8(__fdiv_rn(xr[r], sq), __NV_SATFINITE, __NV_E4M3);
-        smem[lay.q + r * 128 + (((c >> 4) ^ (r & 7)) << 4) + (c & 15)] = code;
+      for (int dh = 0; dh < DH; ++dh) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          uint8_t code = 0;
+          if (r < nr) code = __nv_cvt_float_to_fp8(__fdiv_rn(xr[dh][r], sq), __NV_SATFINITE, __NV_E4M3);
+          smem[q_off(r, xq + 128 * dh)] = code;
+        }
       }
-      for (int i = xq; i < (NQK - NR) * 8; i += 128)  // the rows past the tile
-        *reinterpret_cast<uint4*>(smem + lay.q + NR * 128 + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+      zero_rows(NR);  // the rows past the tile
     } else {
       // bf16 Q as two e4m3 terms: hi = e4m3(x / s_hi) with s_hi = amax/448,
       // lo = e4m3((x - hi*s_hi) / s_lo) with s_lo = (max |residual|)/448.
       // hi fills rows 0 .. NR-1 of the Q tile and lo rows NR .. 2NR-1, so one
       // QK product gives both terms; the logit is s_hi*S_hi + s_lo*S_lo.
-      // Thread xq owns NR consecutive channels of one row (NR x 128 values
-      // over 128 threads).
-      constexpr int EPT = NR;
-      const int row = (xq * EPT) / kHeadDim, c0 = (xq * EPT) % kHeadDim;
+      // Thread xq owns EPT consecutive channels of one row (NR x D values
+      // over 128 threads; EPT divides 128, so they share one sub-tile).
+      constexpr int EPT = NR * DH;
+      const int row = (xq * EPT) / D, c0 = (xq * EPT) % D;
       float xv[EPT];
 #pragma unroll
       for (int e = 0; e < EPT; ++e) xv[e] = 0.f;
@@ -532,16 +584,14 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
         else
           lw[e / 4] |= uint32_t(l2) << 16;
       }
-      // 4 codes per word; byte (c & 15) of 16-byte chunk (c >> 4) ^ (row & 7)
+      // 4 codes per word (c is a multiple of 4: one 16-byte chunk)
 #pragma unroll
       for (int e = 0; e < EPT; e += 4) {
         const int c = c0 + e;
-        const int r_hi = row, r_lo = NR + row;
-        *reinterpret_cast<uint32_t*>(smem + lay.q + r_hi * 128 + (((c >> 4) ^ (r_hi & 7)) << 4) + (c & 15)) = hw[e / 4];
-        *reinterpret_cast<uint32_t*>(smem + lay.q + r_lo * 128 + (((c >> 4) ^ (r_lo & 7)) << 4) + (c & 15)) = lw[e / 4];
+        *reinterpret_cast<uint32_t*>(smem + q_off(row, c)) = hw[e / 4];
+        *reinterpret_cast<uint32_t*>(smem + q_off(NR + row, c)) = lw[e / 4];
       }
-      for (int i = xq; i < (NQK - 2 * NR) * 8; i += 128)  // the rows past the two terms
-        *reinterpret_cast<uint4*>(smem + lay.q + 2 * NR * 128 + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+      zero_rows(2 * NR);  // the rows past the two terms
       const float kq = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g) * p.qk_scale_log2;
       sc_hi = s_hi * kq;
       sc_lo = s_lo * kq;
@@ -738,13 +788,13 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
         __syncwarp();  // lane 0's factors
         tc::tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < NPV; c += 16) {
+        for (int c = 0; c < DH * NPV; c += 16) {
           float v[16];
           tc::tmem_ld16(tO + lane_off + c, v);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int col = c + j;
+            const int col = (c + j) % NPV;            // column within its O accumulator
             const int r = col < NH ? col : col - NH;  // hi column r, lo column NH + r
             if (r < NR) v[j] *= ctl.alpha[qd][r];
           }
@@ -760,23 +810,28 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
         if (a < nt) tc::mbar_arrive(tc::smem_u32(&ctl.p_full[bs(i + a)]));
       if (!ok) break;
     }
-    // the final O: wait for the last PV product
-    float o_acc[NR];
+    // the final O: wait for the last PV product; o_acc[dh][r] is channel 128 dh + x
+    float o_acc[DH][NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) o_acc[r] = 0.f;
+    for (int dh = 0; dh < DH; ++dh)
+#pragma unroll
+      for (int r = 0; r < NR; ++r) o_acc[dh][r] = 0.f;
     ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(ntiles - 1)]), bp(ntiles - 1), abort, kWaitLimitNs);
     if (ok) {
       tc::tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < NPV; c += 16) {
-        float v[16];
-        tc::tmem_ld16(tO + lane_off + c, v);
-        tc::tmem_wait_ld();
+      for (int dh = 0; dh < DH; ++dh) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c + j;
-          const int r = col < NH ? col : col - NH;
-          if (r < NR) o_acc[r] += v[j];
+        for (int c = 0; c < NPV; c += 16) {
+          float v[16];
+          tc::tmem_ld16(tO + lane_off + dh * NPV + c, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c + j;
+            const int r = col < NH ? col : col - NH;
+            if (r < NR) o_acc[dh][r] += v[j];
+          }
         }
       }
     }
@@ -799,20 +854,27 @@ __global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 
       for (int r = 0; r < NR; ++r) {
         if (r >= nr) break;
         const float lr = ctl.lsum[0][r] + ctl.lsum[1][r] + ctl.lsum[2][r] + ctl.lsum[3][r];
-        const float on = lr > 0.f ? o_acc[r] / lr : 0.f;
         const int row = r0 + r;
-        if (direct) {
-          const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
-          float val = on * vd;
-          if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + x];
-          p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + x] = float_to_out_bits(val, p.out_f16);
-          if (p.lse && x == 0)
-            p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
-                lr > 0.f ? (m_ref[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
-        } else {
-          const int64_t idx = part_index(p, b, w.w, g, row);
-          p.o_part[idx * kHeadDim + x] = on;
-          if (x == 0) {
+        const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
+        const int64_t idx = direct ? 0 : part_index(p, b, w.w, g, row);
+#pragma unroll
+        for (int dh = 0; dh < DH; ++dh) {
+          const int ch = 128 * dh + x;
+          const float on = lr > 0.f ? o_acc[dh][r] / lr : 0.f;
+          if (direct) {
+            float val = on * vd;
+            if (p.o_mul) val *= p.o_mul[int64_t(h) * D + ch];
+            p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + ch] = float_to_out_bits(val, p.out_f16);
+          } else {
+            p.o_part[idx * D + ch] = on;
+          }
+        }
+        if (x == 0) {
+          if (direct) {
+            if (p.lse)
+              p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
+                  lr > 0.f ? (m_ref[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
+          } else {
             p.m_part[idx] = lr > 0.f ? m_ref[r] : -INFINITY;
             p.l_part[idx] = lr * (1.f / 256.f);
           }
@@ -860,7 +922,7 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   cuuint64_t strides[3];
   cuuint32_t box[4];
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  dims[0] = 128;
+  dims[0] = cuuint64_t(p.d);  // channels (e4m3 bytes, or e2m3 codes); a box is 128 of them
   box[0] = 128;
   if (head_inner) {
     dims[1] = cuuint64_t(p.h_k);
@@ -880,9 +942,10 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   dims[3] = cuuint64_t(p.num_pages);
   strides[2] = cuuint64_t(sp);
   box[3] = 1;
-  // e4m3: one byte per element. Packed e2m3: 16U6_ALIGN16B keeps 16 codes in
-  // 12 bytes and lands each group in a 16-byte shared-memory chunk (4 bytes of
-  // padding), which tcgen05.mma reads as e2m3; dims[0] counts codes (128).
+  // e4m3: one byte per element. Packed e2m3 (D = 128 only): 16U6_ALIGN16B
+  // keeps 16 codes in 12 bytes and lands each group in a 16-byte shared-memory
+  // chunk (4 bytes of padding), which tcgen05.mma reads as e2m3; dims[0]
+  // counts codes.
   const CUtensorMapDataType dt =
       p.kv_format == MJ_KV_E2M3 ? CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -891,14 +954,21 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   return r == CUDA_SUCCESS;
 }
 
-template <int NQK, int NPV, int NR, bool FP6, int QM = 0>
-cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
-  const TcSmem lay = tc_smem_layout(p.kv_stages, NQK, NPV, NR <= 8 ? 4 : 2);
-  const int bytes = int(lay.total) + 1024;
+constexpr int kMaxDynSmem = 227 * 1024;  // per-block opt-in limit of sm_100-class GPUs
+
+template <int NQK, int NPV, int NR, bool FP6, int QM, int D>
+cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p0, cudaStream_t stream) {
+  DecodeParams p = p0;
+  // the ring depth the shared memory holds (even, at least 2)
+  auto smem_bytes = [&](int stages) {
+    return int(tc_smem_layout(stages, NQK, NPV, NR <= 8 ? 4 : 2, D / 128).total) + 1024;
+  };
+  while (p.kv_stages > 2 && smem_bytes(p.kv_stages) > kMaxDynSmem) p.kv_stages -= 2;
+  const int bytes = smem_bytes(p.kv_stages);
   static int configured = 0;  // largest dynamic smem size set so far
   if (bytes > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6, QM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         bytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6, QM, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     configured = bytes;
   }
@@ -913,29 +983,32 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6, QM>, mk, mv, p);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6, QM, D>, mk, mv, p);
 }
 
 // The kernel instance for the row tile (the plan's tile width, 16 or 32
 // rows; fewer rows take the 4- or 8-row variants). With bf16 Q as two terms
 // the Q tile holds two rows (hi, lo) per query row.
-template <bool FP6, int QM>
+template <bool FP6, int QM, int D = 128>
 cudaError_t launch_rows(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
   constexpr int K = QM == 1 ? 2 : 1;
   if (p.tw <= 16) {
-    if (p.n_q <= 4) return launch_tc<16, 16, 4, FP6, QM>(mk, mv, p, stream);
-    if (p.n_q <= 8) return launch_tc<16, 16, 8, FP6, QM>(mk, mv, p, stream);
-    return launch_tc<16 * K, 32, 16, FP6, QM>(mk, mv, p, stream);
+    if (p.n_q <= 4) return launch_tc<16, 16, 4, FP6, QM, D>(mk, mv, p, stream);
+    if (p.n_q <= 8) return launch_tc<16, 16, 8, FP6, QM, D>(mk, mv, p, stream);
+    return launch_tc<16 * K, 32, 16, FP6, QM, D>(mk, mv, p, stream);
   }
-  return launch_tc<32 * K, 64, 32, FP6, QM>(mk, mv, p, stream);
+  return launch_tc<32 * K, 64, 32, FP6, QM, D>(mk, mv, p, stream);
 }
 
 }  // namespace
 
-int tc_default_stages() { return 6; }
+// Default ring depth: 6 entries (3 K and 3 V tiles); with D = 256 an entry is
+// 32 KB, and 2 entries keep two CTAs per SM (a deeper ring takes ctas_per_sm = 1).
+int tc_default_stages(int d) { return d == 256 ? 2 : 6; }
 
 bool tc_supported(const DecodeParams& p) {
   if (p.q_mode == MJ_Q_BF16 && p.kv_format != MJ_KV_E4M3) return false;
+  if (p.kv_format == MJ_KV_E2M3 && p.d != 128) return false;  // packed e2m3: D = 128 only
   if (p.kv_format == MJ_KV_E2M3) {
     // the packed TMA type wants 32-byte aligned strides (and base, checked
     // by the ABI for e2m3)
@@ -962,7 +1035,7 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
     *unsupported = true;
     return cudaSuccess;
   }
-  if (p.kv_stages <= 0) p.kv_stages = tc_default_stages();
+  if (p.kv_stages <= 0) p.kv_stages = tc_default_stages(p.d);
   if (p.kv_stages > tc_max_stages()) p.kv_stages = tc_max_stages();
   // The ring depth is always even, so that K tiles (ring entries u = 2i) and
   // V tiles (u = 2i + 1) never share a slot. Every waiter on full[slot] must
@@ -994,6 +1067,11 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
     // packed e2m3 KV takes fp8 Q only: codes, or quantized here
     return p.q_mode == MJ_Q_FP8_FUSED ? launch_rows<true, 2>(mk, mv, p, stream)
                                       : launch_rows<true, 0>(mk, mv, p, stream);
+  }
+  if (p.d == 256) {
+    if (p.q_mode == MJ_Q_BF16) return launch_rows<false, 1, 256>(mk, mv, p, stream);
+    if (p.q_mode == MJ_Q_FP8_FUSED) return launch_rows<false, 2, 256>(mk, mv, p, stream);
+    return launch_rows<false, 0, 256>(mk, mv, p, stream);
   }
   if (p.q_mode == MJ_Q_BF16) return launch_rows<false, 1>(mk, mv, p, stream);
   if (p.q_mode == MJ_Q_FP8_FUSED) return launch_rows<false, 2>(mk, mv, p, stream);

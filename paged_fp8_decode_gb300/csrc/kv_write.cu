@@ -126,10 +126,10 @@ __device__ __forceinline__ void quantize_store(const uint4* in, const float* sca
 // alias the inputs as far as the compiler knows, so it would not reorder
 // them itself). The row index (token, head) fits in 32 bits (checked on the
 // host).
-template <bool E2M3>
+template <bool E2M3, int D>
 __global__ void __launch_bounds__(kThreads) write_kv_kernel(WriteParams p) {
   constexpr int CH = E2M3 ? 16 : 8;
-  constexpr int NCH = kHeadDim / CH;  // chunks per row
+  constexpr int NCH = D / CH;  // chunks per row
   constexpr int NV = CH / 8;          // 16-byte loads per chunk of one side
   constexpr int U = E2M3 ? 2 : 4;     // items per thread per round
   const uint64_t total = uint64_t(uint32_t(p.num_tokens) * uint32_t(p.h_k)) * NCH;
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) write_kv_kernel(WriteParams p) {
       }
       const int g = head[u];
       const int64_t page = slot[u] / p.page_size, prow = slot[u] % p.page_size;
-      const int s_idx = E2M3 ? g * kHeadDim : (p.scale_per_head ? g : 0);
+      const int s_idx = E2M3 ? g * D : (p.scale_per_head ? g : 0);
       quantize_store<E2M3>(kin[u], p.k_scale + s_idx, p.k_cache + page * p.k_sp + prow * p.k_st + g * p.k_sh,
                            chunk[u]);
       quantize_store<E2M3>(vin[u], p.v_scale + s_idx, p.v_cache + page * p.v_sp + prow * p.v_st + g * p.v_sh,
@@ -206,7 +206,7 @@ cudaError_t launch_write_kv(const mj_write_kv_args& a, cudaStream_t stream) {
   p.scale_per_head = a.scale_per_head;
   p.status = a.status;
   const bool e2m3 = a.kv_format == MJ_KV_E2M3;
-  const int64_t work = int64_t(a.num_tokens) * a.h_k * (kHeadDim / (e2m3 ? 16 : 8));
+  const int64_t work = int64_t(a.num_tokens) * a.h_k * (a.d / (e2m3 ? 16 : 8));
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -222,10 +222,18 @@ cudaError_t launch_write_kv(const mj_write_kv_args& a, cudaStream_t stream) {
   const int sms = sm_count[dev];
   // enough blocks to fill every SM (8 x 256 threads each), fewer for small writes
   const int64_t blocks = std::min<int64_t>((work + kThreads - 1) / kThreads, int64_t(sms) * 8);
-  if (e2m3)
-    write_kv_kernel<true><<<unsigned(blocks), kThreads, 0, stream>>>(p);
-  else
-    write_kv_kernel<false><<<unsigned(blocks), kThreads, 0, stream>>>(p);
+  const unsigned nb = unsigned(blocks);
+  if (a.d == 256) {
+    if (e2m3)
+      write_kv_kernel<true, 256><<<nb, kThreads, 0, stream>>>(p);
+    else
+      write_kv_kernel<false, 256><<<nb, kThreads, 0, stream>>>(p);
+  } else {
+    if (e2m3)
+      write_kv_kernel<true, 128><<<nb, kThreads, 0, stream>>>(p);
+    else
+      write_kv_kernel<false, 128><<<nb, kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -9,7 +9,8 @@
 // and rows with no visible key in a split (m = -inf, l = 0) weigh zero; the
 // exponent is never formed from two infinities.
 //
-// One CTA per (request, KV head, query row), one thread per channel: the
+// One CTA per (request, KV head, query row), one thread per channel (D = 128
+// or 256): the
 // split weights are computed by as many threads in parallel, and the channel
 // sums read the partials with independent, coalesced loads.
 #include "mj_device.cuh"
@@ -19,11 +20,12 @@ namespace mj {
 
 namespace {
 
-constexpr int kMergeThreads = kHeadDim;  // 4 warps
-
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
+// D threads (one per channel): 4 warps for D = 128, 8 for D = 256
+template <int D>
+__global__ void __launch_bounds__(D) merge_kernel(DecodeParams p) {
+  constexpr int kWarps = D / 32;
   extern __shared__ float wsh[];  // weights of the live splits
-  __shared__ float red[kMergeThreads / 32];
+  __shared__ float red[kWarps];
   // launched with programmatic stream serialization: the partials are the
   // preceding decode grid's output
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -38,16 +40,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
 
   // max logit over the live splits
   float mloc = -INFINITY;
-  for (int s = c; s < live; s += kMergeThreads) mloc = fmaxf(mloc, p.m_part[part_index(p, b, s, g, row)]);
+  for (int s = c; s < live; s += D) mloc = fmaxf(mloc, p.m_part[part_index(p, b, s, g, row)]);
   mloc = warp_max(mloc);
   if (lane == 0) red[warp] = mloc;
   __syncthreads();
-  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float M = red[0];
+#pragma unroll
+  for (int w2 = 1; w2 < kWarps; ++w2) M = fmaxf(M, red[w2]);
   __syncthreads();
 
   // split weights
   float wloc = 0.f;
-  for (int s = c; s < live; s += kMergeThreads) {
+  for (int s = c; s < live; s += D) {
     const int64_t idx = part_index(p, b, s, g, row);
     const float ms = p.m_part[idx];
     const float wgt = (M == -INFINITY || ms == -INFINITY) ? 0.f : fast_exp2(ms - M) * p.l_part[idx];
@@ -57,11 +61,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
   wloc = warp_sum(wloc);
   if (lane == 0) red[warp] = wloc;
   __syncthreads();
-  const float wsum = red[0] + red[1] + red[2] + red[3];
+  float wsum = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < kWarps; ++w2) wsum += red[w2];
 
   // weighted channel sum
-  const float* op = p.o_part + part_index(p, b, 0, g, row) * kHeadDim + c;
-  const int64_t split_stride = int64_t(p.h_k) * p.n_q * kHeadDim;  // part_index step per split
+  const float* op = p.o_part + part_index(p, b, 0, g, row) * D + c;
+  const int64_t split_stride = int64_t(p.h_k) * p.n_q * D;  // part_index step per split
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   int s = 0;
   for (; s + 4 <= live; s += 4) {
@@ -76,7 +82,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
   const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
   const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
   float val = wsum > 0.f ? acc / wsum * vd : 0.f;
-  if (p.o_mul) val *= p.o_mul[int64_t(h) * kHeadDim + c];
+  if (p.o_mul) val *= p.o_mul[int64_t(h) * D + c];
   p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + c] = float_to_out_bits(val, p.out_f16);
   if (p.lse && c == 0)
     p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] = wsum > 0.f ? (M + fast_log2(wsum)) * kLn2 : -INFINITY;
@@ -88,7 +94,7 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   if (!p.with_reduction || p.num_seqs == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_seqs, p.h_k, p.n_q);
-  cfg.blockDim = dim3(kMergeThreads);
+  cfg.blockDim = dim3(p.d);
   cfg.dynamicSmemBytes = size_t(p.max_splits) * sizeof(float);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -96,7 +102,7 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+  return p.d == 256 ? cudaLaunchKernelEx(&cfg, merge_kernel<256>, p) : cudaLaunchKernelEx(&cfg, merge_kernel<128>, p);
 }
 
 }  // namespace mj

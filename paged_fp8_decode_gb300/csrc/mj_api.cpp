@@ -37,7 +37,7 @@ bool page_size_ok(int ps) { return ps == 16 || ps == 32 || ps == 64 || ps == 128
 int make_params(const mj_decode_args* a, DecodeParams* p) {
   if (!a) return MJ_ERR_INVALID_ARG;
   if (a->num_seqs < 0 || a->q_len < 1 || a->h_k < 1 || a->h_q < 1 || a->h_q % a->h_k) return MJ_ERR_INVALID_ARG;
-  if (a->d != mj::kHeadDim) return MJ_ERR_UNSUPPORTED;
+  if (!mj::head_dim_ok(a->d)) return MJ_ERR_UNSUPPORTED;
   if (a->kv_format != MJ_KV_E4M3 && a->kv_format != MJ_KV_E2M3) return MJ_ERR_UNSUPPORTED;
   if (!page_size_ok(a->page_size)) return MJ_ERR_UNSUPPORTED;
   if (a->num_pages < 1 || a->num_work < 0 || a->block_table_stride < 0) return MJ_ERR_INVALID_ARG;
@@ -259,7 +259,7 @@ int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, in
                   int h_q, int h_k, int d, const float* q_mul, uint8_t* q_codes, float* q_descale,
                   void* stream) {
   if (num_seqs < 0 || q_len < 1 || h_k < 1 || h_q < 1 || h_q % h_k) return MJ_ERR_INVALID_ARG;
-  if (d != mj::kHeadDim) return MJ_ERR_UNSUPPORTED;
+  if (!mj::head_dim_ok(d)) return MJ_ERR_UNSUPPORTED;
   if (num_seqs == 0) return MJ_OK;
   if (!q || !q_codes || !q_descale) return MJ_ERR_INVALID_ARG;
   if (q_tok_stride < 0 || q_head_stride < 0) return MJ_ERR_INVALID_ARG;
@@ -285,7 +285,7 @@ int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, in
 int mj_write_kv(const mj_write_kv_args* a, void* stream) {
   if (!a) return MJ_ERR_INVALID_ARG;
   if (a->num_tokens < 0 || a->h_k < 1 || a->num_pages < 0) return MJ_ERR_INVALID_ARG;
-  if (a->d != mj::kHeadDim) return MJ_ERR_UNSUPPORTED;
+  if (!mj::head_dim_ok(a->d)) return MJ_ERR_UNSUPPORTED;
   if (a->kv_format != MJ_KV_E4M3 && a->kv_format != MJ_KV_E2M3) return MJ_ERR_UNSUPPORTED;
   if (a->page_size != 16 && a->page_size != 32 && a->page_size != 64 && a->page_size != 128)
     return MJ_ERR_UNSUPPORTED;
@@ -314,7 +314,7 @@ int mj_write_kv(const mj_write_kv_args* a, void* stream) {
 int mj_workspace_size(int part_seqs, int max_splits, int max_q_len, int h_q, int h_k, int d, size_t* bytes) {
   if (!bytes || part_seqs < 0 || max_splits < 1 || max_q_len < 1 || h_k < 1 || h_q < 1 || h_q % h_k)
     return MJ_ERR_INVALID_ARG;
-  if (d != mj::kHeadDim) return MJ_ERR_UNSUPPORTED;
+  if (!mj::head_dim_ok(d)) return MJ_ERR_UNSUPPORTED;
   const int64_t rows = int64_t(part_seqs) * max_splits * h_k * int64_t(max_q_len) * (h_q / h_k);
   *bytes = mj::kWsHeader + size_t(rows) * (size_t(d) + 2) * sizeof(float);
   return MJ_OK;

@@ -10,7 +10,10 @@
 namespace mj {
 
 constexpr int kKvTile = 128;   // tokens per KV tile (the plan's unit)
-constexpr int kHeadDim = 128;  // supported head size
+constexpr int kMaxHeadDim = 256;
+// Supported head sizes: 128 and 256 (the runner page's T5DecodeRunner asserts
+// head_size % 128 == 0; its kernels are built per head size).
+inline bool head_dim_ok(int d) { return d == 128 || d == 256; }
 constexpr int kMaxRowTile = 32;
 
 // Workspace layout: a 256-byte header (status word at offset 0), then the

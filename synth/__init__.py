@@ -323,6 +323,14 @@ def fp6_decode(seed: int = 1005) -> Workload:
                      seed=seed)
 
 
+def d256_decode(seed: int = 1006) -> Workload:
+    """B=64, q_len=1, 16/8 heads (GQA 2), head size 256 (the head shape of
+    Gemma-2/3-class models), page 16, every length 4096, per-KV-head e4m3
+    scales, HND: 1.07 GB of KV, twice the Qwen3-8B batch's."""
+    return make_case(name="d256_decode", num_seqs=64, q_len=1, h_q=16, h_k=8, d=256, page_size=16,
+                     seq_lens=[4096] * 64, layout="HND", scale_mode="head", seed=seed)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "qwen3_8b_decode": qwen3_8b_decode,
@@ -331,6 +339,7 @@ WORKLOADS = {
     "spec_verify": spec_verify,
     "spec_verify_noncausal": lambda seed=1004: spec_verify(False, seed),
     "fp6_decode": fp6_decode,
+    "d256_decode": d256_decode,
 }
 
 

@@ -104,7 +104,8 @@ def _valid_args():
 
 @pytest.mark.parametrize("field,value,status", [
     ("d", 64, mj.MJ_ERR_UNSUPPORTED),
-    ("d", 256, mj.MJ_ERR_UNSUPPORTED),
+    ("d", 192, mj.MJ_ERR_UNSUPPORTED),
+    ("d", 512, mj.MJ_ERR_UNSUPPORTED),
     ("page_size", 8, mj.MJ_ERR_UNSUPPORTED),
     ("kv_format", 7, mj.MJ_ERR_UNSUPPORTED),
     ("h_q", 9, mj.MJ_ERR_INVALID_ARG),
@@ -150,12 +151,30 @@ def test_reduction_needs_a_large_enough_workspace(lib):
 def test_workspace_size_formula(lib):
     n = mj.mj_workspace_size(38, 64, 1, 32, 8)
     assert n == 256 + 38 * 64 * 8 * 4 * (128 + 2) * 4
+    n = mj.mj_workspace_size(38, 64, 1, 16, 8, 256)
+    assert n == 256 + 38 * 64 * 8 * 2 * (256 + 2) * 4
+    with pytest.raises(mj.MjError):
+        mj.mj_workspace_size(38, 64, 1, 16, 8, 192)
+
+
+def test_head_size_256_passes_the_host_checks(lib):
+    """D = 256 is accepted: with no work rows the call validates and returns
+    MJ_OK without launching anything (no device is touched)."""
+    a = _valid_args()
+    a.d = 256
+    a.k_stride_page, a.k_stride_token, a.k_stride_head = 8192, 256, 4096
+    a.v_stride_page, a.v_stride_token, a.v_stride_head = 8192, 256, 4096
+    a.out_tok_stride, a.out_head_stride = 2048, 256
+    a.num_work, a.impl = 0, 1  # nothing to launch; the CUDA-core path needs no driver query
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_OK
+    assert lib.mj_merge_lse(ctypes.byref(a), None) == mj.MJ_OK  # no reduction: nothing to merge
 
 
 def test_quantize_rejections(lib):
     f = lib.mj_quantize_q
     base = 1 << 40
     assert f(base, 4096, 128, 2, 1, 32, 8, 64, None, base, base, None) == mj.MJ_ERR_UNSUPPORTED
+    assert f(base, 8192, 256, 2, 1, 32, 8, 384, None, base, base, None) == mj.MJ_ERR_UNSUPPORTED
     assert f(base, 4096, 128, 2, 1, 30, 8, 128, None, base, base, None) == mj.MJ_ERR_INVALID_ARG
     assert f(None, 4096, 128, 2, 1, 32, 8, 128, None, base, base, None) == mj.MJ_ERR_INVALID_ARG
     assert f(base + 2, 4096, 128, 2, 1, 32, 8, 128, None, base, base, None) == mj.MJ_ERR_ALIGNMENT

@@ -66,6 +66,11 @@ SMALL = [
          outlier_channels=4, pad_every=9, seed=44),
     dict(name="e2m3_nhd", num_tokens=97, num_pages=12, page_size=16, layout="NHD", kv_format="e2m3",
          outlier_channels=4, pad_every=3, seed=45),
+    # head size 256: 256-byte e4m3 rows, 192-byte packed e2m3 rows
+    dict(name="fp8_d256_nhd", num_tokens=211, d=256, num_pages=30, page_size=16, layout="NHD", kv_format="fp8",
+         scale_mode="head", pad_every=6, seed=50),
+    dict(name="e2m3_d256_hnd", num_tokens=150, d=256, num_pages=4, page_size=64, layout="HND", kv_format="e2m3",
+         outlier_channels=4, pad_every=8, seed=51),
 ]
 
 

@@ -29,10 +29,11 @@ def _small(**kw):
     return synth.make_case(**base)
 
 
-@pytest.mark.parametrize("kv_format,q_len,causal", [("fp8", 1, True), ("fp8", 3, True),
-                                                    ("fp8", 3, False), ("e2m3", 2, True)])
-def test_matches_brute_force(kv_format, q_len, causal):
-    w = _small(kv_format=kv_format, q_len=q_len, causal=causal, seq_lens=[5, 21, 9],
+@pytest.mark.parametrize("kv_format,q_len,causal,d", [("fp8", 1, True, 128), ("fp8", 3, True, 128),
+                                                      ("fp8", 3, False, 128), ("e2m3", 2, True, 128),
+                                                      ("fp8", 2, True, 256), ("e2m3", 1, False, 256)])
+def test_matches_brute_force(kv_format, q_len, causal, d):
+    w = _small(kv_format=kv_format, q_len=q_len, causal=causal, seq_lens=[5, 21, 9], d=d,
                outlier_channels=2 if kv_format == "e2m3" else 0)
     codes, desc, out, _ = _run(w)
     for b in range(w.num_seqs):
@@ -81,8 +82,9 @@ def test_hnd_and_nhd_views_agree():
     np.testing.assert_array_equal(o1, o2)
 
 
-def test_constant_v_returns_v():
-    w = _small()
+@pytest.mark.parametrize("d", [128, 256])
+def test_constant_v_returns_v(d):
+    w = _small(d=d)
     w.v_cache[...] = F.e4m3_encode(1.5)
     _, _, out, _ = _run(w)
     for b in range(w.num_seqs):
@@ -102,8 +104,9 @@ def test_single_key_returns_its_v_row():
                 np.testing.assert_allclose(out[b, g * w.h_r + r], v, rtol=1e-13)
 
 
-def test_one_row_is_scipy_softmax_times_v():
-    w = _small()
+@pytest.mark.parametrize("d", [128, 256])
+def test_one_row_is_scipy_softmax_times_v(d):
+    w = _small(d=d)
     codes, desc, out, lse = _run(w)
     b, g = 1, 1
     L = int(w.seq_lens[b])

@@ -124,3 +124,24 @@ def test_token_order_does_not_matter(kv_format):
     perm = rng.permutation(T)
     W.write_kv(key[perm], val[perm], b_k, b_v, slots[perm], PS, st, st, kv_format, ks, vs)
     assert np.array_equal(a_k, b_k) and np.array_equal(a_v, b_v)
+
+
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+def test_head_size_256_row_is_two_128_channel_rows(kv_format):
+    """A 256-channel row's bytes are the two 128-channel halves' bytes side by
+    side: one code per byte (e4m3), or a little-endian 6-bit stream whose
+    first 128 codes fill exactly 96 bytes (e2m3). The 128-channel encoding is
+    pinned by the hand-packed fixtures."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((5, HK, 256)).astype(np.float32) * 3
+    if kv_format == W.KV_E4M3:
+        sc = rng.uniform(0.002, 0.05, HK).astype(np.float32)
+        lo, hi = sc, sc
+    else:
+        sc = rng.uniform(0.1, 2.0, (HK, 256)).astype(np.float32)
+        lo, hi = sc[:, :128], sc[:, 128:]
+    whole = W.quantize_rows(x, sc, kv_format)
+    assert whole.shape == (5, HK, W.row_bytes(256, kv_format))
+    halves = np.concatenate([W.quantize_rows(x[..., :128], lo, kv_format),
+                             W.quantize_rows(x[..., 128:], hi, kv_format)], axis=-1)
+    assert np.array_equal(whole, halves)

@@ -23,9 +23,11 @@ Sources (the mjolnir-kernel 0.1.0 pages):
 
 Modules:
 
-* :mod:`oracle.formats` — OCP e4m3 / e2m3 codecs and the fp6 4-in-3 packing.
+* :mod:`oracle.formats` — OCP e4m3 / e2m3 / e3m2 / e2m1 codecs, the fp6
+  4-in-3 packing and the fp4 2-per-byte packing.
 * :mod:`oracle.kvwrite` — the KV-cache write at ``slot_mapping`` (e4m3 with
-  per-tensor / per-head scales, packed e2m3 with per-channel scales).
+  per-tensor / per-head scales, packed e2m3 / e3m2 / e2m1 with per-channel
+  scales).
 * :mod:`oracle.qquant`  — the Q quantization recipe (bit-exact target).
 * :mod:`oracle.plan`    — ``tile_width``, ``slots`` and the split-KV plan
   (bit-exact target).

@@ -57,7 +57,10 @@ import math
 
 import numpy as np
 
-from .formats import e2m3_decode, e4m3_decode, fp6_unpack_rows
+from .formats import e2m1_decode, e2m3_decode, e3m2_decode, e4m3_decode, fp4_unpack_rows, fp6_unpack_rows
+
+# packed (narrow) KV formats: codes per row are unpacked before decoding
+_UNPACK = {"e2m3": fp6_unpack_rows, "e3m2": fp6_unpack_rows, "e2m1": fp4_unpack_rows}
 
 
 def decode_codes(codes, kv_format: str) -> np.ndarray:
@@ -65,6 +68,10 @@ def decode_codes(codes, kv_format: str) -> np.ndarray:
         return e4m3_decode(codes)
     if kv_format == "e2m3":
         return e2m3_decode(codes)
+    if kv_format == "e3m2":
+        return e3m2_decode(codes)
+    if kv_format == "e2m1":
+        return e2m1_decode(codes)
     raise ValueError(kv_format)
 
 
@@ -94,13 +101,13 @@ def gather_unit(k_logical, v_logical, block_table, b: int, g: int, L: int, page_
 
     ``*_logical``: ``[num_pages, page_size, h_k, row_bytes]`` byte arrays
     (any strides: a transposed view of an HND or NHD buffer). e4m3 rows are
-    one code per byte; packed e2m3 rows are unpacked here."""
+    one code per byte; packed e2m3 / e3m2 / e2m1 rows are unpacked here."""
     j = np.arange(L)
     pages = np.asarray(block_table)[b, j // page_size]
     slots_ = j % page_size
     kc, vc = k_logical[pages, slots_, g, :], v_logical[pages, slots_, g, :]
-    if kv_format == "e2m3":
-        kc, vc = fp6_unpack_rows(kc), fp6_unpack_rows(vc)
+    if kv_format in _UNPACK:
+        kc, vc = _UNPACK[kv_format](kc), _UNPACK[kv_format](vc)
     return kc, vc
 
 
@@ -207,8 +214,9 @@ def merge_partials(ms, ls, os_):
 def effective_kv_bytes(seq_lens, h_k: int, d: int, kv_format: str) -> int:
     """Algorithmic KV bytes of one step: every valid token's K and V row of
     every KV head, read once (``kv_row_bytes`` = d bytes for e4m3, d*6/8 for
-    packed e2m3, ``T5DecodeRunner.__init__``)."""
-    row = d if kv_format == "fp8" else d * 6 // 8
+    packed e2m3, ``T5DecodeRunner.__init__``; d*6/8 for e3m2 and d/2 for
+    e2m1 by the same count of bits)."""
+    row = {"fp8": d, "e2m3": d * 6 // 8, "e3m2": d * 6 // 8, "e2m1": d // 2}[kv_format]
     return int(sum(int(x) for x in seq_lens)) * h_k * 2 * row
 
 
@@ -216,12 +224,12 @@ def brute_force_unit(qcodes_bg, qdesc, k_logical, v_logical, kdesc, vdesc, block
                      page_size, kv_format, softmax_scale, q_len, h_r, causal):
     """Triple loop over rows, keys and channels, scalar math only; for the
     tiny pin cases."""
-    from .formats import e2m3_value, e4m3_value
+    from .formats import e2m1_value, e2m3_value, e3m2_value, e4m3_value
 
-    dec = e4m3_value if kv_format == "fp8" else e2m3_value
-    if kv_format == "e2m3":  # unpack every page once, then index codes
-        k_logical = fp6_unpack_rows(k_logical)
-        v_logical = fp6_unpack_rows(v_logical)
+    dec = {"fp8": e4m3_value, "e2m3": e2m3_value, "e3m2": e3m2_value, "e2m1": e2m1_value}[kv_format]
+    if kv_format in _UNPACK:  # unpack every page once, then index codes
+        k_logical = _UNPACK[kv_format](k_logical)
+        v_logical = _UNPACK[kv_format](v_logical)
     n_q, d = qcodes_bg.shape
     out = np.zeros((n_q, d))
     for row in range(n_q):

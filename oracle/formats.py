@@ -20,12 +20,26 @@ Test infrastructure only (see :mod:`oracle`).
   A row of ``d`` codes is ``d*6/8`` bytes (``kv_row_bytes`` in
   ``T5DecodeRunner.__init__``).
 
+* **e3m2** (OCP FP6 E3M2) and **e2m1** (OCP FP4 E2M1): the other narrow KV
+  formats the package README lists ("Beyond fp8: the harness": fp6
+  ``e2m3``/``e3m2`` and fp4 ``e2m1``, read by ``tcgen05 kind::f8f6f4``). The
+  pages name them only; the codecs are the OCP definitions. e3m2: 1 sign
+  bit, 3 exponent bits with bias 3, 2 mantissa bits, subnormals ``m/4 *
+  2**-2``, largest ``1.75 * 2**4 = 28``. e2m1: 1 sign bit, 2 exponent bits
+  with bias 1, 1 mantissa bit, subnormal ``m/2``, largest ``1.5 * 2**2 = 6``.
+  Neither has NaN or infinity.
+* **packing** of those (readings): e3m2 rows as e2m3 rows (both are fp6);
+  e2m1 rows as a little-endian bitstream of 4-bit codes, code ``i`` at bits
+  ``[4*i, 4*i+4)`` (low nibble first), ``d/2`` bytes per row.
+
 Pins (``tests/test_oracle_formats.py``): hand-derived code values from the
 format definitions (``tests/golden/e4m3_codes.txt``,
-``tests/golden/e2m3_codes.txt``), exhaustive decode/encode round trips of
-both formats, ties-to-even at every midpoint, saturation, agreement with
+``tests/golden/e2m3_codes.txt``, ``tests/golden/e3m2_codes.txt``,
+``tests/golden/e2m1_codes.txt``), exhaustive decode/encode round trips of
+every format, ties-to-even at every midpoint, saturation, agreement with
 torch's own ``float8_e4m3fn`` conversion on random inputs, and hand-packed
-byte fixtures (``tests/golden/fp6_packing.txt``) read in both directions.
+byte fixtures (``tests/golden/fp6_packing.txt``,
+``tests/golden/fp4_packing.txt``) read in both directions.
 """
 
 from __future__ import annotations
@@ -34,6 +48,8 @@ import numpy as np
 
 E4M3_MAX = 448.0
 E2M3_MAX = 7.5
+E3M2_MAX = 28.0
+E2M1_MAX = 6.0
 
 
 # ----------------------------------------------------------------------------
@@ -146,6 +162,113 @@ def e2m3_encode(x) -> np.ndarray:
     code = np.where(top, 0x1F, code).astype(np.uint8)
     code = np.where(np.signbit(x), code | 0x20, code).astype(np.uint8)
     return code
+
+
+# ----------------------------------------------------------------------------
+# e3m2 and e2m1
+# ----------------------------------------------------------------------------
+def e3m2_value(code: int) -> float:
+    """Value of one 6-bit e3m2 code, straight from the bit fields."""
+    code = int(code) & 0x3F
+    sign = -1.0 if code & 0x20 else 1.0
+    e = (code >> 2) & 0x7
+    m = code & 0x3
+    if e == 0:
+        return sign * (m / 4.0) * 2.0 ** (1 - 3)
+    return sign * (1.0 + m / 4.0) * 2.0 ** (e - 3)
+
+
+def e2m1_value(code: int) -> float:
+    """Value of one 4-bit e2m1 code, straight from the bit fields."""
+    code = int(code) & 0xF
+    sign = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return sign * (m / 2.0) * 2.0 ** (1 - 1)
+    return sign * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+E3M2_TABLE = np.array([e3m2_value(c) for c in range(64)], dtype=np.float64)
+E2M1_TABLE = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e3m2_decode(codes) -> np.ndarray:
+    return E3M2_TABLE[np.asarray(codes, dtype=np.uint8) & 0x3F]
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    return E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF]
+
+
+def _nearest_code(x, pos_values, sign_bit: int) -> np.ndarray:
+    """The plain rounding rule of :func:`e2m3_encode` over a format's
+    non-negative values in code order (strictly increasing): the nearer
+    neighbour, the even code at an exact midpoint, saturation at the largest
+    magnitude, and the sign bit set when ``x`` has its sign bit set."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    vals = pos_values
+    n = len(vals)
+    i = np.searchsorted(vals, a, side="right") - 1  # vals[i] <= a
+    i = np.clip(i, 0, n - 1)
+    top = i >= n - 1
+    j = np.minimum(i + 1, n - 1)
+    twice = 2.0 * a  # exact: the values need few bits
+    mid = vals[i] + vals[j]
+    up = (twice > mid) | ((twice == mid) & (i % 2 == 1))
+    code = np.where(up, j, i)
+    code = np.where(top, n - 1, code).astype(np.uint8)
+    return np.where(np.signbit(x), code | sign_bit, code).astype(np.uint8)
+
+
+def e3m2_encode(x) -> np.ndarray:
+    """Round to the nearest e3m2 value, ties to the even code, saturating at
+    28 (code 0x1F); sign bit 5 follows the sign of ``x``. NaN is outside the
+    contract (the format has none)."""
+    return _nearest_code(x, E3M2_TABLE[:0x20], 0x20)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Round to the nearest e2m1 value, ties to the even code, saturating at 6
+    (code 0x7); sign bit 3 follows the sign of ``x``. NaN is outside the
+    contract."""
+    return _nearest_code(x, E2M1_TABLE[:0x8], 0x8)
+
+
+# ----------------------------------------------------------------------------
+# 2-codes-per-byte little-endian bitstream (e2m1 rows)
+# ----------------------------------------------------------------------------
+def fp4_unpack_rows(packed) -> np.ndarray:
+    """Packed rows ``[..., k]`` (uint8) -> codes ``[..., 2*k]``: code ``i`` is
+    bits ``[4i, 4i+4)`` of the row's little-endian bitstream (a plain loop)."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    nbytes = packed.shape[-1]
+    flat = packed.reshape(-1, nbytes).astype(np.uint32)
+    out = np.zeros((flat.shape[0], 2 * nbytes), dtype=np.uint8)
+    for i in range(2 * nbytes):
+        code = np.zeros(flat.shape[0], dtype=np.uint32)
+        for k in range(4):
+            bit = 4 * i + k
+            code |= ((flat[:, bit // 8] >> (bit % 8)) & 1) << k
+        out[:, i] = code
+    return out.reshape(packed.shape[:-1] + (2 * nbytes,))
+
+
+def fp4_pack_rows(codes) -> np.ndarray:
+    """Codes ``[..., 2*k]`` (4-bit values in uint8) -> packed rows ``[..., k]``;
+    the inverse of :func:`fp4_unpack_rows` (bit ``k`` of code ``i`` to bit
+    ``4i + k``)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    ncodes = codes.shape[-1]
+    assert ncodes % 2 == 0, "a packed e2m1 row holds a whole number of bytes"
+    flat = codes.reshape(-1, ncodes).astype(np.uint32)
+    out = np.zeros((flat.shape[0], ncodes // 2), dtype=np.uint32)
+    for i in range(ncodes):
+        for k in range(4):
+            bit = 4 * i + k
+            out[:, bit // 8] |= ((flat[:, i] >> k) & 1) << (bit % 8)
+    return out.astype(np.uint8).reshape(codes.shape[:-1] + (ncodes // 2,))
 
 
 # ----------------------------------------------------------------------------

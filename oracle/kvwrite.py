@@ -21,6 +21,11 @@ Sources:
   write". Reading: ``code = e2m3(x / s[h, c])`` (round-to-nearest-even,
   saturating at 7.5), the row's codes packed 4 per 3 bytes
   (:func:`oracle.formats.fp6_pack_rows`).
+* **e3m2 / e2m1 caches** -- the README names these formats beside e2m3 and
+  gives no write for them. Reading: the e2m3 recipe with the format's own
+  encoder (saturating at 28 / 6) and per-(KV head, channel) scales; e3m2 rows
+  packed like e2m3 rows, e2m1 rows 2 codes per byte, low nibble first
+  (:func:`oracle.formats.fp4_pack_rows`).
 * **slots** -- ``slot_mapping[t]`` is the cache slot of token ``t``: page
   ``slot // page_size``, row ``slot % page_size`` (the paged layout of the
   decode path). Reading, as in the serving engine the backend plugs into: a
@@ -41,21 +46,24 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import e2m3_encode, e4m3_encode, fp6_pack_rows
+from .formats import e2m1_encode, e2m3_encode, e3m2_encode, e4m3_encode, fp4_pack_rows, fp6_pack_rows
 
-KV_E4M3, KV_E2M3 = 0, 1
+KV_E4M3, KV_E2M3, KV_E3M2, KV_E2M1 = 0, 1, 2, 3
 
 
 def row_bytes(d: int, kv_format: int) -> int:
-    """Bytes of one (token, KV head) row: ``d`` (e4m3) or ``3d/4`` (e2m3)."""
-    return d if kv_format == KV_E4M3 else d * 3 // 4
+    """Bytes of one (token, KV head) row: ``d`` (e4m3), ``3d/4`` (e2m3,
+    e3m2) or ``d/2`` (e2m1)."""
+    if kv_format == KV_E4M3:
+        return d
+    return d // 2 if kv_format == KV_E2M1 else d * 3 // 4
 
 
 def quantize_rows(x, scale, kv_format: int) -> np.ndarray:
     """Rows ``x`` ``[n, H_k, D]`` -> cache rows ``[n, H_k, row_bytes]``.
 
     ``scale``: e4m3 -- shape ``(1,)`` (per tensor) or ``(H_k,)`` (per head);
-    e2m3 -- shape ``(H_k, D)`` (per head and channel).
+    e2m3 / e3m2 / e2m1 -- shape ``(H_k, D)`` (per head and channel).
     """
     x = np.asarray(x, dtype=np.float32)
     s = np.asarray(scale, dtype=np.float32)
@@ -64,7 +72,13 @@ def quantize_rows(x, scale, kv_format: int) -> np.ndarray:
         y = (x / s).astype(np.float32)  # IEEE float32 quotient
         return e4m3_encode(y)
     y = (x / s.reshape(1, *s.shape)).astype(np.float32)
-    return fp6_pack_rows(e2m3_encode(y))
+    if kv_format == KV_E2M3:
+        return fp6_pack_rows(e2m3_encode(y))
+    if kv_format == KV_E3M2:
+        return fp6_pack_rows(e3m2_encode(y))
+    if kv_format == KV_E2M1:
+        return fp4_pack_rows(e2m1_encode(y))
+    raise ValueError(kv_format)
 
 
 def write_kv(key, value, k_pool, v_pool, slot_mapping, page_size: int, k_strides, v_strides,

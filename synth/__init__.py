@@ -11,10 +11,14 @@ N(0,1) values to the stored code format:
   ``s = amax/448`` per tensor or per KV head;
 * e2m3 KV: nearest of the 64 e2m3 values (ties to the even code) of
   ``X / s_c`` with static per-(KV head, channel) scales ``s_c = amax/7.5``,
-  packed 4 codes per 3 bytes as a little-endian bitstream.
+  packed 4 codes per 3 bytes as a little-endian bitstream;
+* e3m2 / e2m1 KV: the same with the format's largest value (28 / 6) in the
+  scale; e3m2 rows packed like e2m3 rows, e2m1 rows 2 codes per byte (low
+  nibble first).
 
 Unused pool pages and the tail slots of each request's last page are
-poisoned (e4m3 NaN ``0x7F``; e2m3 has no NaN, so its largest code ``0x1F``),
+poisoned (e4m3 NaN ``0x7F``; the narrow formats have no NaN, so their
+largest code: ``0x1F`` for e2m3 and e3m2, ``0x7`` for e2m1),
 and unused block-table entries are ``-1``: a decode path that reads past a
 request's last valid key shows up as NaN or as a wrong result.
 
@@ -33,6 +37,10 @@ import numpy as np
 
 E4M3_NAN = 0x7F
 E2M3_POISON = 0x1F
+E3M2_POISON = 0x1F
+E2M1_POISON = 0x7
+# the narrow (channel-scaled) KV formats: largest value, row bits per code
+NARROW = {"e2m3": (7.5, 6), "e3m2": (28.0, 6), "e2m1": (6.0, 4)}
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -52,7 +60,7 @@ class Workload:
     h_k: int
     d: int
     page_size: int
-    kv_format: str  # "fp8" | "e2m3"
+    kv_format: str  # "fp8" | "e2m3" | "e3m2" | "e2m1"
     layout: str  # "HND" | "NHD"
     causal: bool
     seq_lens: np.ndarray  # int32 [B]; padding requests 0
@@ -119,6 +127,51 @@ def _e2m3_codes(x: np.ndarray) -> np.ndarray:
     return code | np.where(np.signbit(x), np.uint8(0x20), np.uint8(0))
 
 
+def _e3m2_codes(x: np.ndarray) -> np.ndarray:
+    """Nearest e3m2 code (ties to even) of float32 values, saturating at 28.
+
+    In [0.25, 28] e3m2 and e5m2 both carry 2 mantissa bits with normal
+    exponents, so torch's float8_e5m2 conversion rounds identically there and
+    the e3m2 code is the e5m2 code with the exponent rebased (bias 15 -> 3).
+    Below 0.25, e3m2 is the subnormal grid k/16 and the code is rint(16|x|)."""
+    import torch
+
+    a = np.minimum(np.abs(x.astype(np.float32, copy=False)), np.float32(28.0))
+    c5 = torch.from_numpy(np.ascontiguousarray(a)).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    hi = (((c5 >> 2).astype(np.int16) - 12) << 2) | (c5 & 3)
+    lo = np.rint(a * np.float32(16.0)).astype(np.int16)
+    code = np.where(a >= 0.25, hi, lo).astype(np.uint8)
+    return code | np.where(np.signbit(x), np.uint8(0x20), np.uint8(0))
+
+
+def _e2m1_codes(x: np.ndarray) -> np.ndarray:
+    """Nearest e2m1 code (ties to even) of float32 values, saturating at 6:
+    per binade the code is its first code plus rint of the offset in steps
+    (0.5 below 2, 1 in [2, 4), 2 in [4, 6]); rint's ties to even are the even
+    codes."""
+    a = np.minimum(np.abs(x.astype(np.float32, copy=False)), np.float32(6.0))
+    code = np.where(a < 1.0, np.rint(2 * a),
+                    np.where(a < 2.0, 2 + np.rint(2 * (a - 1)),
+                             np.where(a < 4.0, 4 + np.rint(a - 2), 6 + np.rint((a - 4) / 2))))
+    code = code.astype(np.uint8)
+    return code | np.where(np.signbit(x), np.uint8(0x8), np.uint8(0))
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """``[..., 2k]`` 4-bit codes -> ``[..., k]`` bytes, code 2j in the low nibble of byte j."""
+    c = codes.astype(np.uint8).reshape(codes.shape[:-1] + (-1, 2))
+    return (c[..., 0] | (c[..., 1] << 4)).astype(np.uint8)
+
+
+def _narrow_rows(x: np.ndarray, kv_format: str) -> np.ndarray:
+    """Scaled values -> packed rows of a narrow format."""
+    if kv_format == "e2m3":
+        return pack_e2m3(_e2m3_codes(x))
+    if kv_format == "e3m2":
+        return pack_e2m3(_e3m2_codes(x))
+    return pack_e2m1(_e2m1_codes(x))
+
+
 def pack_e2m3(codes: np.ndarray) -> np.ndarray:
     """``[..., 4k]`` 6-bit codes -> ``[..., 3k]`` bytes, little-endian bitstream."""
     c = codes.astype(np.uint32).reshape(codes.shape[:-1] + (-1, 4))
@@ -141,8 +194,9 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
     ``seq_lens``: lengths of all ``num_seqs`` requests (0 = padding request).
     ``pool_pages``: pool size; default exactly the pages the requests use.
     Pages are drawn without replacement from the pool in a seeded random
-    order. ``scale_mode``: "tensor" | "head" (e4m3) — e2m3 always uses
-    per-(KV head, channel) scales folded into ``q_mul`` / ``o_mul``.
+    order. ``scale_mode``: "tensor" | "head" (e4m3) — the narrow formats
+    (e2m3, e3m2, e2m1) always use per-(KV head, channel) scales folded into
+    ``q_mul`` / ``o_mul``.
     """
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     assert seq_lens.shape == (num_seqs,)
@@ -171,7 +225,7 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
     tok_slots = np.concatenate(tok_slots) if tok_slots else np.zeros(0, np.int64)
     n_tok = len(tok_pages)
 
-    row_bytes = d if kv_format == "fp8" else d * 6 // 8
+    row_bytes = d if kv_format == "fp8" else d * NARROW[kv_format][1] // 8
     if layout == "HND":
         shape = (pool, h_k, page_size, row_bytes)
         strides = (h_k * page_size * row_bytes, row_bytes, page_size * row_bytes)
@@ -183,8 +237,10 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
 
     if kv_format == "fp8":
         poison_row = np.full(row_bytes, E4M3_NAN, dtype=np.uint8)
+    elif kv_format == "e2m1":
+        poison_row = pack_e2m1(np.full(d, E2M1_POISON, dtype=np.uint8))
     else:
-        poison_row = pack_e2m3(np.full(d, E2M3_POISON, dtype=np.uint8))
+        poison_row = pack_e2m3(np.full(d, E2M3_POISON if kv_format == "e2m3" else E3M2_POISON, dtype=np.uint8))
 
     # flat row index of (page, head g, slot) in the physical buffer
     def flat_rows(g):
@@ -232,10 +288,10 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
             else:
                 s_c = (np.maximum(x.max(axis=0), -x.min(axis=0)) if x.size
                        else np.ones(d, np.float32)).astype(np.float32)
-                s_c = np.maximum(s_c / np.float32(7.5), np.float32(1e-30))
+                s_c = np.maximum(s_c / np.float32(NARROW[kv_format][0]), np.float32(1e-30))
                 ch_scale[g] = s_c
                 np.divide(x, s_c[None, :], out=x)
-                codes = pack_e2m3(_e2m3_codes(x))
+                codes = _narrow_rows(x, kv_format)
             rows[flat_rows(g)] = codes
             if xs is not None:
                 xs[g] = None
@@ -257,7 +313,7 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
     q_f32 = qb.to(torch.float32).numpy().copy()
 
     q_mul = o_mul = None
-    if kv_format == "e2m3":
+    if kv_format in NARROW:
         q_mul = np.repeat(chans["k"], h_r, axis=0).astype(np.float32)
         o_mul = np.repeat(chans["v"], h_r, axis=0).astype(np.float32)
 
@@ -359,8 +415,8 @@ class WriteCase:
     kv_strides: tuple       # byte strides (page, token, head)
     page_size: int
     num_pages: int
-    kv_format: str          # "fp8" | "e2m3"
-    k_scale: np.ndarray     # float32: [1] / [h_k] (fp8) or [h_k, d] (e2m3)
+    kv_format: str          # "fp8" | "e2m3" | "e3m2" | "e2m1"
+    k_scale: np.ndarray     # float32: [1] / [h_k] (fp8) or [h_k, d] (narrow formats)
     v_scale: np.ndarray
     scale_per_head: bool
 
@@ -370,8 +426,8 @@ def kv_write_case(*, name="write", num_tokens, h_k=8, d=128, page_size=16, num_p
     """New K/V rows (N(0,1), rounded to bf16, optional x10 outlier channels),
     a slot for each token (distinct, random over the pool; every
     ``pad_every``-th token is padding, slot -1), pools pre-filled with random
-    bytes, and scales: fp8 ``amax/448`` per tensor or per KV head, e2m3
-    ``amax/7.5`` per (KV head, channel)."""
+    bytes, and scales: fp8 ``amax/448`` per tensor or per KV head, the narrow
+    formats ``amax/max`` per (KV head, channel) (max 7.5 / 28 / 6)."""
     import torch
 
     rng = _rng(seed, 20)
@@ -388,7 +444,7 @@ def kv_write_case(*, name="write", num_tokens, h_k=8, d=128, page_size=16, num_p
     slots = rng.permutation(cap)[:num_tokens].astype(np.int64)
     if pad_every:
         slots[pad_every - 1::pad_every] = -1
-    rb = d if kv_format == "fp8" else d * 3 // 4
+    rb = d if kv_format == "fp8" else d * NARROW[kv_format][1] // 8
     strides = (h_k * page_size * rb, rb, page_size * rb) if layout == "HND" else (page_size * h_k * rb, h_k * rb, rb)
     size = num_pages * page_size * h_k * rb
     k_pool = rng.integers(0, 256, size, dtype=np.uint8)
@@ -397,8 +453,8 @@ def kv_write_case(*, name="write", num_tokens, h_k=8, d=128, page_size=16, num_p
     scales = []
     for s in range(2):
         v = np.abs(xf[s][live]) if live.any() else np.ones((1, h_k, d), np.float32)
-        if kv_format == "e2m3":
-            scales.append(np.maximum(v.max(axis=0), 1e-6).astype(np.float32) / np.float32(7.5))
+        if kv_format in NARROW:
+            scales.append(np.maximum(v.max(axis=0), 1e-6).astype(np.float32) / np.float32(NARROW[kv_format][0]))
         elif scale_mode == "head":
             scales.append(np.maximum(v.max(axis=(0, 2)), 1e-6).astype(np.float32) / np.float32(448.0))
         else:

@@ -31,10 +31,12 @@ def _small(**kw):
 
 @pytest.mark.parametrize("kv_format,q_len,causal,d", [("fp8", 1, True, 128), ("fp8", 3, True, 128),
                                                       ("fp8", 3, False, 128), ("e2m3", 2, True, 128),
-                                                      ("fp8", 2, True, 256), ("e2m3", 1, False, 256)])
+                                                      ("fp8", 2, True, 256), ("e2m3", 1, False, 256),
+                                                      ("e3m2", 2, True, 128), ("e2m1", 1, True, 128),
+                                                      ("e2m1", 3, False, 256)])
 def test_matches_brute_force(kv_format, q_len, causal, d):
     w = _small(kv_format=kv_format, q_len=q_len, causal=causal, seq_lens=[5, 21, 9], d=d,
-               outlier_channels=2 if kv_format == "e2m3" else 0)
+               outlier_channels=0 if kv_format == "fp8" else 2)
     codes, desc, out, _ = _run(w)
     for b in range(w.num_seqs):
         for g in range(w.h_k):

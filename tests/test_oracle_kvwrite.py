@@ -34,7 +34,7 @@ def _scales(kv_format, rng):
     return rng.uniform(0.1, 2.0, (HK, D)).astype(np.float32), rng.uniform(0.1, 2.0, (HK, D)).astype(np.float32)
 
 
-@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3, W.KV_E3M2, W.KV_E2M1])
 @pytest.mark.parametrize("kind", ["HND", "NHD"])
 def test_padding_writes_nothing_and_rows_land_at_their_slots(kv_format, kind):
     rng = np.random.default_rng(11)
@@ -84,7 +84,21 @@ def test_e2m3_representable_rows_are_exact():
     assert np.array_equal(F.fp6_unpack_rows(rows), codes)
 
 
-@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+def test_narrow_representable_rows_are_exact():
+    """Power-of-two channel scales times e3m2 / e2m1 values: x / s is exactly
+    the value, so the rows hold exactly those codes."""
+    rng = np.random.default_rng(16)
+    s = (2.0 ** rng.integers(-4, 4, size=(HK, D))).astype(np.float32)
+    for fmt, ncode, dec, unpack, rb in ((W.KV_E3M2, 64, F.e3m2_decode, F.fp6_unpack_rows, 96),
+                                        (W.KV_E2M1, 16, F.e2m1_decode, F.fp4_unpack_rows, 64)):
+        codes = rng.integers(0, ncode, size=(4, HK, D), dtype=np.uint8)
+        x = (dec(codes) * s).astype(np.float32)
+        rows = W.quantize_rows(x, s, fmt)
+        assert rows.shape == (4, HK, rb) and W.row_bytes(D, fmt) == rb
+        assert np.array_equal(unpack(rows), codes)
+
+
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3, W.KV_E3M2, W.KV_E2M1])
 def test_written_rows_are_within_half_a_step(kv_format):
     rng = np.random.default_rng(14)
     x = (rng.standard_normal((64, HK, D)) * 3).astype(np.float32)
@@ -96,10 +110,12 @@ def test_written_rows_are_within_half_a_step(kv_format):
         dec = F.e4m3_decode(codes)
         top = 448.0
     else:
-        codes, vals = F.fp6_unpack_rows(rows), F.E2M3_TABLE[:0x20]
+        unpack, table, n, top = {W.KV_E2M3: (F.fp6_unpack_rows, F.E2M3_TABLE, 0x20, 7.5),
+                                 W.KV_E3M2: (F.fp6_unpack_rows, F.E3M2_TABLE, 0x20, 28.0),
+                                 W.KV_E2M1: (F.fp4_unpack_rows, F.E2M1_TABLE, 0x8, 6.0)}[kv_format]
+        codes, vals = unpack(rows), table[:n]
         y = x / ks.astype(np.float64)
-        dec = F.e2m3_decode(codes)
-        top = 7.5
+        dec = table[codes]
     a = np.minimum(np.abs(y), top)
     i = np.clip(np.searchsorted(vals, a, side="right") - 1, 0, len(vals) - 2)
     half_step = (vals[i + 1] - vals[i]) / 2
@@ -108,7 +124,7 @@ def test_written_rows_are_within_half_a_step(kv_format):
     assert np.all((np.signbit(dec) == np.signbit(y)) | (dec == 0))
 
 
-@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3, W.KV_E3M2, W.KV_E2M1])
 def test_token_order_does_not_matter(kv_format):
     rng = np.random.default_rng(15)
     T = 12
@@ -126,11 +142,11 @@ def test_token_order_does_not_matter(kv_format):
     assert np.array_equal(a_k, b_k) and np.array_equal(a_v, b_v)
 
 
-@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3])
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3, W.KV_E3M2, W.KV_E2M1])
 def test_head_size_256_row_is_two_128_channel_rows(kv_format):
     """A 256-channel row's bytes are the two 128-channel halves' bytes side by
-    side: one code per byte (e4m3), or a little-endian 6-bit stream whose
-    first 128 codes fill exactly 96 bytes (e2m3). The 128-channel encoding is
+    side: one code per byte (e4m3), or a little-endian 6-bit (4-bit) stream
+    whose first 128 codes fill exactly 96 (64) bytes. The 128-channel encoding is
     pinned by the hand-packed fixtures."""
     rng = np.random.default_rng(21)
     x = rng.standard_normal((5, HK, 256)).astype(np.float32) * 3

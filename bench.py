@@ -53,8 +53,19 @@ DEFAULT_KNOBS = {
     "spec_verify_noncausal": (4, 64, 4),
     "fp6_decode": (2, 64, 6),
     "d256_decode": (2, 64, 2),
+    "fp6_e3m2_decode": (2, 64, 6),
+    "fp4_decode": (2, 64, 6),
     "tiny": (2, 16, 0),
 }
+
+
+# largest value of each cache format (the channel scales are amax / max)
+FORMAT_MAX = {"fp8": 448.0, "e2m3": 7.5, "e3m2": 28.0, "e2m1": 6.0}
+
+
+def kv_row_bytes(w) -> int:
+    """Bytes of one (token, KV head) row of the workload's cache format."""
+    return {"fp8": w.d, "e2m3": w.d * 3 // 4, "e3m2": w.d * 3 // 4, "e2m1": w.d // 2}[w.kv_format]
 
 
 def _peaks():
@@ -160,7 +171,7 @@ def cpu_baseline_child(workload: str, budget_s: float, shard: str = "0/1"):
     import synth
 
     w = synth.WORKLOADS[workload]()
-    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    row = kv_row_bytes(w)
     si, sn = (int(v) for v in shard.split("/"))
     units = [(b, g) for b in range(w.num_seqs) for g in range(w.h_k) if w.seq_lens[b] > 0][si::sn]
     done, nbytes, t = 0, 0, 0.0
@@ -216,8 +227,8 @@ def measure_write_kv(w, dev, peak: float) -> dict:
 
     import paged_fp8_decode_gb300 as mj
 
-    fmt = mj.MJ_KV_E4M3 if w.kv_format == "fp8" else mj.MJ_KV_E2M3
-    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    fmt = mj.KV_FORMATS[w.kv_format]
+    row = kv_row_bytes(w)
     lib = mj.load_library()
     stream = torch.cuda.current_stream(dev)
     gen = torch.Generator(device=dev)
@@ -232,7 +243,7 @@ def measure_write_kv(w, dev, peak: float) -> dict:
         if fmt == mj.MJ_KV_E4M3:
             scales = (amax.amax(dim=2) / 448.0).contiguous()  # per KV head
         else:
-            scales = (amax / 7.5).contiguous()  # per (KV head, channel)
+            scales = (amax / FORMAT_MAX[w.kv_format]).contiguous()  # per (KV head, channel)
         strides = (w.h_k * w.page_size * row, row, w.page_size * row)  # HND
         a = mj.mj_write_kv_args()
         a.num_tokens, a.h_k, a.d = n_tok, w.h_k, w.d
@@ -351,7 +362,7 @@ def reference_arm(args):
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]()
-    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    row = kv_row_bytes(w)
     units = [(b, g) for b in range(w.num_seqs) for g in range(w.h_k) if w.seq_lens[b] > 0]
     for i in range(args.warmup):
         _oracle_unit_seconds(w, [units[i % len(units)]])
@@ -419,7 +430,7 @@ def main_ours(args):
     stream = torch.cuda.current_stream(dev)
     info = step.plan(w.seq_lens, w.num_seqs, stream)
     a = step.args(kv, out, w.num_seqs, w.softmax_scale, q=q)
-    row = w.d if w.kv_format == "fp8" else w.d * 3 // 4
+    row = kv_row_bytes(w)
     kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.h_k * 2 * row
     tokens = int((w.seq_lens > 0).sum()) * w.q_len
     launches_per_step = (1 if args.q_mode == "fp8" else 0) + 1 + (1 if info["with_reduction"] else 0)

@@ -1,5 +1,5 @@
 /*
- * mj.h — C ABI of libmj: paged decode attention over an e4m3 or packed e2m3
+ * mj.h — C ABI of libmj: paged decode attention over an e4m3 or packed e2m3 (e3m2, e2m1)
  * KV cache, for NVIDIA GB300 (sm_103a).
  *
  * One decode step is four calls, in the order the mjolnir-kernel README
@@ -25,8 +25,8 @@
  *    Device calls only enqueue work on it; argument errors are detected on
  *    the host before anything is enqueued.
  *  - Device pointers must be 16-byte aligned ("T5 kernel needs 16-byte
- *    aligned base pointers", _ptr on the mjolnir/runner.py page); packed e2m3
- *    K/V bases must be 32-byte aligned (T5DecodeRunner._kv_ptr).
+ *    aligned base pointers", _ptr on the mjolnir/runner.py page); packed
+ *    (e2m3, e3m2, e2m1) K/V bases must be 32-byte aligned (T5DecodeRunner._kv_ptr).
  *  - Q and O strides are in ELEMENTS; K/V strides are in BYTES, so e4m3 and
  *    packed e2m3 caches share one convention.
  *  - Launch shapes depend only on the arguments (the grid is the plan's
@@ -61,16 +61,23 @@ typedef enum mj_status {
   MJ_ERR_DEVICE_CHECK = -6  /* a kernel recorded an anomaly in the workspace status word */
 } mj_status;
 
+/* KV cache formats. The narrow ones (e2m3, e3m2, e2m1; OCP FP6 / FP4, no NaN)
+ * take per-(KV head, channel) scales folded into q_mul / o_mul, fp8 Q only,
+ * and 32-byte aligned cache bases. The package README lists e3m2 and e2m1
+ * beside e2m3 ("Beyond fp8: the harness"); their packing is this library's
+ * reading: e3m2 as e2m3, e2m1 two codes per byte, low nibble first. */
 typedef enum mj_kv_format {
   MJ_KV_E4M3 = 0,  /* one e4m3 code per byte; row = d bytes */
-  MJ_KV_E2M3 = 1   /* packed e2m3: 4 codes per 3 bytes, little-endian bitstream; row = d*3/4 bytes */
+  MJ_KV_E2M3 = 1,  /* packed e2m3: 4 codes per 3 bytes, little-endian bitstream; row = d*3/4 bytes */
+  MJ_KV_E3M2 = 2,  /* packed e3m2 (largest 28): as e2m3; row = d*3/4 bytes */
+  MJ_KV_E2M1 = 3   /* packed e2m1 (largest 6): code 2j in the low nibble of byte j; row = d/2 bytes */
 } mj_kv_format;
 
 /* How the decode call takes Q (T5DecodeRunner's q_mode):
  *   MJ_Q_FP8       — the e4m3 codes and per-(request, KV head) descales
  *                    mj_quantize_q wrote;
  *   MJ_Q_BF16      — the bf16 Q as is (e4m3 KV only, as on the runner page:
- *                    packed e2m3 is "fp8 Q only");
+ *                    packed e2m3 is "fp8 Q only"; the same for e3m2 / e2m1);
  *   MJ_Q_FP8_FUSED — the bf16 Q, quantized by the decode kernel itself with
  *                    mj_quantize_q's recipe (same codes, same descales), so
  *                    the step needs no separate quantize launch. */
@@ -144,7 +151,7 @@ MJ_API int mj_plan_split_kv(const int32_t* seq_lens_host, int num_seqs, int q_le
  *
  * q          device bf16, element (b*q_len + t, h, c) at
  *            q[(b*q_len+t)*q_tok_stride + h*q_head_stride + c]; channel stride 1.
- * q_mul      nullable device float32 [h_q][d] (e2m3 KV: K channel scales).
+ * q_mul      nullable device float32 [h_q][d] (packed KV: K channel scales).
  * q_codes    device uint8 [num_seqs][h_k][q_len*h_r][d], row t*h_r + r
  *            (h_r = h_q/h_k), written.
  * q_descale  device float32 [num_seqs][h_k], written.
@@ -168,7 +175,7 @@ typedef struct mj_decode_args {
   int num_seqs;   /* requests in the batch (real + trailing padding) */
   int q_len;      /* query tokens per request (1 = decode; 1+k = speculative verify) */
   int h_q, h_k;   /* query heads, KV heads; h_q % h_k == 0 */
-  int d;          /* head size: 128 or 256 (packed e2m3 at 256: CUDA-core kernel only) */
+  int d;          /* head size: 128 or 256 (packed formats at 256: CUDA-core kernel only) */
   int causal;     /* 1: query t sees key j iff j <= seq_len - q_len + t;
                      0: every query token sees every key (README "What it does") */
   float softmax_scale;
@@ -187,7 +194,7 @@ typedef struct mj_decode_args {
   int64_t v_stride_page, v_stride_token, v_stride_head;  /* bytes, multiples of 16 */
   /* K/V descales, float32; element (b, g) at ptr[b*seq_stride + g*head_stride]:
      (0,0) per tensor, (0,1) per KV head, (h_k,1) per (request, KV head).
-     Packed e2m3 KV: the channel scales are folded into q_mul / o_mul and
+     Packed (e2m3, e3m2, e2m1) KV: the channel scales are folded into q_mul / o_mul and
      these are 1 (_install_fp6_scales, mjolnir/backend.py page). */
   const float* k_descale;
   const float* v_descale;
@@ -328,9 +335,10 @@ MJ_API int mj_decode_attention_noalloc(const mj_decode_args* args, void* stream)
  *   e4m3: code[c] = e4m3(x[c] / scale)      scale = k_scale[0] (per tensor)
  *                                           or k_scale[g] (scale_per_head)
  *   e2m3: code[c] = e2m3(x[c] / k_scale[g*d + c]), packed 4 codes per 3 bytes
+ *   e3m2, e2m1: likewise with their own code and packing (mj_kv_format)
  * x is the bf16 input widened to float32; the division is IEEE float32 and
  * the rounding to the cache format is to nearest, ties to even, saturating
- * (448 / 7.5). Likewise for V with v_scale. A negative slot marks a padding
+ * (448 / 7.5 / 28 / 6). Likewise for V with v_scale. A negative slot marks a padding
  * token: nothing is written for it. A slot at or past num_pages*page_size is
  * skipped and, if status != NULL, bit 1 of *status is set.
  *
@@ -356,7 +364,7 @@ typedef struct mj_write_kv_args {
   int64_t k_stride_page, k_stride_token, k_stride_head;  /* bytes */
   int64_t v_stride_page, v_stride_token, v_stride_head;  /* bytes */
 
-  const float* k_scale;       /* device float32: e4m3 [1] or [h_k]; e2m3 [h_k][d] */
+  const float* k_scale;       /* device float32: e4m3 [1] or [h_k]; packed formats [h_k][d] */
   const float* v_scale;
   int scale_per_head;         /* e4m3 only: 1 = one scale per KV head, 0 = per tensor */
 

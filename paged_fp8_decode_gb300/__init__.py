@@ -1,6 +1,6 @@
 """paged_fp8_decode_gb300 — Python binding of libmj (include/mj.h).
 
-Paged decode attention over an e4m3 or packed e2m3 KV cache on GB300
+Paged decode attention over an e4m3 or packed e2m3 / e3m2 / e2m1 KV cache on GB300
 (sm_103a). Every step of the path runs in the CUDA library; this module only
 marshals arguments: torch tensors become device pointers and strides, torch
 streams become ``cudaStream_t`` handles. The function names are the C names.
@@ -28,7 +28,9 @@ MJ_ERR_DEVICE_CHECK = -6
 
 MJ_KV_E4M3 = 0
 MJ_KV_E2M3 = 1
-KV_FORMATS = {"fp8": MJ_KV_E4M3, "e2m3": MJ_KV_E2M3}
+MJ_KV_E3M2 = 2
+MJ_KV_E2M1 = 3
+KV_FORMATS = {"fp8": MJ_KV_E4M3, "e2m3": MJ_KV_E2M3, "e3m2": MJ_KV_E3M2, "e2m1": MJ_KV_E2M1}
 
 MJ_Q_FP8 = 0
 MJ_Q_BF16 = 1
@@ -257,7 +259,7 @@ def mj_write_kv(key, value, slot_mapping, k_cache, v_cache, kv_strides, page_siz
     stride 1). ``slot_mapping``: int64 ``[T]`` (negative = padding).
     ``k_cache`` / ``v_cache``: uint8 pools; ``kv_strides``: byte strides
     ``(page, token, head)`` shared by both. ``k_scale`` / ``v_scale``:
-    float32 -- e4m3 ``[1]`` or ``[h_k]`` (``scale_per_head``), e2m3
+    float32 -- e4m3 ``[1]`` or ``[h_k]`` (``scale_per_head``), the packed formats
     ``[h_k, d]``. ``status``: optional int32/uint32 device word."""
     assert key.stride(2) == 1 and value.stride(2) == 1
     a = mj_write_kv_args()

@@ -11,7 +11,8 @@
 // into the result.
 //
 // This is the generic path: any row tile up to 32 (16 with D = 256), any
-// strides, e4m3 or packed e2m3, D = 128 or 256, e4m3 Q codes or bf16 Q as is.
+// strides, e4m3 or packed e2m3 / e3m2 / e2m1, D = 128 or 256, e4m3 Q codes or
+// bf16 Q as is.
 // The tensor-core kernel is the fast path.
 #include <cuda_fp8.h>
 
@@ -25,8 +26,16 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 
+// Four 6-bit (e2m3 / e3m2) or 4-bit (e2m1) codes, one per byte, widened to
+// e4m3 codes (value / kv_widen_factor).
+__device__ __forceinline__ uint32_t widen4_codes(uint32_t four_codes, int kv_format) {
+  if (kv_format == MJ_KV_E2M3) return e2m3x4_to_e4m3x4(four_codes);
+  if (kv_format == MJ_KV_E3M2) return e3m2x4_to_e4m3x4(four_codes);
+  return e2m1x4_to_e4m3x4(four_codes);
+}
+
 // Codes 16*i .. 16*i+15 of one K row as floats (e4m3: bytes 16i..16i+15;
-// e2m3: packed bytes 12i..12i+11 widened to e4m3, value x 2^-6).
+// e2m3 / e3m2: packed bytes 12i..12i+11, e2m1: bytes 8i..8i+7, widened to e4m3).
 __device__ __forceinline__ void load_k16(const uint8_t* row, int kv_format, int i, float k[16]) {
   if (kv_format == MJ_KV_E4M3) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + i);
@@ -34,6 +43,12 @@ __device__ __forceinline__ void load_k16(const uint8_t* row, int kv_format, int 
     e4m3x4_to_float(v.y, k + 4);
     e4m3x4_to_float(v.z, k + 8);
     e4m3x4_to_float(v.w, k + 12);
+  } else if (kv_format == MJ_KV_E2M1) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(row) + i);
+    e4m3x4_to_float(e2m1x4_to_e4m3x4(spread4x4(v.x & 0xFFFFu)), k + 0);
+    e4m3x4_to_float(e2m1x4_to_e4m3x4(spread4x4(v.x >> 16)), k + 4);
+    e4m3x4_to_float(e2m1x4_to_e4m3x4(spread4x4(v.y & 0xFFFFu)), k + 8);
+    e4m3x4_to_float(e2m1x4_to_e4m3x4(spread4x4(v.y >> 16)), k + 12);
   } else {
     const uint32_t* r32 = reinterpret_cast<const uint32_t*>(row) + 3 * i;
     const uint32_t w0 = __ldg(r32), w1 = __ldg(r32 + 1), w2 = __ldg(r32 + 2);
@@ -41,10 +56,10 @@ __device__ __forceinline__ void load_k16(const uint8_t* row, int kv_format, int 
     const uint32_t g1 = __funnelshift_r(w0, w1, 24) & 0xFFFFFFu;
     const uint32_t g2 = __funnelshift_r(w1, w2, 16) & 0xFFFFFFu;
     const uint32_t g3 = w2 >> 8;
-    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g0)), k + 0);
-    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g1)), k + 4);
-    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g2)), k + 8);
-    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g3)), k + 12);
+    e4m3x4_to_float(widen4_codes(spread6x4(g0), kv_format), k + 0);
+    e4m3x4_to_float(widen4_codes(spread6x4(g1), kv_format), k + 4);
+    e4m3x4_to_float(widen4_codes(spread6x4(g2), kv_format), k + 8);
+    e4m3x4_to_float(widen4_codes(spread6x4(g3), kv_format), k + 12);
   }
 }
 
@@ -52,10 +67,13 @@ __device__ __forceinline__ void load_k16(const uint8_t* row, int kv_format, int 
 __device__ __forceinline__ void load_v4(const uint8_t* row, int kv_format, int j, float v[4]) {
   if (kv_format == MJ_KV_E4M3) {
     e4m3x4_to_float(__ldg(reinterpret_cast<const uint32_t*>(row) + j), v);
+  } else if (kv_format == MJ_KV_E2M1) {
+    const uint32_t h = __ldg(reinterpret_cast<const uint16_t*>(row) + j);
+    e4m3x4_to_float(e2m1x4_to_e4m3x4(spread4x4(h)), v);
   } else {
     const uint8_t* p = row + 3 * j;
     const uint32_t g = uint32_t(__ldg(p)) | (uint32_t(__ldg(p + 1)) << 8) | (uint32_t(__ldg(p + 2)) << 16);
-    e4m3x4_to_float(e2m3x4_to_e4m3x4(spread6x4(g)), v);
+    e4m3x4_to_float(widen4_codes(spread6x4(g), kv_format), v);
   }
 }
 

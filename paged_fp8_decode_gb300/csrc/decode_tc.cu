@@ -1,897 +1,11 @@
-// Tensor-core variant of mj_decode_attention for sm_103a: TMA page streaming
-// into a shared-memory ring, tcgen05.mma (kind f8f6f4, e4m3 x e4m3 -> f32) with
-// accumulators in tensor memory, online softmax on CUDA cores.
-//
-// The README of the mjolnir-kernel package ("A decode step", item 3) describes
-// the shape of this design for Jetson Thor: TMA page loads into a ring with an
-// L2 evict-first hint, tcgen05 MMAs accumulating S and O in TMEM, softmax
-// warpgroups. This kernel is written for GB300 from that description:
-//
-// * One CTA per (work row, KV head, query-row tile); 7 warps (10 with packed
-//   e2m3 KV):
-//     warps 0, 6 TMA producers of the K and the V tiles: block-table lookups
-//                (32 entries per warp load), one 4-D tensor-map load per
-//                (page, head, 128-channel sub-tile) into the ring;
-//     warp 1     TMEM allocation and the single-thread MMA issuer;
-//     warps 2-5  softmax warpgroup: thread x owns TMEM lane x, i.e. key x of a
-//                128-key tile for S and channel x (of each 128-channel half)
-//                for O;
-//     warps 7-9  packed e2m3 KV only: widen each landed V tile to e4m3.
-// * The ring alternates K and V tiles of 128 keys x D bytes (D / 128 sub-tiles
-//   of 128 keys x 128 bytes), 128-byte swizzled by the TMA so that
-//   tcgen05.mma reads them directly.
-// * Both products are issued "keys as M" so that M = 128 fills the tensor
-//   core even for a handful of query rows:
-//     S^T[key][row] = K[key][:] . Q[row][:]       A = K tile (K-major), B = Q tile
-//     O^T[d][col]  += V^T[d][key] . P^T[key][col] A = V tile (MN-major), B = P tile
-// * P is written as two e4m3 terms, hi = e4m3(p) and lo = e4m3(p - hi), in
-//   separate columns of the same PV product (the query rows leave spare N
-//   columns anyway): O gets P to ~2^-8 relative precision at no extra MMA.
-//   P is scaled by 2^8 (p = 2^(t - m + 8) <= 256) so that its e4m3 terms stay
-//   normal well into the tail of the softmax; the factor cancels in O / l.
-// * Keys at or past the device seq_len are masked by select on S; in a
-//   request's last, partial tile the V producer warp also zeroes the V rows
-//   past the end before the PV product (page tails may hold NaN codes, and
-//   0 * NaN would reach O through the MMA).
-// * Every wait is bounded (2 s); a timeout raises a status bit and the CTA
-//   unwinds, frees its TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <climits>
-#include <cstddef>
-#include <mutex>
-#include <type_traits>
-
-#include "mj_device.cuh"
-#include "mj_internal.h"
-#include "tc_ptx.cuh"
+// Host side of the tcgen05 decode path: its envelope (tc_supported), the
+// 4-D tensor maps of the K and V caches, and the dispatch to the per-variant
+// launchers (decode_tc_*.cu). The kernel is in decode_tc_kernel.cuh.
+#include "decode_tc_kernel.cuh"
 
 namespace mj {
 
 namespace {
-
-constexpr int kThreadsTc = 224;      // e4m3 KV: 7 warps
-// packed e2m3 KV: + 3 V-widening warps (7-9). With warps 2-5 on the four SM
-// sub-partitions, the widening work then spreads over three of them rather
-// than two (two CTAs per SM keep at most five warps per sub-partition either
-// way, so the register budget is the same).
-constexpr int kThreadsTcFp6 = 320;
-constexpr int kConvThreads = kThreadsTcFp6 - 7 * 32;
-constexpr int kConvWarp0 = 7;
-constexpr int kSoftmaxWarp0 = 2;     // warps 2-5: softmax warpgroup
-constexpr int kVProducerWarp = 6;
-constexpr int kTileBytes = kKvTile * 128;  // 128 keys x 128 bytes
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
-struct TcSmem {
-  // offsets (bytes) from the 1024-aligned dynamic shared-memory base
-  uint32_t ring, q, p0, p1, ctrl, total;
-};
-
-// Shared-memory bytes of one 128-channel sub-tile of the Q tile (nqk rows).
-__host__ __device__ constexpr uint32_t q_sub_bytes(int nqk) { return uint32_t((nqk * 128 + 1023) / 1024) * 1024u; }
-
-// nsb: S / P buffers in flight (P buffer j at p0 + j * (p1 - p0)); dh: 128-channel
-// sub-tiles per row (D / 128): a ring entry holds dh 16 KB sub-tiles, the Q
-// tile dh sub-tiles of q_sub_bytes(nqk).
-__host__ __device__ inline TcSmem tc_smem_layout(int stages, int nqk, int npv, int nsb, int dh) {
-  TcSmem s;
-  s.ring = 0;
-  s.q = stages * dh * kTileBytes;
-  s.p0 = s.q + dh * q_sub_bytes(nqk);
-  s.p1 = s.p0 + ((npv * 128 + 1023) / 1024) * 1024;
-  s.ctrl = s.p0 + nsb * (s.p1 - s.p0);
-  s.total = s.ctrl + 3072;
-  return s;
-}
-
-// control block inside the ctrl region
-struct Ctrl {
-  uint64_t full[16];
-  uint64_t empty[16];
-  uint64_t s_full[4];
-  uint64_t p_full[4];
-  uint64_t o_full[4];
-  uint64_t red_bar[2];  // the 4 softmax warps have posted their row maxima
-  uint64_t sum_bar;     // ... their row sums
-  uint64_t drain;       // MMA drain after an abort
-  uint64_t q_ready;     // the softmax warps have written the Q tile
-  uint64_t vconv[16];   // e2m3 KV: V tile of ring slot s widened to e4m3
-  uint64_t v_tail;      // e4m3 KV: the last, partial V tile has its rows past the end zeroed
-  uint32_t tmem_base;
-  int abort;
-  alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
-  alignas(16) float lsum[4][32];    // row sums of the 4 softmax warps
-  float alpha[4][32];               // per softmax warp: the rescale factors of the current tiles
-  float qamax[2][4];                // bf16 Q: per softmax warp, |x| max and |residual| max
-};
-static_assert(sizeof(Ctrl) <= 3072, "control block");
-static_assert(offsetof(Ctrl, red) % 16 == 0 && offsetof(Ctrl, lsum) % 16 == 0, "float4 access to red/lsum");
-
-// Reduce NR per-lane values over the 32 lanes of a warp, one row per lane
-// group: a reduce-scatter (each step halves the rows a lane keeps and
-// exchanges the other half) followed by a butterfly over the lanes that share
-// a row. Row r ends up in lanes r*(32/NR) .. r*(32/NR) + 32/NR - 1. This takes
-// NR - 1 + log2(32/NR) shuffles instead of 5*NR for independent butterflies.
-template <int NR, bool MAX>
-__device__ __forceinline__ float rs_reduce(float (&v)[NR], int lane) {
-#pragma unroll
-  for (int c = NR, m = 16; c > 1; c >>= 1, m >>= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int j = 0; j < c / 2; ++j) {
-      const float send = upper ? v[j] : v[c / 2 + j];
-      const float keep = upper ? v[c / 2 + j] : v[j];
-      const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
-      v[j] = MAX ? fmaxf(keep, recv) : keep + recv;
-    }
-  }
-  float r = v[0];
-#pragma unroll
-  for (int m = 16 / NR; m > 0; m >>= 1) {
-    const float o = __shfl_xor_sync(0xFFFFFFFFu, r, m);
-    r = MAX ? fmaxf(r, o) : r + o;
-  }
-  return r;
-}
-
-__device__ __forceinline__ uint32_t p_byte_offset(int n, int key) {
-  // P^T tile: row n (a B-matrix column), 128 keys, K-major, 128-byte swizzle
-  return uint32_t(n) * 128u + ((uint32_t((key >> 4) ^ (n & 7))) << 4) + uint32_t(key & 15);
-}
-
-// Widen the 16 packed e2m3 codes of a 16-byte shared-memory chunk (12 bytes of
-// little-endian bitstream, 4 bytes of padding, as TMA's 16U6_ALIGN16B type
-// stores them) to 16 e4m3 codes worth 2^-6 times the e2m3 values: per code,
-// the 5 magnitude bits keep their place and the sign moves from bit 5 to bit 7
-// (an e2m3 code read as e4m3 with a zero-extended exponent is exactly 2^-6
-// times its value, subnormals included). Every resulting code is finite.
-__device__ __forceinline__ uint32_t widen4(uint32_t g) {
-  // code k of g sits at bits [6k, 6k + 6): magnitude -> byte k bits 0-4, sign -> bit 7
-  return (g & 0x1Fu) | ((g << 2) & 0x1F80u) | ((g << 4) & 0x1F8000u) | ((g << 6) & 0x1F800000u) |
-         ((g << 8) & 0x80000000u);
-}
-
-__device__ __forceinline__ uint4 widen_chunk(uint4 in) {
-  uint4 o;
-  o.x = widen4(in.x);
-  o.y = widen4(__funnelshift_r(in.x, in.y, 24));
-  o.z = widen4(__funnelshift_r(in.y, in.z, 16));
-  o.w = widen4(in.z >> 8);
-  return o;
-}
-
-// QM, how Q arrives (mj_q_mode): 0 e4m3 codes from mj_quantize_q; 1 bf16 Q
-// as is, represented as two e4m3 terms per value; 2 bf16 Q quantized here
-// with mj_quantize_q's recipe (see the Q staging in the softmax warps).
-// D, the head size (128 or 256): a K or V row of D channels is DH = D / 128
-// sub-tiles of 128 bytes; QK accumulates over the sub-tiles and PV runs once
-// per sub-tile into its own O accumulator (channel 128 * dh + lane).
-template <int NQK, int NPV, int NR, bool FP6, int QM = 0, int D = 128>
-__global__ void __launch_bounds__(FP6 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 2 : 1))
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                     DecodeParams p) {
-  constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
-  constexpr int DH = D / 128;
-  constexpr uint32_t kEntry = DH * kTileBytes;  // one ring entry: a K or V tile
-  constexpr uint32_t kQSub = q_sub_bytes(NQK);
-  static_assert(NH <= NQK && NR <= NH && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
-  static_assert(QM != 1 || (!FP6 && 2 * NR <= NQK), "bf16 Q: e4m3 KV, hi and lo rows in the Q tile");
-  static_assert((D == 128 || D == 256) && (!FP6 || D == 128), "head size (packed e2m3: 128)");
-  // TP tiles per softmax iteration; NSB S and P buffers let QK run up to
-  // NSB - 1 tiles ahead of PV.
-  constexpr int TP = NR <= 8 ? 2 : 1;
-  constexpr int NSB = 2 * TP;
-  // TMEM: NSB S buffers (NQK columns each), DH O accumulators (NPV columns each)
-  constexpr int kCols = NSB * NQK + DH * NPV;
-  static_assert(kCols <= 256, "TMEM columns");
-  constexpr uint32_t kTmemCols = kCols <= 64 ? 64 : (kCols <= 128 ? 128 : 256);
-
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-  // CTA x = (work row, KV head) with the head fastest: the CTAs that run
-  // together stream the same requests' pages (with token-major layouts the
-  // heads of a page interleave, so they share DRAM rows)
-  const int g = int(blockIdx.x % unsigned(p.h_k));
-  const int4 w = reinterpret_cast<const int4*>(p.work)[blockIdx.x / unsigned(p.h_k)];
-  const int b = w.x;
-  if (w.z <= w.y || b < 0 || b >= p.num_seqs) return;
-  if (p.with_reduction && (w.w < 0 || w.w >= p.max_splits || b >= p.part_seqs)) {
-    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPlan);
-    return;
-  }
-  const int L = p.seq_lens[b];
-  if (L <= 0) return;
-  const int64_t k0 = int64_t(w.y) * kKvTile;
-  const int64_t k1 = min(int64_t(w.z) * kKvTile, int64_t(L));
-  if (k1 <= k0) return;
-  const int r0 = blockIdx.y * p.tw;
-  const int nr = min(min(p.tw, p.n_q - r0), NR);
-  if (nr <= 0) return;
-  const int ntiles = int((k1 - k0 + kKvTile - 1) / kKvTile);
-  // the last tile ends before k0 + ntiles * 128: its V rows past the end get zeroed
-  const bool last_partial = k0 + int64_t(ntiles) * kKvTile > k1;
-  const int stages = p.kv_stages;
-
-  const TcSmem lay = tc_smem_layout(stages, NQK, NPV, NSB, DH);
-  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + lay.ctrl);
-  const uint32_t ring_addr = tc::smem_u32(smem + lay.ring);
-  const uint32_t q_addr = tc::smem_u32(smem + lay.q);
-  const uint32_t p_stride = lay.p1 - lay.p0;  // P buffer j at p0 + j * p_stride
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- set-up: barriers, TMEM, Q tile ------------------------------------
-  if (tid == 0) {
-    for (int s = 0; s < stages; ++s) {
-      tc::mbar_init(tc::smem_u32(&ctl.full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&ctl.empty[s]), 1);
-    }
-    for (int s = 0; s < NSB; ++s) {
-      tc::mbar_init(tc::smem_u32(&ctl.s_full[s]), 1);
-      tc::mbar_init(tc::smem_u32(&ctl.p_full[s]), 128);
-      tc::mbar_init(tc::smem_u32(&ctl.o_full[s]), 1);
-    }
-    for (int s = 0; s < 2; ++s) tc::mbar_init(tc::smem_u32(&ctl.red_bar[s]), 4);
-    tc::mbar_init(tc::smem_u32(&ctl.sum_bar), 4);
-    tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
-    tc::mbar_init(tc::smem_u32(&ctl.q_ready), 128);
-    tc::mbar_init(tc::smem_u32(&ctl.v_tail), 1);
-    if (FP6)
-      for (int s = 0; s < stages; ++s) tc::mbar_init(tc::smem_u32(&ctl.vconv[s]), kConvThreads);
-    ctl.abort = 0;
-    tc::fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tc::prefetch_tmap(&tmap_k);
-    tc::prefetch_tmap(&tmap_v);
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = ctl.tmem_base;
-  volatile int* abort = &ctl.abort;
-
-  // TMEM columns: S buffer j % NSB at [(j % NSB) NQK, ...), the O accumulators
-  // after them (sub-tile dh at tO + dh * NPV)
-  auto tS = [&](int j) { return tmem + uint32_t((j % NSB) * NQK); };
-  const uint32_t tO = tmem + uint32_t(NSB * NQK);
-  // barrier slot and phase parity of tile j's S / P / O events
-  auto bs = [&](int j) { return j % NSB; };
-  auto bp = [&](int j) { return uint32_t(j / NSB) & 1u; };
-
-  if (warp == 0 || warp == kVProducerWarp) {
-    // ======================= TMA producers ==================================
-    // warp 0 loads the K tiles (ring entries u = 2i), warp kVProducerWarp the
-    // V tiles (u = 2i + 1), concurrently: a CTA's TMA issue rate, not HBM,
-    // bounds small-page streaming, and two issuing warps double it.
-    const int half = warp == 0 ? 0 : 1;
-    const CUtensorMap* map = half ? &tmap_v : &tmap_k;
-    const uint64_t pol = p.evict_first ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
-    const int ps = p.page_size;
-    const int ppt = kKvTile / ps;
-    const int64_t first_page = k0 / ps;
-    const int64_t npages = (k1 + ps - 1) / ps - first_page;
-    const int32_t* bt = p.block_table + int64_t(b) * p.bt_stride + first_page;
-    const uint32_t page_bytes = uint32_t(ps) * 128u;                 // shared-memory footprint
-    const uint32_t page_tx = uint32_t(ps) * uint32_t(p.row_bytes);  // bytes the copy delivers
-    int64_t batch = -1;
-    int entry = -1;
-    bool ok = true;
-    int issued = 0;  // tiles whose load this warp issued
-    for (int i = 0; i < ntiles && ok; ++i) {
-      // lane j < nvalid issues the load of page j of tile i (one page id per lane)
-      const int nvalid = int(min(int64_t(ppt), npages - int64_t(i) * ppt));
-      const int64_t e0 = int64_t(i) * ppt;
-      if (batch < 0 || e0 + nvalid > batch + 32) {
-        batch = e0;
-        entry = (e0 + lane < npages) ? bt[e0 + lane] : -1;
-      }
-      const int pg = __shfl_sync(0xFFFFFFFFu, entry, int(e0 - batch) + (lane & 7));
-      if (half == 0 && lane < nvalid && (pg < 0 || int64_t(pg) >= p.num_pages)) atomicOr(p.status, kStatusBadPage);
-      const int u = 2 * i + half;
-      const int slot = u % stages;
-      const uint32_t round = uint32_t(u / stages);
-      const uint32_t full = tc::smem_u32(&ctl.full[slot]);
-      if (lane == 0) {
-        ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
-        if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_tx);
-      }
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-      if (ok && lane < nvalid) {
-        // sub-tile dh: channels 128 dh .. 128 dh + 127 (x = 128 dh bytes, 16-byte aligned)
-#pragma unroll
-        for (int dh = 0; dh < DH; ++dh) {
-          const uint32_t dst = ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes + uint32_t(lane) * page_bytes;
-          if (p.tma_head_inner)
-            tc::tma_load_4d(dst, map, full, 128 * dh, g, 0, pg, pol);
-          else
-            tc::tma_load_4d(dst, map, full, 128 * dh, 0, g, pg, pol);
-        }
-      }
-      if (ok) ++issued;
-      __syncwarp();
-    }
-    if (!FP6 && half == 1 && ok && last_partial) {
-      // Last, partial V tile: zero its rows past the end (page tails and
-      // stale ring contents may hold NaN codes, and 0 * NaN would reach O
-      // through the PV product), then release it to the MMA issuer. This warp
-      // may wait on the slot's full barrier: its own wait on the slot's empty
-      // barrier showed that the previous occupant has landed and been consumed.
-      const int u = 2 * (ntiles - 1) + 1;
-      const int slot = u % stages;
-      if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-      if (ok) {
-        const int first_dead = int(k1 - (k0 + int64_t(ntiles - 1) * kKvTile));  // rows >= this are past the end
-#pragma unroll
-        for (int dh = 0; dh < DH; ++dh) {
-          uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry + dh * kTileBytes);
-          for (int c = first_dead * 8 + lane; c < kKvTile * 8; c += 32) tile[c] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        tc::fence_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.v_tail));
-      }
-    }
-    if (!ok && lane == 0) {
-      // abort: wait (bounded) for this warp's loads still in flight before the CTA exits
-      const uint64_t t0 = tc::globaltimer_ns();
-      for (int i = max(0, issued - stages); i < issued; ++i) {
-        const int u = 2 * i + half;
-        while (!tc::mbar_try_wait(tc::smem_u32(&ctl.full[u % stages]), uint32_t(u / stages) & 1u) &&
-               tc::globaltimer_ns() - t0 < 100000000ull) {
-        }
-      }
-    }
-  } else if (FP6 && warp >= kConvWarp0) {
-    // ======================= V widening (e2m3 KV) ============================
-    // Each V tile is widened in place, chunk by chunk, once its load lands.
-    const int ct = tid - kConvWarp0 * 32;  // 0 .. kConvThreads - 1
-    bool ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      const int u = 2 * i + 1;
-      const int slot = u % stages;
-      ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
-      if (!ok) break;
-      uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry);
-#pragma unroll 4
-      for (int k = ct; k < kTileBytes / 16; k += kConvThreads) tile[k] = widen_chunk(tile[k]);
-      tc::fence_async_smem();
-      tc::mbar_arrive(tc::smem_u32(&ctl.vconv[slot]));
-    }
-  } else if (warp == 1) {
-    // ======================= MMA issuer ======================================
-    if (lane == 0) {
-      // K is read as e2m3 straight from the packed TMA layout (kind::f8f6f4
-      // mixes an e2m3 A with the e4m3 Q); V always arrives as e4m3.
-      constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false) | (FP6 ? (3u << 7) : 0u);
-      // PV: A = V tile (MN-major), B = P (MN-major, no swizzle: [key][16 columns] blocks)
-      constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, true);
-      const uint64_t qdesc = tc::smem_desc(q_addr, 16, 1024, tc::kSwizzle128B);
-      // Event loop: issue QK_nq as soon as K tile nq has landed (at most one
-      // tile ahead of PV: two S buffers), and PV_np as soon as P_np is
-      // written and V tile np has landed. Neither product waits behind the
-      // other's operands.
-      bool ok = tc::mbar_wait(tc::smem_u32(&ctl.q_ready), 0, abort, kWaitLimitNs);
-      int nq = 0, np = 0;
-      uint64_t t_idle = 0;
-      while (ok && np < ntiles) {
-        bool progressed = false;
-        if (nq < ntiles && nq <= np + NSB - 1) {
-          const int u = 2 * nq;
-          const int slot = u % stages;
-          if (tc::mbar_test_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u)) {
-            tc::tc_fence_after();
-#pragma unroll
-            for (int dh = 0; dh < DH; ++dh) {
-              const uint64_t kdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes, 16,
-                                                   1024, tc::kSwizzle128B);
-              const uint64_t qd = qdesc + uint64_t((uint32_t(dh) * kQSub) >> 4);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)  // 128 channels of the sub-tile in steps of 32 bytes
-                tc::umma_f8f6f4(tS(nq), kdesc + uint64_t(2 * k), qd + uint64_t(2 * k), idesc_qk, dh > 0 || k > 0);
-            }
-            tc::umma_commit(tc::smem_u32(&ctl.s_full[bs(nq)]));
-            tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
-            ++nq;
-            progressed = true;
-          }
-        }
-        if (np < nq) {
-          const int u = 2 * np + 1;
-          const int slot = u % stages;
-          // V tile ready: widened (e2m3), tail-zeroed (last partial e4m3 tile, a
-          // one-shot barrier), else landed
-          const bool tail = !FP6 && last_partial && np == ntiles - 1;
-          const uint32_t vbar = tc::smem_u32(FP6 ? &ctl.vconv[slot] : (tail ? &ctl.v_tail : &ctl.full[slot]));
-          const uint32_t vpar = tail ? 0u : uint32_t(u / stages) & 1u;
-          if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[bs(np)]), bp(np)) && tc::mbar_test_wait(vbar, vpar)) {
-            tc::tc_fence_after();
-            // P, MN-major without swizzle: 8-key core groups 128 B apart (LBO),
-            // 16-column blocks 2 KB apart (SBO)
-            const uint64_t pdesc =
-                tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(bs(np)) * p_stride, 128, 2048, 0);
-#pragma unroll
-            for (int dh = 0; dh < DH; ++dh) {
-              const uint64_t vdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes,
-                                                   kTileBytes, 1024, tc::kSwizzle128B);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V, 32 x 16 B of P)
-                tc::umma_f8f6f4(tO + uint32_t(dh * NPV), vdesc + uint64_t(256 * k), pdesc + uint64_t(32 * k), idesc_pv,
-                                (np > 0 || k > 0));
-            }
-            tc::umma_commit(tc::smem_u32(&ctl.o_full[bs(np)]));
-            tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
-            ++np;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_idle = 0;
-        } else {
-          const uint64_t now = tc::globaltimer_ns();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > kWaitLimitNs || *abort) {
-            *abort = 1;
-            ok = false;
-            break;
-          }
-        }
-      }
-      if (!ok) {
-        // abort: wait (bounded) until every MMA issued so far has completed
-        tc::umma_commit(tc::smem_u32(&ctl.drain));
-        const uint64_t t0 = tc::globaltimer_ns();
-        while (!tc::mbar_try_wait(tc::smem_u32(&ctl.drain), 0) && tc::globaltimer_ns() - t0 < 100000000ull) {
-        }
-      }
-    }
-  } else {
-    // ======================= softmax warpgroup ===============================
-    // Q codes and descales come from the preceding grid (mj_quantize_q) when
-    // it is launched just before: wait for it here only, so that the TMA
-    // producers stream KV meanwhile.
-    tc::grid_dependency_wait();
-    const int xq = tid - kSoftmaxWarp0 * 32;
-    float sc_hi = 0.f, sc_lo = 0.f;  // bf16 Q: logit scales of its hi and lo terms
-    float sq = 1.f;                  // Q quantized here: its descale
-    // max over the 128 softmax threads (the four softmax warps always reach this barrier)
-    auto block_max = [&](float v, int slot) {
-      v = warp_max(v);
-      if (lane == 0) ctl.qamax[slot][warp & 3] = v;
-      tc::named_bar_sync(1, 128);
-      return fmaxf(fmaxf(ctl.qamax[slot][0], ctl.qamax[slot][1]), fmaxf(ctl.qamax[slot][2], ctl.qamax[slot][3]));
-    };
-    // Q tile: DH sub-tiles (channels 128 dh ..) of [NQK rows][128 B], K-major,
-    // 128-byte swizzle: byte c of row r in sub-tile c >> 7, 16-byte chunk
-    // ((c & 127) >> 4) ^ (r & 7)
-    auto q_off = [&](int r, int c) {
-      return lay.q + uint32_t(c >> 7) * kQSub + uint32_t(r * 128 + ((((c & 127) >> 4) ^ (r & 7)) << 4) + (c & 15));
-    };
-    // zero rows r_from .. NQK-1 of every sub-tile
-    auto zero_rows = [&](int r_from) {
-      for (int i = xq; i < (NQK - r_from) * 8 * DH; i += 128) {
-        const int dh = i / ((NQK - r_from) * 8), j = i % ((NQK - r_from) * 8);
-        *reinterpret_cast<uint4*>(smem + lay.q + dh * kQSub + r_from * 128 + j * 16) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
-    if constexpr (QM == 0) {
-      // Q codes rows r0 .. r0+nr-1 into the Q tile; other rows 0
-      const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * D;
-      for (int i = xq; i < NQK * 8 * DH; i += 128) {
-        const int r = i / (8 * DH), c = (i % (8 * DH)) * 16;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * D + c);
-        *reinterpret_cast<uint4*>(smem + q_off(r, c)) = v;
-      }
-    } else if constexpr (QM == 2) {
-      // mj_quantize_q's recipe, in the kernel: x = bf16 Q (times q_mul), the
-      // scale from the amax over all q_len*h_r rows of (b, g), then e4m3
-      // round-to-nearest-even satfinite, every step an IEEE float32 operation,
-      // so the codes and the descale are the ones that call writes. Thread xq
-      // takes channels xq + 128 dh of every row.
-      auto q_in = [&](int rr, int c) {
-        const int tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
-        float v = bf16_bits_to_float(p.q_bf16[int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c]);
-        if (p.q_mul) v = __fmul_rn(v, p.q_mul[int64_t(h) * D + c]);
-        return v;
-      };
-      // the tile's rows once, into registers (independent loads); the rows of
-      // (b, g) outside the tile only count towards the amax
-      float xr[DH][NR];
-      float am = 0.f;
-#pragma unroll
-      for (int dh = 0; dh < DH; ++dh) {
-        const int c = xq + 128 * dh;
-#pragma unroll
-        for (int r = 0; r < NR; ++r) xr[dh][r] = r < nr ? q_in(r0 + r, c) : 0.f;
-#pragma unroll
-        for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[dh][r]));
-        for (int rr = 0; rr < p.n_q; ++rr)
-          if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr, c)));
-      }
-      sq = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.0f);
-#pragma unroll
-      for (int dh = 0; dh < DH; ++dh) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          uint8_t code = 0;
-          if (r < nr) code = __nv_cvt_float_to_fp8(__fdiv_rn(xr[dh][r], sq), __NV_SATFINITE, __NV_E4M3);
-          smem[q_off(r, xq + 128 * dh)] = code;
-        }
-      }
-      zero_rows(NR);  // the rows past the tile
-    } else {
-      // bf16 Q as two e4m3 terms: hi = e4m3(x / s_hi) with s_hi = amax/448,
-      // lo = e4m3((x - hi*s_hi) / s_lo) with s_lo = (max |residual|)/448.
-      // hi fills rows 0 .. NR-1 of the Q tile and lo rows NR .. 2NR-1, so one
-      // QK product gives both terms; the logit is s_hi*S_hi + s_lo*S_lo.
-      // Thread xq owns EPT consecutive channels of one row (NR x D values
-      // over 128 threads; EPT divides 128, so they share one sub-tile).
-      constexpr int EPT = NR * DH;
-      const int row = (xq * EPT) / D, c0 = (xq * EPT) % D;
-      float xv[EPT];
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) xv[e] = 0.f;
-      if (row < nr) {
-        const int rr = r0 + row, tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
-        const uint16_t* src = p.q_bf16 + int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c0;
-#pragma unroll
-        for (int e = 0; e < EPT; e += 4) {
-          const uint2 u = *reinterpret_cast<const uint2*>(src + e);
-          xv[e] = __uint_as_float(u.x << 16);
-          xv[e + 1] = __uint_as_float(u.x & 0xFFFF0000u);
-          xv[e + 2] = __uint_as_float(u.y << 16);
-          xv[e + 3] = __uint_as_float(u.y & 0xFFFF0000u);
-        }
-      }
-      float am = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) am = fmaxf(am, fabsf(xv[e]));
-      const float s_hi = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.f);
-      uint32_t hw[EPT / 4];
-      float rm = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPT; e += 2) {
-        const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(xv[e], s_hi), __fdiv_rn(xv[e + 1], s_hi)), __NV_SATFINITE, __NV_E4M3);
-        const float2 hv = e4m3x2_to_float2(h2);
-        xv[e] -= hv.x * s_hi;  // the residual
-        xv[e + 1] -= hv.y * s_hi;
-        rm = fmaxf(rm, fmaxf(fabsf(xv[e]), fabsf(xv[e + 1])));
-        if ((e & 3) == 0)
-          hw[e / 4] = uint32_t(h2);
-        else
-          hw[e / 4] |= uint32_t(h2) << 16;
-      }
-      const float rmax = block_max(rm, 1);
-      const float s_lo = rmax > 0.f ? __fdiv_rn(rmax, 448.f) : 1.f;
-      uint32_t lw[EPT / 4];
-#pragma unroll
-      for (int e = 0; e < EPT; e += 2) {
-        const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(xv[e], s_lo), __fdiv_rn(xv[e + 1], s_lo)), __NV_SATFINITE, __NV_E4M3);
-        if ((e & 3) == 0)
-          lw[e / 4] = uint32_t(l2);
-        else
-          lw[e / 4] |= uint32_t(l2) << 16;
-      }
-      // 4 codes per word (c is a multiple of 4: one 16-byte chunk)
-#pragma unroll
-      for (int e = 0; e < EPT; e += 4) {
-        const int c = c0 + e;
-        *reinterpret_cast<uint32_t*>(smem + q_off(row, c)) = hw[e / 4];
-        *reinterpret_cast<uint32_t*>(smem + q_off(NR + row, c)) = lw[e / 4];
-      }
-      zero_rows(2 * NR);  // the rows past the two terms
-      const float kq = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g) * p.qk_scale_log2;
-      sc_hi = s_hi * kq;
-      sc_lo = s_lo * kq;
-    }
-    tc::fence_async_smem();
-    tc::mbar_arrive(tc::smem_u32(&ctl.q_ready));
-    const int qd = warp & 3;          // TMEM lane quadrant of this warp
-    const int x = qd * 32 + lane;     // key of the tile (S) / channel (O)
-    const uint32_t lane_off = uint32_t(qd * 32) << 16;
-    const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
-    // bf16 Q as two terms: the logits are formed when S is read (scale 1 below)
-    const float scale =
-        QM == 1 ? 1.f : (QM == 2 ? sq : p.q_descale[int64_t(b) * p.h_k + g]) * kd * p.qk_scale_log2;
-    // last visible key of each row (query token t sees keys j <= L - q_len + t)
-    int lim[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-      lim[r] = r < nr ? (p.causal ? L - p.q_len + (r0 + r) / p.h_r : INT_MAX) : -1;
-    const int lim_min = lim[0];  // the tile's first row has the smallest limit
-
-    // m_ref: the reference max each row's P is scaled by; it only moves when a
-    // tile's max exceeds it by more than kTau (log2 units), and then O (kept
-    // in TMEM across tiles) is rescaled in place. P = 2^(t - m_ref + 8) stays
-    // <= 2^(8 + kTau) < 448, so both e4m3 terms of P stay finite.
-    constexpr float kTau = 0.6f;
-    float m_ref[NR], l_part[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      m_ref[r] = -INFINITY;
-      l_part[r] = 0.f;
-    }
-    bool ok = true;
-    constexpr int kGroup = 32 / NR;  // lanes that share a row after rs_reduce
-    const int my_row = lane / kGroup;
-
-    // TP tiles per iteration: with few rows, the two S buffers are processed
-    // together (256 keys), so the row-max reduction, the cross-warp exchange
-    // and the fences are paid once per pair and the two tiles' arithmetic
-    // interleaves.
-    for (int i = 0; i < ntiles; i += TP) {
-      const int nt = min(TP, ntiles - i);
-      float s[TP][NR];  // S columns of the real rows only
-#pragma unroll
-      for (int a = 0; a < TP; ++a) {
-        if (a < nt) {
-          ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.s_full[bs(i + a)]), bp(i + a), abort, kWaitLimitNs);
-        }
-      }
-      if (!ok) break;
-      tc::tc_fence_after();
-      if constexpr (QM != 1) {
-#pragma unroll
-        for (int a = 0; a < TP; ++a) {
-          if (a < nt) {
-            tc::tmem_ld_cols<NR>(tS(i + a) + lane_off, s[a]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < NR; ++c) s[a][c] = -INFINITY;
-          }
-        }
-        tc::tmem_wait_ld();
-      } else {
-        // columns 0 .. NR-1: the hi term's products, NR .. 2NR-1: the lo term's
-        float s2[TP][2 * NR];
-#pragma unroll
-        for (int a = 0; a < TP; ++a)
-          if (a < nt) tc::tmem_ld_cols<2 * NR>(tS(i + a) + lane_off, s2[a]);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int a = 0; a < TP; ++a)
-#pragma unroll
-          for (int c = 0; c < NR; ++c) s[a][c] = a < nt ? fmaf(s2[a][NR + c], sc_lo, s2[a][c] * sc_hi) : -INFINITY;
-      }
-
-      int key[TP];
-      bool valid[TP];
-#pragma unroll
-      for (int a = 0; a < TP; ++a) {
-        key[a] = int(k0) + (i + a) * kKvTile + x;
-        valid[a] = a < nt && key[a] < int(k1);
-      }
-      // Every key of the iteration visible to every row (the common case:
-      // no tile past the end, no causal limit inside): no per-row masks.
-      // Rows past nr then see S = 0 (their Q rows are zero); their P only
-      // reaches O columns that are never written out.
-      const int64_t it_end = k0 + int64_t(i + nt) * kKvTile;  // one past the iteration's last key
-      const bool all_vis = nt == TP && it_end <= k1 && it_end - 1 <= int64_t(lim_min);
-      float tmp[NR];
-      if (all_vis) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          float v = s[0][r] * scale;
-#pragma unroll
-          for (int a = 1; a < TP; ++a) v = fmaxf(v, s[a][r] * scale);
-          tmp[r] = v;
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          float v = -INFINITY;
-#pragma unroll
-          for (int a = 0; a < TP; ++a)
-            v = fmaxf(v, (valid[a] && key[a] <= lim[r]) ? s[a][r] * scale : -INFINITY);
-          tmp[r] = v;
-        }
-      }
-      const int xi = i / TP;  // exchange sequence number
-      const float wmax = rs_reduce<NR, true>(tmp, lane);
-      if (lane % kGroup == 0) ctl.red[xi & 1][qd][my_row] = wmax;
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.red_bar[xi & 1]));
-      ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[xi & 1]), uint32_t(xi >> 1) & 1u, abort, kWaitLimitNs);
-      if (!ok) break;
-
-      // new reference maxima (the same decision in every thread)
-      bool rescale = false;
-#pragma unroll
-      for (int r = 0; r < NR; r += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][0][r]);
-        const float4 b4 = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][1][r]);
-        const float4 c4 = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][2][r]);
-        const float4 d4 = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][3][r]);
-        const float tm[4] = {fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x)), fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y)),
-                             fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z)), fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w))};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float alpha = 1.f;
-          if (tm[j] > m_ref[r + j] + kTau) {  // false for -inf tiles
-            alpha = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
-            rescale |= m_ref[r + j] != -INFINITY;
-            m_ref[r + j] = tm[j];
-            l_part[r + j] *= alpha;
-          }
-          // the O rescale below reads the factors back from shared memory
-          if (lane == 0) ctl.alpha[qd][r + j] = alpha;
-        }
-      }
-      // P = 2^(t - m_ref + 8) as hi + lo e4m3 terms; this key's column of
-      // P^T: hi of row r at byte r, lo at byte NH + r of the key's 16-byte
-      // chunk in 16-column block (byte / 16).
-      // (one body, instantiated masked and unmasked: a select would make
-      // fully visible tiles pay for the masks)
-      auto make_p = [&](auto masked) {
-        float c8[NR];
-#pragma unroll
-        for (int r = 0; r < NR; ++r) c8[r] = 8.f - m_ref[r];
-#pragma unroll
-        for (int a = 0; a < TP; ++a) {
-          if (a >= nt) break;
-          uint32_t words[NPV / 4];
-#pragma unroll
-          for (int w2 = 0; w2 < NPV / 4; ++w2) words[w2] = 0u;
-#pragma unroll
-          for (int r = 0; r < NR; r += 2) {
-            float pr[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              if constexpr (decltype(masked)::value) {
-                const bool vis = valid[a] && key[a] <= lim[r + j] && m_ref[r + j] != -INFINITY;
-                pr[j] = vis ? fast_exp2(fmaf(s[a][r + j], scale, c8[r + j])) : 0.f;
-              } else {
-                pr[j] = fast_exp2(fmaf(s[a][r + j], scale, c8[r + j]));
-              }
-            }
-            const __nv_fp8x2_storage_t hi2 =
-                __nv_cvt_float2_to_fp8x2(make_float2(pr[0], pr[1]), __NV_SATFINITE, __NV_E4M3);
-            const float2 hf = e4m3x2_to_float2(hi2);
-            const __nv_fp8x2_storage_t lo2 =
-                __nv_cvt_float2_to_fp8x2(make_float2(pr[0] - hf.x, pr[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
-            const float2 lf = e4m3x2_to_float2(lo2);
-            l_part[r] += hf.x + lf.x;
-            l_part[r + 1] += hf.y + lf.y;
-            words[r / 4] |= uint32_t(hi2) << ((r % 4) * 8);
-            words[(NH + r) / 4] |= uint32_t(lo2) << (((NH + r) % 4) * 8);
-          }
-          uint8_t* pt = smem + lay.p0 + bs(i + a) * p_stride;
-#pragma unroll
-          for (int bk = 0; bk < NPV / 16; ++bk)
-            *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
-                make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
-        }
-      };
-      if (all_vis)
-        make_p(std::false_type{});
-      else
-        make_p(std::true_type{});
-      if (rescale) {
-        // O holds the PV sums up to tile i-1, scaled by the old references:
-        // wait for the last of them and rescale O in TMEM before PV_i (which
-        // waits for p_full, signalled below). Done after P is written, when
-        // S no longer occupies registers.
-        ok = tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(i - 1)]), bp(i - 1), abort, kWaitLimitNs);
-        if (!ok) break;
-        __syncwarp();  // lane 0's factors
-        tc::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < DH * NPV; c += 16) {
-          float v[16];
-          tc::tmem_ld16(tO + lane_off + c, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = (c + j) % NPV;            // column within its O accumulator
-            const int r = col < NH ? col : col - NH;  // hi column r, lo column NH + r
-            if (r < NR) v[j] *= ctl.alpha[qd][r];
-          }
-          tc::tmem_st16(tO + lane_off + c, v);
-        }
-        tc::tmem_wait_st();
-      }
-
-      tc::fence_async_smem();
-      tc::tc_fence_before();
-#pragma unroll
-      for (int a = 0; a < TP; ++a)
-        if (a < nt) tc::mbar_arrive(tc::smem_u32(&ctl.p_full[bs(i + a)]));
-      if (!ok) break;
-    }
-    // the final O: wait for the last PV product; o_acc[dh][r] is channel 128 dh + x
-    float o_acc[DH][NR];
-#pragma unroll
-    for (int dh = 0; dh < DH; ++dh)
-#pragma unroll
-      for (int r = 0; r < NR; ++r) o_acc[dh][r] = 0.f;
-    ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(ntiles - 1)]), bp(ntiles - 1), abort, kWaitLimitNs);
-    if (ok) {
-      tc::tc_fence_after();
-#pragma unroll
-      for (int dh = 0; dh < DH; ++dh) {
-#pragma unroll
-        for (int c = 0; c < NPV; c += 16) {
-          float v[16];
-          tc::tmem_ld16(tO + lane_off + dh * NPV + c, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c + j;
-            const int r = col < NH ? col : col - NH;
-            if (r < NR) o_acc[dh][r] += v[j];
-          }
-        }
-      }
-    }
-
-    // ---- epilogue --------------------------------------------------------
-    {
-      float tmp[NR];
-#pragma unroll
-      for (int r = 0; r < NR; ++r) tmp[r] = l_part[r];
-      const float wsum = rs_reduce<NR, false>(tmp, lane);
-      if (lane % kGroup == 0) ctl.lsum[qd][my_row] = wsum;
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.sum_bar));
-    ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.sum_bar), 0, abort, kWaitLimitNs);
-    if (ok) {
-      const bool direct = !p.with_reduction || p.n_splits[b] <= 1;
-      const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (r >= nr) break;
-        const float lr = ctl.lsum[0][r] + ctl.lsum[1][r] + ctl.lsum[2][r] + ctl.lsum[3][r];
-        const int row = r0 + r;
-        const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
-        const int64_t idx = direct ? 0 : part_index(p, b, w.w, g, row);
-#pragma unroll
-        for (int dh = 0; dh < DH; ++dh) {
-          const int ch = 128 * dh + x;
-          const float on = lr > 0.f ? o_acc[dh][r] / lr : 0.f;
-          if (direct) {
-            float val = on * vd;
-            if (p.o_mul) val *= p.o_mul[int64_t(h) * D + ch];
-            p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + ch] = float_to_out_bits(val, p.out_f16);
-          } else {
-            p.o_part[idx * D + ch] = on;
-          }
-        }
-        if (x == 0) {
-          if (direct) {
-            if (p.lse)
-              p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
-                  lr > 0.f ? (m_ref[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
-          } else {
-            p.m_part[idx] = lr > 0.f ? m_ref[r] : -INFINITY;
-            p.l_part[idx] = lr * (1.f / 256.f);
-          }
-        }
-      }
-    }
-  }
-
-  // ---- teardown ------------------------------------------------------------
-  if (*abort && tid == 0) atomicOr(p.status, kStatusTimeout);
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, kTmemCols);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // host side
@@ -922,7 +36,7 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   cuuint64_t strides[3];
   cuuint32_t box[4];
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  dims[0] = cuuint64_t(p.d);  // channels (e4m3 bytes, or e2m3 codes); a box is 128 of them
+  dims[0] = cuuint64_t(p.d);  // channels (e4m3 bytes, or packed codes); a box is 128 of them
   box[0] = 128;
   if (head_inner) {
     dims[1] = cuuint64_t(p.h_k);
@@ -942,62 +56,18 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
   dims[3] = cuuint64_t(p.num_pages);
   strides[2] = cuuint64_t(sp);
   box[3] = 1;
-  // e4m3: one byte per element. Packed e2m3 (D = 128 only): 16U6_ALIGN16B
-  // keeps 16 codes in 12 bytes and lands each group in a 16-byte shared-memory
-  // chunk (4 bytes of padding), which tcgen05.mma reads as e2m3; dims[0]
-  // counts codes.
-  const CUtensorMapDataType dt =
-      p.kv_format == MJ_KV_E2M3 ? CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  // e4m3: one byte per element. Packed formats (D = 128 only): 16U6_ALIGN16B
+  // (e2m3, e3m2) keeps 16 codes in 12 bytes and lands each group in a 16-byte
+  // shared-memory chunk (4 bytes of padding); 16U4_ALIGN16B (e2m1) keeps 16
+  // codes in 8 bytes and lands them in the first half of a 16-byte chunk.
+  // tcgen05.mma reads either chunk as its 16 codes; dims[0] counts codes.
+  const CUtensorMapDataType dt = p.kv_format == MJ_KV_E4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : p.kv_format == MJ_KV_E2M1 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
+                                                             : CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B;
   const CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
-}
-
-constexpr int kMaxDynSmem = 227 * 1024;  // per-block opt-in limit of sm_100-class GPUs
-
-template <int NQK, int NPV, int NR, bool FP6, int QM, int D>
-cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p0, cudaStream_t stream) {
-  DecodeParams p = p0;
-  // the ring depth the shared memory holds (even, at least 2)
-  auto smem_bytes = [&](int stages) {
-    return int(tc_smem_layout(stages, NQK, NPV, NR <= 8 ? 4 : 2, D / 128).total) + 1024;
-  };
-  while (p.kv_stages > 2 && smem_bytes(p.kv_stages) > kMaxDynSmem) p.kv_stages -= 2;
-  const int bytes = smem_bytes(p.kv_stages);
-  static int configured = 0;  // largest dynamic smem size set so far
-  if (bytes > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, FP6, QM, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    configured = bytes;
-  }
-  cudaLaunchConfig_t cfg = {};
-  if (int64_t(p.num_work) * p.h_k > INT32_MAX || p.n_row_tiles > 65535) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3(unsigned(p.num_work) * unsigned(p.h_k), unsigned(p.n_row_tiles));
-  cfg.blockDim = dim3(FP6 ? kThreadsTcFp6 : kThreadsTc);
-  cfg.dynamicSmemBytes = size_t(bytes);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with mj_quantize_q
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NQK, NPV, NR, FP6, QM, D>, mk, mv, p);
-}
-
-// The kernel instance for the row tile (the plan's tile width, 16 or 32
-// rows; fewer rows take the 4- or 8-row variants). With bf16 Q as two terms
-// the Q tile holds two rows (hi, lo) per query row.
-template <bool FP6, int QM, int D = 128>
-cudaError_t launch_rows(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
-  constexpr int K = QM == 1 ? 2 : 1;
-  if (p.tw <= 16) {
-    if (p.n_q <= 4) return launch_tc<16, 16, 4, FP6, QM, D>(mk, mv, p, stream);
-    if (p.n_q <= 8) return launch_tc<16, 16, 8, FP6, QM, D>(mk, mv, p, stream);
-    return launch_tc<16 * K, 32, 16, FP6, QM, D>(mk, mv, p, stream);
-  }
-  return launch_tc<32 * K, 64, 32, FP6, QM, D>(mk, mv, p, stream);
 }
 
 }  // namespace
@@ -1008,15 +78,13 @@ int tc_default_stages(int d) { return d == 256 ? 2 : 6; }
 
 bool tc_supported(const DecodeParams& p) {
   if (p.q_mode == MJ_Q_BF16 && p.kv_format != MJ_KV_E4M3) return false;
-  if (p.kv_format == MJ_KV_E2M3 && p.d != 128) return false;  // packed e2m3: D = 128 only
-  if (p.kv_format == MJ_KV_E2M3) {
-    // the packed TMA type wants 32-byte aligned strides (and base, checked
-    // by the ABI for e2m3)
+  if (p.kv_format != MJ_KV_E4M3) {
+    if (p.d != 128) return false;  // packed formats: D = 128 only
+    // the packed TMA types want 32-byte aligned strides (and base, checked
+    // by the ABI for the packed formats)
     const int64_t st[] = {p.k_sp, p.k_st, p.k_sh, p.v_sp, p.v_st, p.v_sh};
     for (int64_t v : st)
       if (v % 32) return false;
-  } else if (p.kv_format != MJ_KV_E4M3) {
-    return false;
   }
   if (p.n_q > 32 && p.tw != 32) return false;
   if (p.num_pages > INT32_MAX || p.h_k > 65535) return false;
@@ -1060,22 +128,15 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
   }
   if (p.num_work == 0) return cudaSuccess;
   // row tile = the plan's tile width (16 or 32 rows)
-  if (p.kv_format == MJ_KV_E2M3) {
-    // K enters the MMA as true e2m3 values (no 2^-6 widening factor); V is
-    // widened in shared memory and keeps the factor in v_fmt.
-    p.qk_scale_log2 *= 1.0f / 64.0f;
-    // packed e2m3 KV takes fp8 Q only: codes, or quantized here
-    return p.q_mode == MJ_Q_FP8_FUSED ? launch_rows<true, 2>(mk, mv, p, stream)
-                                      : launch_rows<true, 0>(mk, mv, p, stream);
+  if (p.kv_format != MJ_KV_E4M3) {
+    // K enters the MMA as true values (no widening factor); V is widened in
+    // shared memory and keeps the factor in v_fmt.
+    p.qk_scale_log2 *= 1.0f / kv_widen_factor(p.kv_format);
+    if (p.kv_format == MJ_KV_E2M3) return launch_tc_e2m3(mk, mv, p, stream);
+    if (p.kv_format == MJ_KV_E3M2) return launch_tc_e3m2(mk, mv, p, stream);
+    return launch_tc_e2m1(mk, mv, p, stream);
   }
-  if (p.d == 256) {
-    if (p.q_mode == MJ_Q_BF16) return launch_rows<false, 1, 256>(mk, mv, p, stream);
-    if (p.q_mode == MJ_Q_FP8_FUSED) return launch_rows<false, 2, 256>(mk, mv, p, stream);
-    return launch_rows<false, 0, 256>(mk, mv, p, stream);
-  }
-  if (p.q_mode == MJ_Q_BF16) return launch_rows<false, 1>(mk, mv, p, stream);
-  if (p.q_mode == MJ_Q_FP8_FUSED) return launch_rows<false, 2>(mk, mv, p, stream);
-  return launch_rows<false, 0>(mk, mv, p, stream);
+  return p.d == 256 ? launch_tc_e4m3_d256(mk, mv, p, stream) : launch_tc_e4m3_d128(mk, mv, p, stream);
 }
 
 }  // namespace mj

@@ -4,12 +4,13 @@
 // the mjolnir/backend.py page): token t's row of KV head g goes to page
 // slot / page_size, row slot % page_size; code = fmt(x / scale), with one
 // scale per tensor or per KV head (e4m3) or per (KV head, channel) (packed
-// e2m3, the channel scales of _install_fp6_scales). The quotient is IEEE
+// e2m3, the channel scales of _install_fp6_scales; e3m2 and e2m1 likewise).
+// The quotient is IEEE
 // float32 (__fdiv_rn) and the rounding to the cache format is to nearest,
 // ties to even, saturating, so the bytes are identical to that recipe.
 //
 // HBM-bound: each thread reads one 16-byte chunk of bf16 of K and of V
-// (8 channels; two chunks for e2m3) and writes their codes once.
+// (8 channels; two chunks for the packed formats) and writes their codes once.
 // Consecutive threads take consecutive chunks of a row, and rows of
 // consecutive heads and tokens, so both the loads and the stores are
 // coalesced.
@@ -45,6 +46,38 @@ __device__ __forceinline__ uint32_t e2m3_code(float y) {
   return c | (signbit(y) ? 0x20u : 0u);
 }
 
+// e3m2 code of y: round to nearest, ties to even, saturating at 28; sign bit
+// 5. Below 0.25 the subnormal grid is k/16; each binade [2^e, 2^(e+1)),
+// e = -2 .. 4, has 4 steps of 2^e / 4 (code (e + 3) * 4 + step). As in
+// e2m3_code the scalings are exact and __float2uint_rn is the one rounding.
+__device__ __forceinline__ uint32_t e3m2_code(float y) {
+  const float a = fminf(fabsf(y), 28.0f);
+  uint32_t c;
+  if (a < 0.25f) {
+    c = __float2uint_rn(a * 16.0f);  // 0 .. 4 (4 = 0.25, the first normal)
+  } else {
+    const int e = (__float_as_int(a) >> 23) - 127;          // floor(log2 a), -2 .. 4
+    const float m = a * __int_as_float((127 - e) << 23);    // a / 2^e, in [1, 2)
+    c = (uint32_t(e + 3) << 2) + __float2uint_rn((m - 1.0f) * 4.0f);
+  }
+  return c | (signbit(y) ? 0x20u : 0u);
+}
+
+// e2m1 code of y: round to nearest, ties to even, saturating at 6; sign bit 3.
+// Below 1 the grid is k/2; binades [1, 2), [2, 4), [4, 8) have 2 steps each.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fminf(fabsf(y), 6.0f);
+  uint32_t c;
+  if (a < 1.0f) {
+    c = __float2uint_rn(a * 2.0f);  // 0 .. 2 (2 = 1.0)
+  } else {
+    const int e = a >= 4.0f ? 2 : (a >= 2.0f ? 1 : 0);
+    const float m = a * __int_as_float((127 - e) << 23);  // a / 2^e, in [1, 2)
+    c = (uint32_t(e + 1) << 1) + __float2uint_rn((m - 1.0f) * 2.0f);
+  }
+  return c | (signbit(y) ? 0x8u : 0u);
+}
+
 __device__ __forceinline__ void bf16x8_to_float(uint4 v, float x[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -72,10 +105,10 @@ struct WriteParams {
 };
 
 // Quantize one loaded chunk (CH channels of a K or V row) and store its codes.
-// e4m3: in[0] holds 8 channels; e2m3: in[0..1] hold 16.
-template <bool E2M3>
+// e4m3: in[0] holds 8 channels; the packed formats: in[0..1] hold 16.
+template <int F>
 __device__ __forceinline__ void quantize_store(const uint4* in, const float* scale, uint8_t* dst, int c) {
-  if constexpr (!E2M3) {
+  if constexpr (F == MJ_KV_E4M3) {
     float x[8];
     bf16x8_to_float(in[0], x);
     const float s = scale[0];
@@ -87,6 +120,24 @@ __device__ __forceinline__ void quantize_store(const uint4* in, const float* sca
       const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
           make_float2(__fdiv_rn(x[4 * k + 2], s), __fdiv_rn(x[4 * k + 3], s)), __NV_SATFINITE, __NV_E4M3);
       w[k] = uint32_t(lo) | (uint32_t(hi) << 16);
+    }
+    *reinterpret_cast<uint2*>(dst + c * 8) = make_uint2(w[0], w[1]);
+  } else if constexpr (F == MJ_KV_E2M1) {
+    // 16 codes, code k at bits [4k, 4k + 4) of 8 little-endian bytes
+    float x[16];
+    bf16x8_to_float(in[0], x);
+    bf16x8_to_float(in[1], x + 8);
+    const float4* sc = reinterpret_cast<const float4*>(scale + c * 16);
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 s4 = sc[q];
+      const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int idx = 4 * q + k;
+        w[idx >> 3] |= e2m1_code(__fdiv_rn(x[idx], sv[k])) << (4 * (idx & 7));
+      }
     }
     *reinterpret_cast<uint2*>(dst + c * 8) = make_uint2(w[0], w[1]);
   } else {
@@ -103,7 +154,8 @@ __device__ __forceinline__ void quantize_store(const uint4* in, const float* sca
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int idx = 4 * q + k, bit = 6 * idx;
-        const uint64_t code = e2m3_code(__fdiv_rn(x[idx], sv[k]));
+        const float q6 = __fdiv_rn(x[idx], sv[k]);
+        const uint64_t code = F == MJ_KV_E2M3 ? e2m3_code(q6) : e3m2_code(q6);
         if (bit < 64) {
           lo |= code << bit;
           if (bit + 6 > 64) hi |= code >> (64 - bit);
@@ -120,18 +172,20 @@ __device__ __forceinline__ void quantize_store(const uint4* in, const float* sca
 }
 
 // One work item per (token, head, chunk of CH channels), K and V: CH = 8 for
-// e4m3 (8 codes = 8 bytes), 16 for e2m3 (16 codes = 12 bytes). A thread takes
+// e4m3 (8 codes = 8 bytes), 16 for the packed formats (16 codes = 12 bytes,
+// or 8 for e2m1). A thread takes
 // U items a stride apart and issues all their loads before any store, so
 // enough bytes are in flight to cover the memory latency (the stores may
 // alias the inputs as far as the compiler knows, so it would not reorder
 // them itself). The row index (token, head) fits in 32 bits (checked on the
 // host).
-template <bool E2M3, int D>
+template <int F, int D>
 __global__ void __launch_bounds__(kThreads) write_kv_kernel(WriteParams p) {
-  constexpr int CH = E2M3 ? 16 : 8;
+  constexpr bool PK = F != MJ_KV_E4M3;  // packed (channel-scaled) format
+  constexpr int CH = PK ? 16 : 8;
   constexpr int NCH = D / CH;  // chunks per row
   constexpr int NV = CH / 8;          // 16-byte loads per chunk of one side
-  constexpr int U = E2M3 ? 2 : 4;     // items per thread per round
+  constexpr int U = PK ? 2 : 4;       // items per thread per round
   const uint64_t total = uint64_t(uint32_t(p.num_tokens) * uint32_t(p.h_k)) * NCH;
   const uint64_t stride = uint64_t(gridDim.x) * kThreads;
   for (uint64_t base = uint64_t(blockIdx.x) * kThreads + threadIdx.x; base < total; base += U * stride) {
@@ -167,12 +221,22 @@ __global__ void __launch_bounds__(kThreads) write_kv_kernel(WriteParams p) {
       }
       const int g = head[u];
       const int64_t page = slot[u] / p.page_size, prow = slot[u] % p.page_size;
-      const int s_idx = E2M3 ? g * D : (p.scale_per_head ? g : 0);
-      quantize_store<E2M3>(kin[u], p.k_scale + s_idx, p.k_cache + page * p.k_sp + prow * p.k_st + g * p.k_sh,
+      const int s_idx = PK ? g * D : (p.scale_per_head ? g : 0);
+      quantize_store<F>(kin[u], p.k_scale + s_idx, p.k_cache + page * p.k_sp + prow * p.k_st + g * p.k_sh,
                            chunk[u]);
-      quantize_store<E2M3>(vin[u], p.v_scale + s_idx, p.v_cache + page * p.v_sp + prow * p.v_st + g * p.v_sh,
+      quantize_store<F>(vin[u], p.v_scale + s_idx, p.v_cache + page * p.v_sp + prow * p.v_st + g * p.v_sh,
                            chunk[u]);
     }
+  }
+}
+
+template <int D>
+void launch_format(int kv_format, unsigned nb, const WriteParams& p, cudaStream_t stream) {
+  switch (kv_format) {
+    case MJ_KV_E2M3: write_kv_kernel<MJ_KV_E2M3, D><<<nb, kThreads, 0, stream>>>(p); break;
+    case MJ_KV_E3M2: write_kv_kernel<MJ_KV_E3M2, D><<<nb, kThreads, 0, stream>>>(p); break;
+    case MJ_KV_E2M1: write_kv_kernel<MJ_KV_E2M1, D><<<nb, kThreads, 0, stream>>>(p); break;
+    default: write_kv_kernel<MJ_KV_E4M3, D><<<nb, kThreads, 0, stream>>>(p); break;
   }
 }
 
@@ -205,8 +269,8 @@ cudaError_t launch_write_kv(const mj_write_kv_args& a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.scale_per_head = a.scale_per_head;
   p.status = a.status;
-  const bool e2m3 = a.kv_format == MJ_KV_E2M3;
-  const int64_t work = int64_t(a.num_tokens) * a.h_k * (a.d / (e2m3 ? 16 : 8));
+  const bool packed = a.kv_format != MJ_KV_E4M3;
+  const int64_t work = int64_t(a.num_tokens) * a.h_k * (a.d / (packed ? 16 : 8));
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -222,18 +286,10 @@ cudaError_t launch_write_kv(const mj_write_kv_args& a, cudaStream_t stream) {
   const int sms = sm_count[dev];
   // enough blocks to fill every SM (8 x 256 threads each), fewer for small writes
   const int64_t blocks = std::min<int64_t>((work + kThreads - 1) / kThreads, int64_t(sms) * 8);
-  const unsigned nb = unsigned(blocks);
-  if (a.d == 256) {
-    if (e2m3)
-      write_kv_kernel<true, 256><<<nb, kThreads, 0, stream>>>(p);
-    else
-      write_kv_kernel<false, 256><<<nb, kThreads, 0, stream>>>(p);
-  } else {
-    if (e2m3)
-      write_kv_kernel<true, 128><<<nb, kThreads, 0, stream>>>(p);
-    else
-      write_kv_kernel<false, 128><<<nb, kThreads, 0, stream>>>(p);
-  }
+  if (a.d == 256)
+    launch_format<256>(a.kv_format, unsigned(blocks), p, stream);
+  else
+    launch_format<128>(a.kv_format, unsigned(blocks), p, stream);
   return cudaGetLastError();
 }
 

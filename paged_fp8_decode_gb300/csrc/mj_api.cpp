@@ -38,14 +38,14 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   if (!a) return MJ_ERR_INVALID_ARG;
   if (a->num_seqs < 0 || a->q_len < 1 || a->h_k < 1 || a->h_q < 1 || a->h_q % a->h_k) return MJ_ERR_INVALID_ARG;
   if (!mj::head_dim_ok(a->d)) return MJ_ERR_UNSUPPORTED;
-  if (a->kv_format != MJ_KV_E4M3 && a->kv_format != MJ_KV_E2M3) return MJ_ERR_UNSUPPORTED;
+  if (!mj::kv_format_ok(a->kv_format)) return MJ_ERR_UNSUPPORTED;
   if (!page_size_ok(a->page_size)) return MJ_ERR_UNSUPPORTED;
   if (a->num_pages < 1 || a->num_work < 0 || a->block_table_stride < 0) return MJ_ERR_INVALID_ARG;
   if (a->impl < MJ_IMPL_AUTO || a->impl > MJ_IMPL_TCGEN05) return MJ_ERR_INVALID_ARG;
   if (!(a->softmax_scale > 0.f) || !std::isfinite(a->softmax_scale)) return MJ_ERR_INVALID_ARG;
   if (a->q_mode != MJ_Q_FP8 && a->q_mode != MJ_Q_BF16 && a->q_mode != MJ_Q_FP8_FUSED) return MJ_ERR_UNSUPPORTED;
   const bool bf16_q = a->q_mode != MJ_Q_FP8;  // the call reads bf16 Q
-  if (a->q_mode == MJ_Q_BF16 && a->kv_format != MJ_KV_E4M3) return MJ_ERR_UNSUPPORTED;  // e2m3 KV is fp8-Q only
+  if (a->q_mode == MJ_Q_BF16 && a->kv_format != MJ_KV_E4M3) return MJ_ERR_UNSUPPORTED;  // packed KV is fp8-Q only
   if (a->q_mul && !aligned(a->q_mul, 16)) return MJ_ERR_ALIGNMENT;
   const void* q0 = bf16_q ? a->q_bf16 : a->q_codes;
   const void* q1 = bf16_q ? a->q_bf16 : a->q_descale;
@@ -57,7 +57,7 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
     if (a->q_tok_stride < 0 || a->q_head_stride < 0) return MJ_ERR_INVALID_ARG;
     if (a->q_tok_stride % 8 || a->q_head_stride % 8) return MJ_ERR_ALIGNMENT;
   }
-  const uintptr_t kv_align = a->kv_format == MJ_KV_E2M3 ? 32 : 16;
+  const uintptr_t kv_align = a->kv_format == MJ_KV_E4M3 ? 16 : 32;
   const void* a16[] = {q0, q1, a->block_table, a->seq_lens, a->work,
                        a->n_splits, a->out, a->workspace};
   for (const void* ptr : a16)
@@ -100,7 +100,7 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   q.causal = a->causal ? 1 : 0;
   q.kv_format = a->kv_format;
   q.page_size = a->page_size;
-  q.row_bytes = a->kv_format == MJ_KV_E4M3 ? a->d : a->d * 3 / 4;
+  q.row_bytes = mj::kv_row_bytes(a->kv_format, a->d);
   q.num_pages = a->num_pages;
   q.tw = mj_tile_width(n_q);
   q.n_row_tiles = n_row_tiles(n_q);
@@ -133,8 +133,8 @@ int make_params(const mj_decode_args* a, DecodeParams* p) {
   q.chunk_tiles = std::max(1, a->chunk_tiles);
   q.max_splits = std::max(1, a->max_splits);
   q.part_seqs = a->part_seqs;
-  // Widened e2m3 codes are the true values times 2^-6 (see e2m3x4_to_e4m3x4).
-  const float fmt = a->kv_format == MJ_KV_E2M3 ? 64.f : 1.f;
+  // Widened narrow codes are the true values over kv_widen_factor.
+  const float fmt = mj::kv_widen_factor(a->kv_format);
   q.qk_scale_log2 = a->softmax_scale * 1.4426950408889634f * fmt;
   q.v_fmt = fmt;
   q.o_mul = a->o_mul;
@@ -286,7 +286,7 @@ int mj_write_kv(const mj_write_kv_args* a, void* stream) {
   if (!a) return MJ_ERR_INVALID_ARG;
   if (a->num_tokens < 0 || a->h_k < 1 || a->num_pages < 0) return MJ_ERR_INVALID_ARG;
   if (!mj::head_dim_ok(a->d)) return MJ_ERR_UNSUPPORTED;
-  if (a->kv_format != MJ_KV_E4M3 && a->kv_format != MJ_KV_E2M3) return MJ_ERR_UNSUPPORTED;
+  if (!mj::kv_format_ok(a->kv_format)) return MJ_ERR_UNSUPPORTED;
   if (a->page_size != 16 && a->page_size != 32 && a->page_size != 64 && a->page_size != 128)
     return MJ_ERR_UNSUPPORTED;
   if (a->num_tokens == 0) return MJ_OK;

@@ -41,11 +41,33 @@ __device__ __forceinline__ uint32_t e2m3x4_to_e4m3x4(uint32_t four_codes) {
   return (four_codes & 0x1F1F1F1Fu) | ((four_codes & 0x20202020u) << 2);
 }
 
+// Widen four 6-bit e3m2 codes (one per byte) to e4m3 codes worth 2^-4 times
+// the e3m2 values: s|EEE|MM read as s|0EEE|MM0 has exponent E-7 instead of
+// E-3 (subnormals: step 2^-8 instead of 2^-4), the same scaling by 2^-4 in
+// both cases, so the move is exact.
+__device__ __forceinline__ uint32_t e3m2x4_to_e4m3x4(uint32_t four_codes) {
+  return ((four_codes & 0x1F1F1F1Fu) << 1) | ((four_codes & 0x20202020u) << 2);
+}
+
+// Widen four 4-bit e2m1 codes (one per byte) to e4m3 codes worth 2^-6 times
+// the e2m1 values: s|EE|M read as s|00EE|M00 (exponent E-7 instead of E-1;
+// the subnormal 0.5 becomes 2^-7), exact.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t four_codes) {
+  return ((four_codes & 0x07070707u) << 2) | ((four_codes & 0x08080808u) << 4);
+}
+
 // Spread four 6-bit codes held in the low 24 bits of `g` (code i at bits
 // [6i, 6i+6), the little-endian bitstream) into the four bytes of a word.
 __device__ __forceinline__ uint32_t spread6x4(uint32_t g) {
   return (g & 0x3Fu) | ((g << 2) & 0x3F00u) | ((g << 4) & 0x3F0000u) | ((g << 6) & 0x3F000000u);
 }
+
+// Spread four 4-bit codes held in the low 16 bits of `h` (code i at bits
+// [4i, 4i+4)) into the four bytes of a word.
+__device__ __forceinline__ uint32_t spread4x4(uint32_t h) {
+  return (h & 0xFu) | ((h << 4) & 0xF00u) | ((h << 8) & 0xF0000u) | ((h << 12) & 0xF000000u);
+}
+
 
 // 2^x with the hardware approximation (ex2.approx, relative error ~2^-22).
 // exp2(-inf) = 0.

@@ -16,6 +16,19 @@ constexpr int kMaxHeadDim = 256;
 inline bool head_dim_ok(int d) { return d == 128 || d == 256; }
 constexpr int kMaxRowTile = 32;
 
+// Widening factor of a cache format: the kernels widen a narrow code to an
+// e4m3 code worth value / factor (e2m3, e2m1: 2^-6; e3m2: 2^-4; e4m3: 1).
+__host__ __device__ constexpr float kv_widen_factor(int kv_format) {
+  return kv_format == MJ_KV_E3M2 ? 16.f : (kv_format == MJ_KV_E4M3 ? 1.f : 64.f);
+}
+
+// Bytes of one (token, KV head) row of a cache format.
+__host__ __device__ constexpr int kv_row_bytes(int kv_format, int d) {
+  return kv_format == MJ_KV_E4M3 ? d : (kv_format == MJ_KV_E2M1 ? d / 2 : d * 3 / 4);
+}
+
+inline bool kv_format_ok(int f) { return f >= MJ_KV_E4M3 && f <= MJ_KV_E2M1; }
+
 // Workspace layout: a 256-byte header (status word at offset 0), then the
 // split partials o_part [rows][d], m_part [rows], l_part [rows].
 constexpr size_t kWsHeader = 256;

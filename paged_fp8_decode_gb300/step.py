@@ -30,7 +30,7 @@ class PagedKV:
     v_strides: tuple
     page_size: int
     num_pages: int
-    kv_format: str  # "fp8" | "e2m3"
+    kv_format: str  # "fp8" | "e2m3" | "e3m2" | "e2m1"
     k_descale: torch.Tensor  # float32
     v_descale: torch.Tensor
     descale_strides: tuple  # (seq, head) in elements

@@ -379,6 +379,21 @@ def fp6_decode(seed: int = 1005) -> Workload:
                      seed=seed)
 
 
+def fp6_e3m2_decode(seed: int = 1007) -> Workload:
+    """:func:`fp6_decode` with packed e3m2 KV (largest 28; channel scales amax/28)."""
+    return make_case(name="fp6_e3m2_decode", num_seqs=128, q_len=1, h_q=64, h_k=8, page_size=128,
+                     seq_lens=[8192] * 128, layout="HND", kv_format="e3m2", outlier_channels=4,
+                     seed=seed)
+
+
+def fp4_decode(seed: int = 1008) -> Workload:
+    """:func:`fp6_decode` with packed e2m1 KV (largest 6; channel scales amax/6):
+    64-byte rows, 1.07 GB of KV."""
+    return make_case(name="fp4_decode", num_seqs=128, q_len=1, h_q=64, h_k=8, page_size=128,
+                     seq_lens=[8192] * 128, layout="HND", kv_format="e2m1", outlier_channels=4,
+                     seed=seed)
+
+
 def d256_decode(seed: int = 1006) -> Workload:
     """B=64, q_len=1, 16/8 heads (GQA 2), head size 256 (the head shape of
     Gemma-2/3-class models), page 16, every length 4096, per-KV-head e4m3
@@ -396,6 +411,8 @@ WORKLOADS = {
     "spec_verify_noncausal": lambda seed=1004: spec_verify(False, seed),
     "fp6_decode": fp6_decode,
     "d256_decode": d256_decode,
+    "fp6_e3m2_decode": fp6_e3m2_decode,
+    "fp4_decode": fp4_decode,
 }
 
 

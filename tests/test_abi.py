@@ -108,6 +108,7 @@ def _valid_args():
     ("d", 512, mj.MJ_ERR_UNSUPPORTED),
     ("page_size", 8, mj.MJ_ERR_UNSUPPORTED),
     ("kv_format", 7, mj.MJ_ERR_UNSUPPORTED),
+    ("kv_format", 4, mj.MJ_ERR_UNSUPPORTED),
     ("h_q", 9, mj.MJ_ERR_INVALID_ARG),
     ("q_len", 0, mj.MJ_ERR_INVALID_ARG),
     ("q_codes", None, mj.MJ_ERR_INVALID_ARG),
@@ -130,11 +131,20 @@ def test_decode_args_rejected_on_host(lib, field, value, status):
     assert lib.mj_merge_lse(ctypes.byref(a), None) == status
 
 
-def test_e2m3_needs_32_byte_kv_alignment(lib):
+@pytest.mark.parametrize("kv_format", [mj.MJ_KV_E2M3, mj.MJ_KV_E3M2, mj.MJ_KV_E2M1])
+def test_packed_formats_need_32_byte_kv_alignment(lib, kv_format):
     a = _valid_args()
-    a.kv_format = 1
+    a.kv_format = kv_format
     a.k_cache = (1 << 40) + 0x10010  # 16- but not 32-byte aligned
     assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("kv_format", [mj.MJ_KV_E3M2, mj.MJ_KV_E2M1])
+def test_packed_formats_refuse_bf16_q(lib, kv_format):
+    a = _valid_args()
+    a.kv_format, a.q_mode, a.q_bf16 = kv_format, mj.MJ_Q_BF16, 1 << 40
+    a.q_tok_stride, a.q_head_stride = 1024, 128
+    assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_UNSUPPORTED
 
 
 def test_reduction_needs_a_large_enough_workspace(lib):
@@ -202,7 +212,7 @@ def _valid_write_args():
 
 @pytest.mark.parametrize("field,value,status", [
     ("d", 64, mj.MJ_ERR_UNSUPPORTED),
-    ("kv_format", 3, mj.MJ_ERR_UNSUPPORTED),
+    ("kv_format", 4, mj.MJ_ERR_UNSUPPORTED),
     ("page_size", 48, mj.MJ_ERR_UNSUPPORTED),
     ("num_tokens", -1, mj.MJ_ERR_INVALID_ARG),
     ("h_k", 0, mj.MJ_ERR_INVALID_ARG),

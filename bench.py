@@ -78,10 +78,23 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Every source file a kernel is compiled from: a change to any of them makes
+# the committed DRAM counters stale.
+KERNEL_SOURCES = {
+    "decode_tc.cu": ["decode_tc.cu", "decode_tc_e4m3.cu", "decode_tc_e2m3.cu", "decode_tc_e3m2.cu",
+                     "decode_tc_e2m1.cu", "decode_tc_d256.cu", "decode_tc_kernel.cuh", "tc_ptx.cuh",
+                     "mj_device.cuh", "mj_internal.h"],
+    "decode_simt.cu": ["decode_simt.cu", "mj_device.cuh", "mj_internal.h"],
+}
+
+
 def _kernel_source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "paged_fp8_decode_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for part in KERNEL_SOURCES.get(name, [name]):
+        with open(os.path.join(ROOT, "paged_fp8_decode_gb300", "csrc", part), "rb") as f:
+            data = f.read()
+        h.update(part.encode() + b"\0" + len(data).to_bytes(8, "little") + data)
+    return h.hexdigest()[:16]
 
 
 def _traffic(kernel_file: str, workload: str):

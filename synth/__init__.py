@@ -159,7 +159,7 @@ def _e2m1_codes(x: np.ndarray) -> np.ndarray:
 
 def pack_e2m1(codes: np.ndarray) -> np.ndarray:
     """``[..., 2k]`` 4-bit codes -> ``[..., k]`` bytes, code 2j in the low nibble of byte j."""
-    c = codes.astype(np.uint8).reshape(codes.shape[:-1] + (-1, 2))
+    c = codes.astype(np.uint8).reshape(codes.shape[:-1] + (codes.shape[-1] // 2, 2))
     return (c[..., 0] | (c[..., 1] << 4)).astype(np.uint8)
 
 
@@ -174,13 +174,14 @@ def _narrow_rows(x: np.ndarray, kv_format: str) -> np.ndarray:
 
 def pack_e2m3(codes: np.ndarray) -> np.ndarray:
     """``[..., 4k]`` 6-bit codes -> ``[..., 3k]`` bytes, little-endian bitstream."""
-    c = codes.astype(np.uint32).reshape(codes.shape[:-1] + (-1, 4))
+    n = codes.shape[-1]
+    c = codes.astype(np.uint32).reshape(codes.shape[:-1] + (n // 4, 4))
     c0, c1, c2, c3 = c[..., 0], c[..., 1], c[..., 2], c[..., 3]
     b0 = (c0 | (c1 << 6)) & 0xFF
     b1 = ((c1 >> 2) | (c2 << 4)) & 0xFF
     b2 = ((c2 >> 4) | (c3 << 2)) & 0xFF
     out = np.stack([b0, b1, b2], axis=-1).astype(np.uint8)
-    return out.reshape(codes.shape[:-1] + (-1,))
+    return out.reshape(codes.shape[:-1] + (n // 4 * 3,))
 
 
 # ----------------------------------------------------------------------------

@@ -10,6 +10,13 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
+    # A child run of test_oracle_pins_catch_mistakes.py: install one planted
+    # mistake in the oracle before the pin modules are imported.
+    plant = os.environ.get("MJ_PLANT")
+    if plant:
+        from tests import _plants
+
+        _plants.apply(plant)
 
 
 def load_golden(name):

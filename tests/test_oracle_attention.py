@@ -29,6 +29,14 @@ def _small(**kw):
     return synth.make_case(**base)
 
 
+def _unit_scale(scale, g):
+    """The K or V descale of KV head ``g``, read straight from the array the
+    workload holds: one value for the whole tensor, or one per KV head.
+    (Kept apart from the oracle's own lookup so that a wrong index there shows.)"""
+    s = np.asarray(scale, dtype=np.float64).reshape(-1)
+    return float(s[0]) if s.size == 1 else float(s[g])
+
+
 @pytest.mark.parametrize("kv_format,q_len,causal,d", [("fp8", 1, True, 128), ("fp8", 3, True, 128),
                                                       ("fp8", 3, False, 128), ("e2m3", 2, True, 128),
                                                       ("fp8", 2, True, 256), ("e2m3", 1, False, 256),
@@ -41,7 +49,7 @@ def test_matches_brute_force(kv_format, q_len, causal, d):
     for b in range(w.num_seqs):
         for g in range(w.h_k):
             bf = A.brute_force_unit(codes[b, g], float(desc[b, g]), w.logical("k"), w.logical("v"),
-                                    A.descale_at(w.k_scale, b, g), A.descale_at(w.v_scale, b, g),
+                                    _unit_scale(w.k_scale, g), _unit_scale(w.v_scale, g),
                                     w.block_table, b, g, int(w.seq_lens[b]), w.page_size, w.kv_format,
                                     w.softmax_scale, w.q_len, w.h_r, causal)
             for row in range(w.n_q):
@@ -50,6 +58,25 @@ def test_matches_brute_force(kv_format, q_len, causal, d):
                 want = bf[row] * (w.o_mul[g * w.h_r + r] if w.o_mul is not None else 1.0)
                 np.testing.assert_allclose(o, want, rtol=1e-10, atol=1e-12)
 
+
+
+def test_per_request_and_head_descales_match_brute_force():
+    """Descales given per (request, KV head), a [B, H_k] array whose entries
+    all differ: unit (b, g) must use entry [b, g]."""
+    w = _small(seq_lens=[5, 21, 9], num_seqs=3, h_q=4, h_k=2)
+    ks = np.array([[0.5, 0.75], [1.25, 2.0], [3.0, 0.375]]) * 0.01
+    vs = np.array([[2.0, 0.25], [0.625, 1.5], [0.875, 4.0]]) * 0.01
+    codes, desc = quantize_q(w.q_f32, w.num_seqs, w.q_len, w.h_q, w.h_k, w.d, w.q_mul)
+    out, _ = A.decode_attention(codes, desc, w.logical("k"), w.logical("v"), ks, vs, w.block_table, w.seq_lens,
+                                num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
+                                page_size=w.page_size, kv_format=w.kv_format, softmax_scale=w.softmax_scale,
+                                causal=w.causal)
+    for b in range(w.num_seqs):
+        for g in range(w.h_k):
+            bf = A.brute_force_unit(codes[b, g], float(desc[b, g]), w.logical("k"), w.logical("v"), ks[b][g],
+                                    vs[b][g], w.block_table, b, g, int(w.seq_lens[b]), w.page_size, w.kv_format,
+                                    w.softmax_scale, w.q_len, w.h_r, w.causal)
+            np.testing.assert_allclose(out[b, g * w.h_r:(g + 1) * w.h_r], bf, rtol=1e-10, atol=1e-12)
 
 def test_paged_equals_contiguous_and_page_permutation():
     """The same tokens scattered over random pages of a larger pool, or laid

@@ -337,6 +337,115 @@ def _kvwrite(kind: str):
     W.write_kv = write_kv
 
 
+
+# ----------------------------------------------------------------------------
+# second batch: causal flag, o_mul index, split partials, encoders' signs and
+# ties, code bit order, plan helpers, Q division and scale, cache-write scales
+# ----------------------------------------------------------------------------
+def _causal_ignored():
+    orig = A.visible_mask
+    A.visible_mask = lambda L, q_len, h_r, causal: orig(L, q_len, h_r, False)
+
+
+def _o_mul_by_kv_head():
+    orig = A.decode_attention
+
+    def decode_attention(*args, **kw):
+        om = kw.get("o_mul")
+        if om is not None:
+            om = np.asarray(om)
+            h_r = kw["h_q"] // kw["h_k"]
+            kw["o_mul"] = om[np.arange(kw["h_q"]) // h_r]  # row g of a query-head array
+        return orig(*args, **kw)
+    A.decode_attention = decode_attention
+
+
+def _chunk_unnormalised():
+    def chunk_partial(s, vis, v, a, e):
+        n_q = s.shape[0]
+        if e <= a:
+            return np.full(n_q, -np.inf), np.zeros(n_q), np.zeros((n_q, v.shape[1]))
+        m, l, p = A.softmax_rows(s[:, a:e], vis[:, a:e])
+        return m, l, p @ v[a:e]
+    A.chunk_partial = chunk_partial
+
+
+def _e4m3_sign_dropped():
+    orig = F.e4m3_encode
+    F.e4m3_encode = lambda x: orig(np.abs(np.asarray(x, dtype=np.float64)))
+
+
+def _ties_away_encoder(pos_values, sign_bit):
+    def encode(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.abs(x)
+        n = len(pos_values)
+        i = np.clip(np.searchsorted(pos_values, a, side="right") - 1, 0, n - 1)
+        j = np.minimum(i + 1, n - 1)
+        code = np.where(2.0 * a >= pos_values[i] + pos_values[j], j, i)
+        code = np.where(i >= n - 1, n - 1, code).astype(np.uint8)
+        return np.where(np.signbit(x), code | sign_bit, code).astype(np.uint8)
+    return encode
+
+
+def _fp6_code_bits_reversed():
+    unpack, pack = F.fp6_unpack_rows, F.fp6_pack_rows
+    rev = np.array([int(f"{c:06b}"[::-1], 2) for c in range(64)], dtype=np.uint8)
+    F.fp6_unpack_rows = lambda packed: rev[unpack(packed)]
+    F.fp6_pack_rows = lambda codes: pack(rev[np.asarray(codes, dtype=np.uint8) & 0x3F])
+
+
+def _plan_helper(kind: str):
+    if kind == "tile_width_base_8":
+        def tile_width(n_q, fp8_q):
+            p = 1
+            while p < n_q:
+                p *= 2
+            return max(8, min(32, p))
+        P.tile_width = tile_width
+    elif kind == "slots_ignore_row_tiles":
+        P.slots = lambda sm_count, ctas_per_sm, h_k, n_row_tiles: max(1, (sm_count * ctas_per_sm) // h_k)
+
+
+def _q_copy(kind: str):
+    def quantize_q(q_f32, num_seqs, q_len, h_q, h_k, d, q_mul=None):
+        h_r = h_q // h_k
+        x = np.asarray(q_f32, dtype=np.float32)[: num_seqs * q_len].copy()
+        if q_mul is not None:
+            x = (x * np.asarray(q_mul, dtype=np.float32).reshape(1, h_q, d)).astype(np.float32)
+        x = x.reshape(num_seqs, q_len, h_k, h_r, d)
+        if kind == "amax_head0":
+            amax = np.abs(x[:, :, :, :1]).max(axis=(1, 3, 4)).astype(np.float32)
+        else:
+            amax = np.abs(x).max(axis=(1, 3, 4)).astype(np.float32)
+        if kind == "floor_on_scale":  # the floor applied to the scale itself
+            scale = np.maximum((amax / Q.FP8_MAX).astype(np.float32), Q.AMAX_FLOOR)
+        else:
+            scale = (np.maximum(amax, Q.AMAX_FLOOR) / Q.FP8_MAX).astype(np.float32)
+        sb = scale[:, None, :, None, None]
+        if kind == "reciprocal":
+            y = (x * (np.float32(1.0) / sb).astype(np.float32)).astype(np.float32)
+        else:
+            y = (x / sb).astype(np.float32)
+        codes = Q.e4m3_encode(y).transpose(0, 2, 1, 3, 4).reshape(num_seqs, h_k, q_len * h_r, d)
+        return np.ascontiguousarray(codes), scale
+    Q.quantize_q = quantize_q
+
+
+def _write_head0_scale():
+    orig = W.quantize_rows
+
+    def quantize_rows(x, scale, kv_format):
+        s = np.asarray(scale, dtype=np.float32)
+        if s.size > 1:  # every head takes head 0's scale(s)
+            s = np.broadcast_to(s[:1], s.shape).copy()
+        return orig(x, s, kv_format)
+    W.quantize_rows = quantize_rows
+
+
+def _write_e2m3_ties_away():
+    W.e2m3_encode = _ties_away_encoder(F.E2M3_TABLE[:0x20].copy(), 0x20)
+
 PLANTS = {
     # name: (install, pin module that must catch it)
     "causal_mask_strict": (lambda: _mask(True, False), ATTN),
@@ -375,6 +484,19 @@ PLANTS = {
     "write_scale_multiplied": (lambda: _kvwrite("scale_multiplied"), KVW),
     "write_slot_swapped": (lambda: _kvwrite("slot_swapped"), KVW),
     "write_padding_token": (lambda: _kvwrite("padding_written"), KVW),
+    "causal_flag_ignored": (_causal_ignored, ATTN),
+    "o_mul_row_by_kv_head": (_o_mul_by_kv_head, ATTN),
+    "split_partial_not_normalised": (_chunk_unnormalised, ATTN),
+    "e4m3_sign_dropped": (_e4m3_sign_dropped, FMT),
+    "e2m3_ties_away": (lambda: setattr(F, "e2m3_encode", _ties_away_encoder(F._E2M3_POS, 0x20)), FMT),
+    "fp6_code_bits_reversed": (_fp6_code_bits_reversed, FMT),
+    "plan_tile_width_base_8": (lambda: _plan_helper("tile_width_base_8"), PLAN),
+    "plan_slots_ignore_row_tiles": (lambda: _plan_helper("slots_ignore_row_tiles"), PLAN),
+    "q_reciprocal_multiply": (lambda: _q_copy("reciprocal"), QQ),
+    "q_amax_first_query_head_only": (lambda: _q_copy("amax_head0"), QQ),
+    "q_floor_on_the_scale": (lambda: _q_copy("floor_on_scale"), QQ),
+    "write_every_head_uses_head0_scale": (_write_head0_scale, KVW),
+    "write_e2m3_ties_away": (_write_e2m3_ties_away, KVW),
 }
 
 

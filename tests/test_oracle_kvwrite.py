@@ -99,6 +99,34 @@ def test_narrow_representable_rows_are_exact():
 
 
 @pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3, W.KV_E3M2, W.KV_E2M1])
+def test_rows_at_exact_midpoints_round_to_the_even_code(kv_format):
+    """x / scale exactly halfway between two adjacent values of the format
+    (power-of-two scales keep the quotient exact) is written as the code whose
+    mantissa LSB is 0, for both signs and every adjacent pair."""
+    table, n, sign, unpack = {W.KV_E4M3: (F.E4M3_TABLE, 0x7F, 0x80, None),
+                              W.KV_E2M3: (F.E2M3_TABLE, 0x20, 0x20, F.fp6_unpack_rows),
+                              W.KV_E3M2: (F.E3M2_TABLE, 0x20, 0x20, F.fp6_unpack_rows),
+                              W.KV_E2M1: (F.E2M1_TABLE, 0x8, 0x8, F.fp4_unpack_rows)}[kv_format]
+    mids = (table[: n - 1] + table[1:n]) / 2.0  # between codes i and i + 1
+    want = np.array([i if i % 2 == 0 else i + 1 for i in range(n - 1)], dtype=np.uint8)
+    vals = np.concatenate([mids, -mids])
+    want = np.concatenate([want, want | sign])
+    reps = -(-len(vals) // D)
+    y = np.resize(vals, reps * HK * D).reshape(reps, HK, D)
+    w = np.resize(want, reps * HK * D).reshape(reps, HK, D)
+    if kv_format == W.KV_E4M3:
+        scale = np.array([2.0 ** -5, 2.0 ** 2], dtype=np.float32)
+        x = (y * scale.reshape(1, HK, 1)).astype(np.float32)
+        codes = W.quantize_rows(x, scale, kv_format)
+    else:
+        scale = (2.0 ** (np.arange(HK * D).reshape(HK, D) % 7 - 3)).astype(np.float32)
+        x = (y * scale).astype(np.float32)
+        codes = unpack(W.quantize_rows(x, scale, kv_format))
+    assert np.array_equal(x.astype(np.float64) / (scale.reshape(1, HK, 1) if kv_format == W.KV_E4M3 else scale), y)
+    assert np.array_equal(codes, w)
+
+
+@pytest.mark.parametrize("kv_format", [W.KV_E4M3, W.KV_E2M3, W.KV_E3M2, W.KV_E2M1])
 def test_written_rows_are_within_half_a_step(kv_format):
     rng = np.random.default_rng(14)
     x = (rng.standard_normal((64, HK, D)) * 3).astype(np.float32)

@@ -20,6 +20,12 @@ def test_n_tiles_and_slots():
     assert P.slots(20, 2, 8, 1) == 5  # the pages' Thor: one wave of 2 x 20 CTAs over 8 heads
     assert P.slots(152, 2, 8, 1) == 38
     assert P.slots(10, 1, 64, 1) == 1  # never below one
+    # more query rows than one 32-row tile: the slots are shared by the row tiles
+    assert P.slots(152, 2, 8, 2) == 19 and P.slots(152, 2, 8, 3) == 12
+    p = P.plan_split_kv([4096] * 18, 18, 8, 64, 8, 152, 2, 16, 0, 64)  # 8 x 8 = 64 rows: 2 tiles
+    assert P.n_tiles(8, 8) == 2 and p.slots == 19 and p.with_reduction  # 18 requests < 19 slots
+    p = P.plan_split_kv([4096] * 19, 19, 8, 64, 8, 152, 2, 16, 0, 64)
+    assert p.slots == 19 and not p.with_reduction
 
 
 def _check_plan(p, lens, margin, num_seqs, pad_to, max_splits, slots):

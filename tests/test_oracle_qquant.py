@@ -53,6 +53,27 @@ def test_scale_is_correctly_rounded_quotient():
     assert np.array_equal(scale, want)
 
 
+def test_codes_use_a_true_division_not_a_reciprocal_multiply():
+    """Hand-worked case where x / scale and x * (1/scale) round apart.
+
+    The amax element 3136 gives scale = 3136 / 448 = 7 exactly. For
+    x = 12.6875 the IEEE float32 quotient is exactly 1.8125, the midpoint of
+    the e4m3 values 1.75 (mantissa 6, even) and 1.875, so ties-to-even gives
+    1.75 (code 0x3E; 0xBE for -x). float32(1/7) is 1/7 * (1 + 4.5e-8), and
+    12.6875 * float32(1/7) rounds to 1.8125 + 2^-23, which would give 1.875.
+    All three inputs are exact in bf16."""
+    B, ql, h_q, h_k, d = 1, 1, 2, 1, 128
+    q = np.zeros((1, h_q, d), np.float32)
+    q[0, 0, 0] = 3136.0
+    q[0, 0, 1] = 12.6875
+    q[0, 1, 5] = -12.6875
+    codes, scale = quantize_q(q, B, ql, h_q, h_k, d)
+    assert scale[0, 0] == np.float32(7.0)
+    assert codes[0, 0, 0, 0] == 0x7E
+    assert codes[0, 0, 0, 1] == 0x3E
+    assert codes[0, 0, 1, 5] == 0xBE
+
+
 def test_every_code_is_the_nearest_e4m3_value():
     """Independent of the encoder: search all finite codes for the nearest
     value to x/scale and break ties towards the even code."""

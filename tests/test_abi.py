@@ -248,3 +248,45 @@ def test_bf16_q_mode_host_checks(lib):
     a.q_head_stride = 128
     a.kv_format = mj.MJ_KV_E2M3  # e2m3 KV is fp8-Q only
     assert lib.mj_decode_attention(ctypes.byref(a), None) == mj.MJ_ERR_UNSUPPORTED
+
+
+def test_missing_library_fails_loudly(lib):
+    """No CPU or library fallback: without libmj.so the binding raises."""
+    saved = mj._lib
+    try:
+        mj._lib = None
+        with pytest.raises(RuntimeError, match="no CPU or library fallback"):
+            mj.load_library(os.path.join(ROOT, "no_such_dir", "libmj.so"))
+    finally:
+        mj._lib = saved
+
+
+def test_product_path_never_imports_the_oracle():
+    """The package (binding, step helpers, build, CUDA sources) names no
+    oracle module, and importing it loads none."""
+    pkg = os.path.join(ROOT, "paged_fp8_decode_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b|#include\s+[<\"].*oracle", src, re.M), f
+    import subprocess
+    import sys
+
+    code = ("import sys, paged_fp8_decode_gb300, paged_fp8_decode_gb300.step, paged_fp8_decode_gb300.build; "
+            "print(sorted(m for m in sys.modules if m == 'oracle' or m.startswith('oracle.')))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "[]"
+
+
+def test_noalloc_rejects_oversized_plans_on_the_host(lib):
+    """The allocation-free call checks its fixed scratch before touching the
+    device: a plan whose partials exceed it is refused with MJ_ERR_CAPACITY."""
+    a = mj.mj_decode_args()
+    a.num_seqs, a.q_len, a.h_q, a.h_k, a.d = 8, 1, 32, 8, 128
+    a.with_reduction, a.max_splits, a.part_seqs = 1, 64, 1000
+    need = mj.mj_workspace_size(1000, 64, 1, 32, 8, 128)
+    assert need > mj.NOALLOC_SCRATCH_BYTES
+    assert lib.mj_decode_attention_noalloc(ctypes.byref(a), None) == mj.MJ_ERR_CAPACITY
+    assert lib.mj_decode_attention_noalloc(None, None) == mj.MJ_ERR_INVALID_ARG

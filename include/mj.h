@@ -275,11 +275,12 @@ MJ_API int mj_workspace_status(void* workspace, void* stream, uint32_t* device_s
  * Reads each valid KV row once. For a work row (b, tb, te, s) and KV head g
  * it covers keys [tb*128, min(te*128, seq_lens[b])) and all q_len*h_r query
  * rows of (b, g):
- *   - if !with_reduction or n_splits[b] == 1: writes the final bf16 output
+ *   - if !with_reduction or n_splits[b] == 1: writes the final output (bf16 or fp16, out_dtype)
  *     O * v_descale * o_mul and, if lse != NULL, the row LSE;
  *   - else writes its normalised partial (O~, m, l) into the workspace.
  * Rows of requests with seq_lens[b] == 0 and empty work rows write nothing.
- * Grid: num_work x h_k x n_row_tiles, fixed by the arguments.
+ * Grid: num_work x h_k x n_row_tiles CTAs (the tensor-core kernel orders
+ * them KV head fastest), fixed by the arguments.
  * ---------------------------------------------------------------------- */
 MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
 
@@ -289,7 +290,8 @@ MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
  * split-KV partials by LSE"). For each request b with n_splits[b] > 1 and
  * seq_lens[b] > 0, KV head g and query row:
  *   M = max_s m_s;  w_s = 2^(m_s - M) * l_s (0 for empty splits);
- *   O = sum_s w_s O~_s / sum_s w_s, times v_descale and o_mul, rounded to bf16.
+ *   O = sum_s w_s O~_s / sum_s w_s, times v_descale and o_mul, rounded to the output type
+ *   (bf16 or fp16, out_dtype; to nearest even).
  * Splits whose first key is at or past seq_lens[b] are empty and skipped.
  * A no-op when args->with_reduction == 0. Same argument struct as
  * mj_decode_attention (it reads the partials that call left in the workspace).

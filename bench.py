@@ -68,6 +68,14 @@ def kv_row_bytes(w) -> int:
     return {"fp8": w.d, "e2m3": w.d * 3 // 4, "e3m2": w.d * 3 // 4, "e2m1": w.d // 2}[w.kv_format]
 
 
+def kv_bytes_per_step(w) -> int:
+    """The metric's algorithmic bytes: every valid token's K and V row of
+    every KV head, read once."""
+    import numpy as np
+
+    return int(np.asarray(w.seq_lens, dtype=np.int64).sum()) * w.h_k * 2 * kv_row_bytes(w)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -443,8 +451,7 @@ def main_ours(args):
     stream = torch.cuda.current_stream(dev)
     info = step.plan(w.seq_lens, w.num_seqs, stream)
     a = step.args(kv, out, w.num_seqs, w.softmax_scale, q=q)
-    row = kv_row_bytes(w)
-    kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.h_k * 2 * row
+    kv_bytes = kv_bytes_per_step(w)
     tokens = int((w.seq_lens > 0).sum()) * w.q_len
     launches_per_step = (1 if args.q_mode == "fp8" else 0) + 1 + (1 if info["with_reduction"] else 0)
 

@@ -446,6 +446,58 @@ def _write_head0_scale():
 def _write_e2m3_ties_away():
     W.e2m3_encode = _ties_away_encoder(F.E2M3_TABLE[:0x20].copy(), 0x20)
 
+
+# ----------------------------------------------------------------------------
+# third batch: bf16-Q rows, format dispatch, merge LSE, bf16 rounding, the
+# bf16-Q tile width, write row bytes, the non-causal flag
+# ----------------------------------------------------------------------------
+def _pack_q_head_major():
+    orig = Q.pack_q_rows
+
+    def pack_q_rows(q_f32, num_seqs, q_len, h_q, h_k, d):
+        rows = orig(q_f32, num_seqs, q_len, h_q, h_k, d)
+        h_r = h_q // h_k
+        r = rows.reshape(num_seqs, h_k, q_len, h_r, d).transpose(0, 1, 3, 2, 4)
+        return np.ascontiguousarray(r).reshape(num_seqs, h_k, q_len * h_r, d)
+    Q.pack_q_rows = pack_q_rows
+
+
+def _e3m2_decoded_as_e2m3():
+    orig = A.decode_codes
+    A.decode_codes = lambda codes, kv_format: orig(codes, "e2m3" if kv_format == "e3m2" else kv_format)
+
+
+def _merge_lse_log2():
+    orig = A.merge_partials
+
+    def merge_partials(ms, ls, os_):
+        o, lse = orig(ms, ls, os_)
+        return o, lse / np.log(2.0)
+    A.merge_partials = merge_partials
+
+
+def _bf16_truncates():
+    def to_bf16(x):
+        x = np.asarray(x, dtype=np.float64)
+        m, e = np.frexp(x)
+        return np.ldexp(np.trunc(m * 256.0), e - 8)
+    A.to_bf16 = to_bf16
+
+
+def _tile_width_bf16_as_fp8():
+    orig = P.tile_width
+    P.tile_width = lambda n_q, fp8_q: orig(n_q, True)
+
+
+def _write_e2m1_row_as_fp6():
+    orig = W.row_bytes
+    W.row_bytes = lambda d, kv_format: d * 3 // 4 if kv_format == W.KV_E2M1 else orig(d, kv_format)
+
+
+def _noncausal_as_causal():
+    orig = A.visible_mask
+    A.visible_mask = lambda L, q_len, h_r, causal: orig(L, q_len, h_r, True)
+
 PLANTS = {
     # name: (install, pin module that must catch it)
     "causal_mask_strict": (lambda: _mask(True, False), ATTN),
@@ -497,6 +549,13 @@ PLANTS = {
     "q_floor_on_the_scale": (lambda: _q_copy("floor_on_scale"), QQ),
     "write_every_head_uses_head0_scale": (_write_head0_scale, KVW),
     "write_e2m3_ties_away": (_write_e2m3_ties_away, KVW),
+    "bf16_q_rows_head_major": (_pack_q_head_major, ATTN),
+    "e3m2_decoded_as_e2m3": (_e3m2_decoded_as_e2m3, ATTN),
+    "merge_lse_in_log2": (_merge_lse_log2, ATTN),
+    "bf16_rounding_truncates": (_bf16_truncates, ATTN),
+    "plan_bf16_q_tile_width_as_fp8": (_tile_width_bf16_as_fp8, PLAN),
+    "write_e2m1_row_bytes_as_fp6": (_write_e2m1_row_as_fp6, KVW),
+    "noncausal_block_masked_as_causal": (_noncausal_as_causal, ATTN),
 }
 
 

@@ -299,3 +299,31 @@ def test_fused_quantize_full_size():
     a = run_gpu(w, impl=2, **FULL["qwen3_8b_decode"])
     b = run_gpu(w, impl=2, q_mode="fp8_fused", **FULL["qwen3_8b_decode"])
     assert np.array_equal(a["out"], b["out"]) and b["status"] == 0
+
+
+def _tie_case():
+    """The tiny workload with request 0's Q replaced by a hand-worked case:
+    the amax element 3136 gives the descale 3136 / 448 = 7 exactly, and
+    x = 12.6875 divides to exactly 1.8125, the midpoint of the e4m3 values
+    1.75 (even mantissa) and 1.875. A true division rounds it to 1.75 (code
+    0x3E, 0xBE for -x); a multiply by float32(1/7) would give 1.875."""
+    w = synth.tiny()
+    q = np.zeros_like(w.q_f32)
+    q[0, 0, 0], q[0, 0, 1], q[0, 1, 5] = 3136.0, 12.6875, -12.6875
+    q[w.q_len:] = w.q_f32[w.q_len:]  # request 1 keeps its ordinary values
+    w.q_f32 = q.astype(np.float32)
+    w.q_bits = (w.q_f32.view(np.uint32) >> 16).astype(np.uint16)  # exact: every value is a bf16 value
+    return w
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_quantize_q_rounds_a_true_quotient_at_an_e4m3_tie(impl):
+    w = _tie_case()
+    ref, ref_lse, codes, desc = run_oracle(w)
+    assert desc[0, 0] == np.float32(7.0) and codes[0, 0, 0, 1] == 0x3E and codes[0, 0, 1, 5] == 0xBE
+    a = run_gpu(w, impl=impl)  # mj_quantize_q, then the decode kernel
+    assert np.array_equal(a["q_codes"], codes) and np.array_equal(a["q_descale"], desc)
+    compare(w, a["out"], ref, all_units(w), "e4m3 tie in Q")
+    b = run_gpu(w, impl=impl, q_mode="fp8_fused")  # the decode kernel quantizes Q itself
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+    assert a["status"] == 0 and b["status"] == 0

@@ -77,7 +77,7 @@ typedef enum mj_kv_format {
  *   MJ_Q_FP8       — the e4m3 codes and per-(request, KV head) descales
  *                    mj_quantize_q wrote;
  *   MJ_Q_BF16      — the bf16 Q as is (e4m3 KV only, as on the runner page:
- *                    packed e2m3 is "fp8 Q only"; the same for e3m2 / e2m1);
+ *                    packed e2m3 takes fp8 Q only; the same for e3m2 / e2m1);
  *   MJ_Q_FP8_FUSED — the bf16 Q, quantized by the decode kernel itself with
  *                    mj_quantize_q's recipe (same codes, same descales), so
  *                    the step needs no separate quantize launch. */
@@ -90,7 +90,7 @@ typedef enum mj_out_dtype { MJ_OUT_BF16 = 0, MJ_OUT_F16 = 1 } mj_out_dtype;
  * whenever its preconditions hold, else the CUDA-core kernel. */
 typedef enum mj_impl { MJ_IMPL_AUTO = 0, MJ_IMPL_SIMT = 1, MJ_IMPL_TCGEN05 = 2 } mj_impl;
 
-#define MJ_KV_TILE 128 /* tokens per KV tile: the plan's unit ("128-row KV tiles") */
+#define MJ_KV_TILE 128 /* tokens per KV tile: the unit the plan counts KV in */
 
 /* Human-readable name of a status code (static storage). */
 MJ_API const char* mj_status_string(int status);
@@ -329,7 +329,7 @@ MJ_API int mj_decode_attention_noalloc(const mj_decode_args* args, void* stream)
  * slot_mapping. Source: MjolnirImpl.do_kv_cache_update / _write_kv on the
  * mjolnir/backend.py page (the e4m3 write takes the layer's k/v scale; the
  * packed e2m3 write takes the per-(KV head, channel) scales that
- * _install_fp6_scales says "quantize the cache write").
+ * _install_fp6_scales applies when the cache is written).
  *
  * For token t and KV head g with s = slot_mapping[t] >= 0, the row goes to
  * page s / page_size, row s % page_size of the cache (the decode call's

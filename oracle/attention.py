@@ -36,7 +36,7 @@ Readings where the pages are silent (each listed in the design notes):
 * ``softmax_scale`` is an input (the backend passes the layer's scale);
   the workloads use ``1/sqrt(D)``.
 
-Split-KV (README item 4: "combines the split-KV partials by LSE"): a chunk
+Split-KV (README item 4: a second kernel merges the split partials by their LSE): a chunk
 ``[a, e)`` of the keys yields ``m`` (max logit), ``l`` (sum of
 ``exp(s - m)``) and the normalised partial ``O~ = sum p v / l``; chunks merge
 as ``O = sum_s w_s O~_s / sum_s w_s``, ``w_s = exp(m_s - M) * l_s``,
@@ -144,7 +144,7 @@ def decode_attention(q_codes, q_descale, k_logical, v_logical, k_descale, v_desc
                      o_mul=None, units=None, q_values=False):
     """Full decode step.
 
-    ``q_values`` (the runner's bf16 Q mode, "Q as is"): ``q_codes`` holds the
+    ``q_values`` (the runner's bf16 Q mode, Q left unquantized): ``q_codes`` holds the
     query values in the packed row order (:func:`oracle.qquant.pack_q_rows`)
     and ``q_descale`` is not used.
 

@@ -10,8 +10,8 @@ Sources on the ``mjolnir/runner.py`` page: ``tile_width``;
 pad_to)``, ``with_reduction = max_splits > 1 and num_seqs < slots``, a work
 row ``w`` is non-empty iff ``w[2] > w[1]``). The README ("A decode step",
 item 1) states the aim: exactly one wave of ``ctas_per_sm`` CTAs per SM. KV
-tiles are 128 tokens (the "128-row KV tiles" of ``l2_prefetch`` in the
-runner's constructor).
+tiles are 128 tokens (the tile length ``l2_prefetch`` names in the runner's
+constructor).
 
 The body of ``plan_split_kv`` is not on the pages. Reading (the plainest
 algorithm consistent with the call site and the reduction rule):

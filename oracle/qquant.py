@@ -61,7 +61,7 @@ def quantize_q(q_f32, num_seqs: int, q_len: int, h_q: int, h_k: int, d: int, q_m
 
 
 def pack_q_rows(q_f32, num_seqs: int, q_len: int, h_q: int, h_k: int, d: int) -> np.ndarray:
-    """The bf16-Q mode (``q_mode="bf16"`` of ``T5DecodeRunner``: "Q as is"):
+    """The bf16-Q mode (``q_mode="bf16"`` of ``T5DecodeRunner``: Q unquantized):
     the query values themselves, in the same packed row order as the codes
     (``[B, h_k, q_len*h_r, d]``, row ``t*h_r + r``), as float64."""
     q = np.asarray(q_f32, dtype=np.float64)[: num_seqs * q_len]

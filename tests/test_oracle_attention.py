@@ -223,7 +223,7 @@ def test_bf16_rounding():
 
 
 # ----------------------------------------------------------------------------
-# the bf16-Q mode ("Q as is")
+# the bf16-Q mode (Q left unquantized)
 # ----------------------------------------------------------------------------
 def _run_bf16(w, units=None):
     from oracle.qquant import pack_q_rows

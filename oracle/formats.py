@@ -13,8 +13,9 @@ Test infrastructure only (see :mod:`oracle`).
   bits; exponent field 0 is subnormal (``m/8``); no NaN and no infinity; the
   largest magnitude is ``1.875 * 2**2 = 7.5`` (the 7.5 in the fallback
   descale of ``_install_fp6_scales`` on the ``mjolnir/backend.py`` page).
-* **packing**: the ``VariantKey`` comment on the runner page says e2m3 codes
-  are packed "4 per 3 bytes" as a "little-endian bitstream". Reading: code
+* **packing**: the ``VariantKey`` comment on the runner page packs four e2m3
+  codes into every three bytes and reads them as a little-endian stream of
+  bits. Reading: code
   ``i`` of a row occupies bits ``[6*i, 6*i+6)`` of the row's bytes read as one
   little-endian integer, bit 0 being the least significant bit of byte 0.
   A row of ``d`` codes is ``d*6/8`` bytes (``kv_row_bytes`` in

@@ -24,16 +24,16 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
  *    Device calls only enqueue work on it; argument errors are detected on
  *    the host before anything is enqueued.
- *  - Device pointers must be 16-byte aligned ("T5 kernel needs 16-byte
- *    aligned base pointers", _ptr on the mjolnir/runner.py page); packed
+ *  - Device pointers must be 16-byte aligned (the runner page's _ptr
+ *    rejects other base pointers); packed
  *    (e2m3, e3m2, e2m1) K/V bases must be 32-byte aligned (T5DecodeRunner._kv_ptr).
  *  - Q and O strides are in ELEMENTS; K/V strides are in BYTES, so e4m3 and
  *    packed e2m3 caches share one convention.
  *  - Launch shapes depend only on the arguments (the grid is the plan's
  *    padded num_work), never on device data, so a step can be captured in a
  *    CUDA graph and replayed with new plans written into the same buffers
- *    (runner page, module docstring: "FIXED-ADDRESS device buffers ...
- *    padded to a FIXED grid size per q_len -> CUDA-graph safe").
+ *    (runner page, module docstring: the plan lives in fixed-address
+ *    device buffers padded to a fixed grid per q_len, so graphs stay valid).
  */
 #ifndef MJ_H
 #define MJ_H
@@ -177,7 +177,7 @@ typedef struct mj_decode_args {
   int h_q, h_k;   /* query heads, KV heads; h_q % h_k == 0 */
   int d;          /* head size: 128 or 256 (packed formats at 256: CUDA-core kernel only) */
   int causal;     /* 1: query t sees key j iff j <= seq_len - q_len + t;
-                     0: every query token sees every key (README "What it does") */
+                     0: each query token attends to all keys (README "What it does") */
   float softmax_scale;
 
   /* quantized Q (mj_quantize_q outputs; q_mode MJ_Q_FP8, else unused) */
@@ -286,8 +286,8 @@ MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
 
 /* ------------------------------------------------------------------------
  * mj_merge_lse — combine split-KV partials by log-sum-exp.
- * Source: README "A decode step" item 4 ("a small second kernel combines the
- * split-KV partials by LSE"). For each request b with n_splits[b] > 1 and
+ * Source: README "A decode step" item 4 (a separate, small kernel merges
+ * the split-KV partials by their LSE). For each request b with n_splits[b] > 1 and
  * seq_lens[b] > 0, KV head g and query row:
  *   M = max_s m_s;  w_s = 2^(m_s - M) * l_s (0 for empty splits);
  *   O = sum_s w_s O~_s / sum_s w_s, times v_descale and o_mul, rounded to the output type

@@ -16,9 +16,9 @@ query row ``row = t*h_r + r`` (query token ``t < q_len``, query head
 * ``s_j = softmax_scale * q_descale[b,g] * sum_c qcode[row,c] * k[j,c]``
   using the QUANTIZED Q codes (the kernel never sees bf16 Q);
 * visible keys: causal -> ``j <= L - q_len + t`` (the query block is the last
-  ``q_len`` tokens of the sequence); non-causal -> every ``j < L`` ("every
-  query token sees every key", README "What it does", the parallel-drafter
-  block);
+  ``q_len`` tokens of the sequence); non-causal -> every ``j < L`` (each
+  query token attends to all keys: README "What it does", the
+  parallel-drafter block);
 * ``O[row] = sum_j p_j v_j / sum_j p_j`` with ``p_j = exp(s_j - max s)``;
   then ``O[row, c] *= o_mul[h, c]`` when given (fp6 V channel scales,
   ``_install_fp6_scales`` on the ``mjolnir/backend.py`` page);

@@ -17,8 +17,8 @@ Sources:
   ``k_scale`` in ``T5DecodeRunner.run``).
 * **e2m3 cache** -- ``MjolnirImpl.do_kv_cache_update`` calls the package's
   own packed write with the per-(KV head, channel) scales ``k_ch`` /
-  ``v_ch`` of ``_install_fp6_scales``; the scales "quantize the cache
-  write". Reading: ``code = e2m3(x / s[h, c])`` (round-to-nearest-even,
+  ``v_ch`` of ``_install_fp6_scales``, the scales the cache is written
+  with. Reading: ``code = e2m3(x / s[h, c])`` (round-to-nearest-even,
   saturating at 7.5), the row's codes packed 4 per 3 bytes
   (:func:`oracle.formats.fp6_pack_rows`).
 * **e3m2 / e2m1 caches** -- the README names these formats beside e2m3 and

@@ -40,8 +40,9 @@ KV_TILE = 128
 
 
 def tile_width(n_q: int, fp8_q: bool) -> int:
-    """Rows per CTA tile: next power of two >= n_q, at least 16 (fp8 Q) or 8
-    (bf16 Q), at most 32 (``tile_width`` docstring, runner page)."""
+    """The query rows one CTA takes: the smallest power of two that holds
+    ``n_q``, clamped to [16, 32] with fp8 Q and to [8, 32] with bf16 Q
+    (``tile_width`` on the runner page)."""
     base = 16 if fp8_q else 8
     p = 1
     while p < n_q:

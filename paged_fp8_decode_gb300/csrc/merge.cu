@@ -1,18 +1,17 @@
 // mj_merge_lse kernel: combine split-KV partials by log-sum-exp.
 //
-// README of the mjolnir-kernel package, "A decode step" item 4: a small
-// second kernel combines the split-KV partials by LSE. A partial row holds
-// the split's normalised output O~ (float32, d channels), its max logit m
-// (log2 domain) and its sum l = sum 2^(t - m). For request b, KV head g and
-// query row: M = max_s m_s, w_s = 2^(m_s - M) l_s, O = sum w_s O~_s / sum w_s.
+// README of the mjolnir-kernel package, "A decode step" item 4: the split
+// partials are merged by their log-sum-exp in a kernel of their own. A
+// partial row holds the split's normalised output O~ (float32, d channels),
+// its max logit m (log2 domain) and its sum l = sum 2^(t - m). For request b,
+// KV head g and query row: M = max_s m_s, w_s = 2^(m_s - M) l_s, O = sum w_s O~_s / sum w_s.
 // Splits that start at or past seq_lens[b] (a plan made from an upper bound)
 // and rows with no visible key in a split (m = -inf, l = 0) weigh zero; the
 // exponent is never formed from two infinities.
 //
 // One CTA per (request, KV head, query row), one thread per channel (D = 128
-// or 256): the
-// split weights are computed by as many threads in parallel, and the channel
-// sums read the partials with independent, coalesced loads.
+// or 256): the split weights are computed by as many threads in parallel,
+// and the channel sums read the partials with independent, coalesced loads.
 #include "mj_device.cuh"
 #include "mj_internal.h"
 

@@ -1,10 +1,10 @@
 """A fused multi-step draft decode: one plan, several steps, one CUDA graph.
 
 The mjolnir/backend.py page (MjolnirMetadataBuilder.__init__) describes the
-speculative drafter's loop: the draft metadata is built once and every draft
-step runs on it while the device seq_lens advance in place. A plan stays
-valid across those steps if it is made with num_speculative_tokens of
-headroom (``margin``), because the kernel masks with the live lengths.
+speculative drafter's loop: one set of draft metadata serves all of the
+drafter's steps, and the device sequence lengths grow in place from step to
+step. So the plan is made with num_speculative_tokens of headroom
+(``margin``), and the kernel masks with the current device lengths.
 
 Here each of K draft steps writes its new token's K/V rows into the cache
 (mj_write_kv), advances the device lengths by one, and runs quantize, decode

@@ -96,11 +96,27 @@ KERNEL_SOURCES = {
 }
 
 
-def _kernel_source_hash(name: str) -> str:
+def _code_only(src: str) -> str:
+    """C/CUDA source with comments removed and whitespace runs collapsed: a
+    change to a comment does not change the compiled kernel or its counters.
+    (The kernel sources hold no string literal with a comment marker.)"""
+    import re
+
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def _kernel_source_hash(name: str, read=None) -> str:
+    """Hash of the code (not the comments) of every file the kernel is built from."""
     h = hashlib.sha256()
     for part in KERNEL_SOURCES.get(name, [name]):
-        with open(os.path.join(ROOT, "paged_fp8_decode_gb300", "csrc", part), "rb") as f:
-            data = f.read()
+        if read is None:
+            with open(os.path.join(ROOT, "paged_fp8_decode_gb300", "csrc", part), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(part)
+        data = _code_only(text).encode()
         h.update(part.encode() + b"\0" + len(data).to_bytes(8, "little") + data)
     return h.hexdigest()[:16]
 

@@ -5,7 +5,7 @@
  * One decode step is four calls, in the order the mjolnir-kernel README
  * lists them ("A decode step", items 1-4):
  *
- *   mj_plan_split_kv    (host)   occupancy-pinned split-KV work list
+ *   mj_plan_split_kv    (host)   split-KV work list sized to one wave of CTAs
  *   mj_quantize_q       (device) dynamic per-(request, KV head) e4m3 Q
  *   mj_decode_attention (device) stream KV pages through the block table,
  *                                online softmax, P.V
@@ -32,8 +32,9 @@
  *  - Launch shapes depend only on the arguments (the grid is the plan's
  *    padded num_work), never on device data, so a step can be captured in a
  *    CUDA graph and replayed with new plans written into the same buffers
- *    (runner page, module docstring: the plan lives in fixed-address
- *    device buffers padded to a fixed grid per q_len, so graphs stay valid).
+ *    (runner page, module docstring: the plan's buffers keep their
+ *    addresses and the grid keeps its size per q_len, so a captured graph
+ *    stays valid).
  */
 #ifndef MJ_H
 #define MJ_H
@@ -123,8 +124,8 @@ MJ_API int mj_slots(int sm_count, int ctas_per_sm, int h_k, int q_len, int h_q);
  *                  request-major
  *   padding rows (0, 0, 0, 0) up to pad_to (an empty row: end <= begin).
  *
- * seq_lens_host  [num_seqs] host int32 (exact lengths or an upper bound: the
- *                kernel masks with the exact device lengths).
+ * seq_lens_host  [num_seqs] host int32 (exact lengths or an upper bound:
+ *                masking always uses the true lengths in device memory).
  * pad_to         number of work rows = the decode grid's x extent; must be
  *                >= max(slots, num_seqs) (T5DecodeRunner.__init__: grid.x is
  *                max(slots, max_num_seqs)), else MJ_ERR_CAPACITY.

@@ -15,8 +15,8 @@ Sources (the mjolnir-kernel 0.1.0 pages):
   ``o_mul``), ``VariantKey`` comment on the packed fp6 format.
 * ``mjolnir/backend.py`` — ``_install_fp6_scales`` (channel scales folded
   into Q and into the output), ``_t5_q_len`` (trailing zero-token padding
-  requests), ``_seq_lens_cpu`` (planning on an upper bound; the kernel masks
-  with the exact device lengths).
+  requests), ``_seq_lens_cpu`` (planning on an upper bound; masking uses the
+  true lengths in device memory).
 * The package README ("A decode step", "fp6 (e2m3) KV in vLLM", "What it
   does") — causal vs. non-causal query blocks, the four steps of a decode
   step, split-KV partials merged by LSE.

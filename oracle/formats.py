@@ -22,8 +22,9 @@ Test infrastructure only (see :mod:`oracle`).
   ``T5DecodeRunner.__init__``).
 
 * **e3m2** (OCP FP6 E3M2) and **e2m1** (OCP FP4 E2M1): the other narrow KV
-  formats the package README lists ("Beyond fp8: the harness": fp6
-  ``e2m3``/``e3m2`` and fp4 ``e2m1``, read by ``tcgen05 kind::f8f6f4``). The
+  formats the package README lists in "Beyond fp8: the harness" (6-bit
+  ``e2m3`` and ``e3m2``, 4-bit ``e2m1``; tcgen05's ``kind::f8f6f4`` takes all
+  three). The
   pages name them only; the codecs are the OCP definitions. e3m2: 1 sign
   bit, 3 exponent bits with bias 3, 2 mantissa bits, subnormals ``m/4 *
   2**-2``, largest ``1.75 * 2**4 = 28``. e2m1: 1 sign bit, 2 exponent bits

@@ -80,8 +80,11 @@ def plan_split_kv(seq_lens, num_seqs: int, q_len: int, h_q: int, h_k: int, sm_co
     h_r = h_q // h_k
     nt = n_tiles(q_len, h_r, fp8_q)
     s = slots(sm_count, ctas_per_sm, h_k, nt)
-    lens = [int(x) + margin for x in list(seq_lens)[:num_seqs]]
-    t = [_ceil(L, KV_TILE) if L > 0 else 0 for L in lens]
+    # KV tiles of each request, counted on its length grown by the margin
+    t = []
+    for b in range(num_seqs):
+        grown = int(seq_lens[b]) + margin
+        t.append(_ceil(grown, KV_TILE) if grown > 0 else 0)
     with_reduction = max_splits > 1 and num_seqs < s
 
     work = []

@@ -10,9 +10,10 @@
 // accumulators in tensor memory, online softmax on CUDA cores.
 //
 // The README of the mjolnir-kernel package ("A decode step", item 3) describes
-// the shape of this design for Jetson Thor: TMA page loads into a ring with an
-// L2 evict-first hint, tcgen05 MMAs accumulating S and O in TMEM, softmax
-// warpgroups. This kernel is written for GB300 from that description:
+// the shape of this design for Jetson Thor: pages arrive by TMA in a
+// shared-memory ring (evicted first from L2), the tensor cores keep the
+// scores and the output in TMEM, and warpgroups do the softmax. This kernel is
+// written for GB300 from that description:
 //
 // * One CTA per (work row, KV head, query-row tile); 7 warps (10 with packed
 //   e2m3 / e3m2 / e2m1 KV):

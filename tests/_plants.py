@@ -266,11 +266,11 @@ def _plan(kind: str):
             return orig(seq_lens, num_seqs, q_len, h_q, h_k, sm_count, ctas_per_sm, max_splits, 0, pad_to, fp8_q)
         h_r = h_q // h_k
         s = P.slots(sm_count, ctas_per_sm, h_k, P.n_tiles(q_len, h_r, fp8_q))
-        lens = [int(x) + margin for x in list(seq_lens)[:num_seqs]]
+        grown = [int(seq_lens[b]) + margin for b in range(num_seqs)]
         if kind == "tile_floor":
-            t = [L // P.KV_TILE for L in lens]
+            t = [n // P.KV_TILE for n in grown]
         else:
-            t = [-(-L // P.KV_TILE) if L > 0 else 0 for L in lens]
+            t = [-(-n // P.KV_TILE) if n > 0 else 0 for n in grown]
         red = max_splits > 1 and (num_seqs <= s if kind == "reduction_le" else num_seqs < s)
         work, n_splits = [], []
         if not red:

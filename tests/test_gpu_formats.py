@@ -1,6 +1,6 @@
 """GPU parity of the other narrow KV formats, packed e3m2 and e2m1 (the
-package README, "Beyond fp8: the harness": fp6 e2m3 / e3m2 and fp4 e2m1,
-read by tcgen05 kind::f8f6f4).
+package README, "Beyond fp8: the harness", lists 6-bit e2m3 and e3m2 and
+4-bit e2m1, all taken by tcgen05's kind::f8f6f4).
 
 Both decode kernels against the oracle (output within max|err| <= 2e-2
 max|V| and mean|err| <= 2e-3 max|V|, LSE at 2e-3), the Q quantization fused

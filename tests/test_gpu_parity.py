@@ -109,7 +109,7 @@ def test_split_equals_unsplit(impl):
 @pytest.mark.parametrize("impl", IMPLS)
 def test_upper_bound_plan_and_margin(impl):
     """Planning on longer lengths (upper bound + draft margin) must not change
-    the result: the kernel masks with the exact device lengths."""
+    the result: masking always uses the true lengths in device memory."""
     w = _case("split_nhd")
     got = run_gpu(w, impl=impl, plan_lens=w.seq_lens + 700, margin=3)
     ref, _, _, _ = run_oracle(w)

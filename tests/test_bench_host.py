@@ -57,3 +57,21 @@ def test_traffic_record_of_other_sources_is_not_reported(monkeypatch):
     monkeypatch.setattr(bench, "_kernel_source_hash", lambda name: "0000000000000000")
     assert bench._traffic("decode_tc.cu", "qwen3_8b_decode") is None
     assert real is None or real > 536_870_912  # DRAM bytes include the algorithmic ones
+
+
+def test_source_hash_follows_code_not_comments():
+    import os
+
+    csrc = os.path.join(bench.ROOT, "paged_fp8_decode_gb300", "csrc")
+
+    def read(part, edit=None):
+        text = open(os.path.join(csrc, part), encoding="utf-8").read()
+        return edit(text) if edit and part == "decode_tc_kernel.cuh" else text
+
+    base = bench._kernel_source_hash("decode_tc.cu")
+    assert bench._kernel_source_hash("decode_tc.cu", read=read) == base
+    commented = lambda t: "// a new comment\n/* and a block\n   comment */\n" + t.replace("\n", "\n  ", 3)
+    assert bench._kernel_source_hash("decode_tc.cu", read=lambda p: read(p, commented)) == base
+    recoded = lambda t: t.replace("constexpr float kTau = 0.6f;", "constexpr float kTau = 0.5f;")
+    assert "constexpr float kTau = 0.6f;" in read("decode_tc_kernel.cuh")
+    assert bench._kernel_source_hash("decode_tc.cu", read=lambda p: read(p, recoded)) != base

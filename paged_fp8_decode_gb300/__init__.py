@@ -147,10 +147,32 @@ def _check(fn: str, status: int) -> int:
 
 
 def _ptr(t) -> int | None:
-    """Device pointer of a torch tensor (None -> NULL)."""
+    """Device pointer of a CUDA tensor (None -> NULL). A tensor in host memory
+    is refused: its address handed to a kernel would fault, or on a host the
+    GPU can address, silently read the wrong memory."""
     if t is None:
         return None
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"expected a CUDA tensor for a device pointer, got {getattr(t, 'device', type(t).__name__)}")
     return int(t.data_ptr())
+
+
+def _host_int32(a, n: int, what: str) -> int:
+    """Address of a contiguous int32 host buffer of at least ``n`` elements
+    (numpy array or CPU tensor); anything smaller would be overrun."""
+    import numpy as np
+
+    if isinstance(a, np.ndarray):
+        ok = a.dtype == np.int32 and a.flags.c_contiguous and a.size >= n
+        addr = a.ctypes.data
+    else:
+        import torch
+
+        ok = (not a.is_cuda) and a.dtype == torch.int32 and a.is_contiguous() and a.numel() >= n
+        addr = int(a.data_ptr())
+    if not ok:
+        raise ValueError(f"{what}: need a contiguous int32 host buffer of at least {n} elements")
+    return addr
 
 
 def _stream(stream) -> int | None:
@@ -186,19 +208,20 @@ def mj_plan_split_kv(seq_lens_host, num_seqs: int, q_len: int, h_q: int, h_k: in
     import numpy as np
 
     lib = load_library()
-    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32)[:num_seqs])
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32).reshape(-1)[:num_seqs])
+    if lens.size != num_seqs:
+        raise ValueError(f"seq_lens_host holds {lens.size} lengths, num_seqs is {num_seqs}")
     if work_out is None:
-        work_out = np.zeros((pad_to, 4), dtype=np.int32)
+        work_out = np.zeros((max(0, pad_to), 4), dtype=np.int32)
     if n_splits_out is None:
         n_splits_out = np.zeros(max(1, num_seqs), dtype=np.int32)
-
-    def addr(a):
-        return a.ctypes.data if isinstance(a, np.ndarray) else int(a.data_ptr())
+    work_addr = _host_int32(work_out, 4 * max(0, pad_to), "work_out")
+    nsplit_addr = _host_int32(n_splits_out, num_seqs, "n_splits_out")
 
     chunk, red, slots = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     _check("mj_plan_split_kv", lib.mj_plan_split_kv(
         lens.ctypes.data if num_seqs else None, num_seqs, q_len, h_q, h_k, sm_count, ctas_per_sm,
-        max_splits, margin, pad_to, addr(work_out), addr(n_splits_out), ctypes.byref(chunk),
+        max_splits, margin, pad_to, work_addr, nsplit_addr, ctypes.byref(chunk),
         ctypes.byref(red), ctypes.byref(slots)))
     return {"work": work_out, "n_splits": n_splits_out, "chunk_tiles": chunk.value,
             "with_reduction": bool(red.value), "slots": slots.value, "num_work": pad_to}

@@ -102,6 +102,11 @@ class DecodeStep:
     def args(self, kv: PagedKV, out: torch.Tensor, num_seqs: int, softmax_scale: float,
              q: torch.Tensor | None = None) -> mj_decode_args:
         """The decode call's arguments; ``q`` (bf16 mode): the bf16 Q it reads."""
+        for name, t in (("out", out), ("q", q), ("k_cache", kv.k_cache), ("v_cache", kv.v_cache),
+                        ("k_descale", kv.k_descale), ("v_descale", kv.v_descale), ("block_table", kv.block_table),
+                        ("seq_lens", kv.seq_lens), ("q_mul", kv.q_mul), ("o_mul", kv.o_mul)):
+            if t is not None and not t.is_cuda:
+                raise ValueError(f"{name} must be a CUDA tensor: the kernels read it through a device pointer")
         info = self.plan_info
         a = mj_decode_args()
         if self.q_mode in ("bf16", "fp8_fused"):

@@ -290,3 +290,34 @@ def test_noalloc_rejects_oversized_plans_on_the_host(lib):
     assert need > mj.NOALLOC_SCRATCH_BYTES
     assert lib.mj_decode_attention_noalloc(ctypes.byref(a), None) == mj.MJ_ERR_CAPACITY
     assert lib.mj_decode_attention_noalloc(None, None) == mj.MJ_ERR_INVALID_ARG
+
+
+def test_wrappers_refuse_host_tensors_for_device_pointers(lib):
+    """A CPU tensor's address means nothing to a kernel: the binding refuses it
+    before calling into the library."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(2, 32, 128, dtype=torch.bfloat16)
+    codes = torch.zeros(2, 8, 4, 128, dtype=torch.uint8)
+    desc = torch.zeros(2, 8, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mj.mj_quantize_q(q, 2, 1, 8, codes, desc)
+    key = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    pool = torch.zeros(4 * 16 * 2 * 128, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mj.mj_write_kv(key, key, torch.zeros(4, dtype=torch.int64), pool, pool, (4096, 128, 2048), 16, 4, 0,
+                       torch.ones(1), torch.ones(1))
+
+
+def test_plan_refuses_buffers_it_would_overrun(lib):
+    lens = np.full(8, 1000, np.int32)
+    with pytest.raises(ValueError, match="num_seqs"):
+        mj.mj_plan_split_kv(lens[:5], 8, 1, 32, 8, 152, 2, 16, 0, 64)
+    with pytest.raises(ValueError, match="work_out"):
+        mj.mj_plan_split_kv(lens, 8, 1, 32, 8, 152, 2, 16, 0, 64, work_out=np.zeros((63, 4), np.int32))
+    with pytest.raises(ValueError, match="work_out"):
+        mj.mj_plan_split_kv(lens, 8, 1, 32, 8, 152, 2, 16, 0, 64, work_out=np.zeros((64, 4), np.int64))
+    with pytest.raises(ValueError, match="n_splits_out"):
+        mj.mj_plan_split_kv(lens, 8, 1, 32, 8, 152, 2, 16, 0, 64, n_splits_out=np.zeros(7, np.int32))
+    got = mj.mj_plan_split_kv(lens, 8, 1, 32, 8, 152, 2, 16, 0, 64, work_out=np.zeros((64, 4), np.int32),
+                              n_splits_out=np.zeros(8, np.int32))
+    assert got["with_reduction"] and sum(got["n_splits"]) <= got["slots"]

@@ -73,3 +73,25 @@ def test_bf16_q_as_two_e4m3_terms():
         lo = F.e4m3_decode(F.e4m3_encode((res / s_lo).astype(np.float32)))
         err = np.abs(hi * s_hi + lo * s_lo - q)
         assert err.max() <= amax / 784.0 * (1 + 2.0 ** -16)
+
+
+def test_range_of_p_in_two_e4m3_terms():
+    """P = 2^(t - m_ref + 8) in two e4m3 terms keeps every key down to 17
+    binades below the reference max (p = 2^-9, e4m3's smallest subnormal)
+    and loses every key 18 or more binades below it (p = 2^-10 is a tie
+    between 0 and 2^-9 and rounds to the even code, 0). So a row of N keys
+    loses at most a share N * 2^-18 of the top key's weight, a limit of the
+    representation that long rows with one dominant key can reach."""
+    def two_terms(p):
+        hi = F.e4m3_decode(F.e4m3_encode(np.float32(p)))
+        return hi + F.e4m3_decode(F.e4m3_encode(np.float32(p - hi)))
+
+    for gap in range(0, 18):
+        p = 2.0 ** (8 - gap)
+        assert two_terms(p) == p
+    for gap in range(18, 30):
+        assert two_terms(2.0 ** (8 - gap)) == 0.0
+    # one key 18 binades above N others: the others' whole share is lost
+    n = 131072
+    lost = n * 2.0 ** -18 / (1 + n * 2.0 ** -18)
+    assert abs(lost - 1 / 3) < 1e-12

@@ -282,6 +282,12 @@ MJ_API int mj_workspace_status(void* workspace, void* stream, uint32_t* device_s
  * Rows of requests with seq_lens[b] == 0 and empty work rows write nothing.
  * Grid: num_work x h_k x n_row_tiles CTAs (the tensor-core kernel orders
  * them KV head fastest), fixed by the arguments.
+ * Accuracy: the tensor-core kernel holds the softmax weights as two e4m3
+ * terms scaled to the row's running max, so a key whose logit is 18 or more
+ * binades (about 12.5 nats) below that max weighs zero. A row of N keys can
+ * lose up to N * 2^-18 of its top key's weight that way: negligible unless
+ * one key dominates a very long row. MJ_IMPL_SIMT keeps the weights in
+ * float32 and has no such floor.
  * ---------------------------------------------------------------------- */
 MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
 

@@ -498,6 +498,15 @@ def _noncausal_as_causal():
     orig = A.visible_mask
     A.visible_mask = lambda L, q_len, h_r, causal: orig(L, q_len, h_r, True)
 
+
+def _narrow_sign_dropped(name):
+    orig = getattr(F, name)
+    setattr(F, name, lambda x: orig(np.abs(np.asarray(x, dtype=np.float64))))
+
+
+def _write_e3m2_with_e2m3_encoder():
+    W.e3m2_encode = W.e2m3_encode
+
 PLANTS = {
     # name: (install, pin module that must catch it)
     "causal_mask_strict": (lambda: _mask(True, False), ATTN),
@@ -556,6 +565,9 @@ PLANTS = {
     "plan_bf16_q_tile_width_as_fp8": (_tile_width_bf16_as_fp8, PLAN),
     "write_e2m1_row_bytes_as_fp6": (_write_e2m1_row_as_fp6, KVW),
     "noncausal_block_masked_as_causal": (_noncausal_as_causal, ATTN),
+    "e3m2_sign_dropped": (lambda: _narrow_sign_dropped("e3m2_encode"), FMT),
+    "e2m1_sign_dropped": (lambda: _narrow_sign_dropped("e2m1_encode"), FMT),
+    "write_e3m2_rows_with_e2m3_encoder": (_write_e3m2_with_e2m3_encoder, KVW),
 }
 
 

@@ -2,26 +2,35 @@
 """Benchmark of one paged decode-attention step on GB300.
 
 A step is the whole hot path over one batch: the split-KV plan (host) and
-its upload, ``mj_quantize_q``, ``mj_decode_attention`` and ``mj_merge_lse``.
-Default workload: the Qwen3-8B-shaped decode batch (B=64, q_len=1, 32/8
-heads, D=128, page 16, every length 4096, per-KV-head e4m3 scales, HND,
-16384 pages drawn from a 20000-page pool). Prints ONE JSON line.
+its upload, Q quantization (inside the decode kernel by default, or
+``mj_quantize_q`` with ``--q-mode fp8``), ``mj_decode_attention`` and
+``mj_merge_lse``. Default workload: the Qwen3-8B-shaped decode batch (B=64,
+q_len=1, 32/8 heads, D=128, page 16, every length 4096, per-KV-head e4m3
+scales, HND, 16384 pages drawn from a 20000-page pool). Prints ONE JSON line.
 
 * ``value``: effective KV GB/s = sum(seq_len) * h_k * 2 * row_bytes per step
   / device step time (CUDA events on the launching stream), inputs resident in
   HBM. The KV read per step (537 MB) is larger than the 129 MB L2, so no
   flush is needed between steps.
+* ``configs``: the same figures for the other workloads (long-context split
+  and single sequence, speculative verify causal and non-causal, packed fp6),
+  each timed over a fixed number of steps of its own, with the decode kernel
+  alone timed as back-to-back decode launches between two events.
 * ``e2e``: the same metric end to end through the C ABI from pinned host
-  buffers: each step plans on the host, copies Q, seq_lens, the block table
-  and the plan to the device, runs the three kernels and copies O back.
-* ``roofline``: the decode kernel alone, algorithmic KV bytes per launch /
-  its average CUDA-event duration, against the measured HBM copy bandwidth.
-* ``cpu_baseline``: the CPU oracle timed on a bounded sample in a
-  single-threaded subprocess.
+  buffers: every step plans on the host, uploads its inputs (Q, seq_lens,
+  block table) and its plan, runs the kernels and copies O back to pinned
+  host memory, where the host reads it. Two sets of buffers let step n's
+  copies overlap step n - 1's kernels (a serving loop's pipelining).
+* ``roofline``: the kernel the dispatch runs (``mj_decode_kernel``), KV
+  bytes per launch / the average duration of back-to-back decode launches,
+  against the measured HBM copy bandwidth.
+* ``cpu_baseline``: the CPU oracle timed on a bounded sample of the units,
+  one single-threaded process per host core at once (and one alone).
 
 ``--impl reference`` times the CPU oracle itself, one (request, KV head)
-unit per step. Under torchrun every rank runs an independent replica
-(weak scaling); rank 0 prints.
+unit per step. ``--gpus N`` runs N independent replicas (weak scaling), one
+process per GPU: under torchrun directly, else the script starts torchrun
+itself; rank 0 prints.
 """
 
 from __future__ import annotations
@@ -51,10 +60,10 @@ DEFAULT_KNOBS = {
     "long_single": (2, 64, 6),
     "spec_verify": (4, 64, 4),
     "spec_verify_noncausal": (4, 64, 4),
-    "fp6_decode": (2, 64, 6),
+    "fp6_decode": (2, 64, 4),
     "d256_decode": (2, 64, 2),
-    "fp6_e3m2_decode": (2, 64, 6),
-    "fp4_decode": (2, 64, 6),
+    "fp6_e3m2_decode": (2, 64, 4),
+    "fp4_decode": (2, 64, 4),
     "tiny": (2, 16, 0),
 }
 
@@ -424,17 +433,257 @@ def reference_arm(args):
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
-def main_ours(args):
-    import numpy as np
+# the workloads reported beside the headline one, and their timed steps
+CONFIG_STEPS = {"long_split": 200, "long_single": 400, "spec_verify": 300, "spec_verify_noncausal": 300,
+                "fp6_decode": 100}
+
+
+def launcher_cmd(argv, n: int, port: int) -> list:
+    """The torchrun command that runs this script as n ranks on one node."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", str(n),
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+
+
+def _free_port() -> int:
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _dispatch_kernel(a) -> str:
+    """The decode kernel the library runs for these arguments."""
+    import paged_fp8_decode_gb300 as mj
+
+    return "decode_tc.cu" if mj.mj_decode_kernel(a) == mj.MJ_IMPL_TCGEN05 else "decode_simt.cu"
+
+
+class Bench:
+    """One workload resident on the device, with its step and the calls of a step."""
+
+    def __init__(self, w, dev, knobs, q_mode: str, impl: int):
+        import torch
+
+        from paged_fp8_decode_gb300 import DecodeStep
+        from paged_fp8_decode_gb300.step import paged_kv_from_workload, q_from_workload
+
+        self.w, self.dev, self.q_mode = w, dev, q_mode
+        self.cps, self.msplit, self.stages = knobs
+        self.impl = impl
+        self.kv = paged_kv_from_workload(w, dev)
+        self.q = q_from_workload(w, dev)
+        self.out = torch.empty(w.num_seqs * w.q_len, w.h_q, w.d, dtype=torch.bfloat16, device=dev)
+        self.step = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
+                               ctas_per_sm=self.cps, max_splits=self.msplit, causal=w.causal, impl=impl,
+                               kv_stages=self.stages, device=dev, q_mode=q_mode)
+        self.stream = torch.cuda.current_stream(dev)
+        self.info = self.step.plan(w.seq_lens, w.num_seqs, self.stream)
+        self.args = self.step.args(self.kv, self.out, w.num_seqs, w.softmax_scale, q=self.q)
+        self.kv_bytes = kv_bytes_per_step(w)
+        self.tokens = int((w.seq_lens > 0).sum()) * w.q_len
+        self.launches = (1 if q_mode == "fp8" else 0) + 1 + (1 if self.info["with_reduction"] else 0)
+        self.kernel_file = _dispatch_kernel(self.args)
+
+    def device_step(self):
+        from paged_fp8_decode_gb300 import mj_decode_attention, mj_merge_lse, mj_quantize_q
+
+        w = self.w
+        if self.q_mode == "fp8":  # otherwise the decode kernel quantizes Q itself (or takes it as is)
+            mj_quantize_q(self.q, w.num_seqs, w.q_len, w.h_k, self.step.q_codes, self.step.q_descale,
+                          q_mul=self.kv.q_mul, stream=self.stream)
+        mj_decode_attention(self.args, self.stream)
+        mj_merge_lse(self.args, self.stream)
+
+    def time_steps(self, n: int) -> float:
+        """ms per step over n back-to-back steps (CUDA events on the launching stream)."""
+        import torch
+
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        e0.record(self.stream)
+        for _ in range(n):
+            self.device_step()
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1) / n
+
+    def time_decode(self, n: int) -> float:
+        """µs per launch of the decode kernel alone, n launches back to back
+        between two events (the Q it reads was written by an earlier step)."""
+        import torch
+
+        from paged_fp8_decode_gb300 import mj_decode_attention
+
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        e0.record(self.stream)
+        for _ in range(n):
+            mj_decode_attention(self.args, self.stream)
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1) * 1e3 / n
+
+
+def measure_config(name: str, dev, peak: float, peak_kind: str, q_mode: str, steps: int) -> dict:
+    """One reported workload: step and decode-alone figures, and its DRAM traffic record."""
     import torch
 
     import synth
-    from paged_fp8_decode_gb300 import (DecodeStep, mj_decode_attention, mj_merge_lse, mj_quantize_q,
-                                        mj_workspace_status)
-    from paged_fp8_decode_gb300.build import build
-    from paged_fp8_decode_gb300.step import paged_kv_from_workload, q_from_workload
+    from paged_fp8_decode_gb300 import mj_workspace_status
 
+    w = synth.WORKLOADS[name]()
+    b = Bench(w, dev, DEFAULT_KNOBS.get(name, (2, 64, 0)), q_mode, 0)
+    for _ in range(5):
+        b.device_step()
+    ms = b.time_steps(steps)
+    dec_us = b.time_decode(max(20, steps // 2))
+    status = mj_workspace_status(b.step.workspace, b.stream)
+    gbs = b.kv_bytes / (ms * 1e-3) / 1e9
+    dec_gbs = b.kv_bytes / (dec_us * 1e-6) / 1e9
+    traffic = _traffic(b.kernel_file, name)
+    rec = {
+        "step_us": round(ms * 1e3, 3), "kv_gbs": round(gbs, 1), "pct_of_nominal_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+        f"pct_of_{peak_kind}_hbm": round(100 * gbs / peak, 2),
+        "tokens_per_s": round(b.tokens / (ms * 1e-3), 1), "decode_us": round(dec_us, 3),
+        "decode_frac": round(dec_gbs / peak, 4), "kernel": b.kernel_file.replace(".cu", ""),
+        "kv_bytes_per_step": b.kv_bytes, "steps": steps, "launches_per_step": b.launches,
+        "knobs": {"ctas_per_sm": b.cps, "max_splits": b.msplit, "kv_stages": b.stages, "q_mode": q_mode,
+                  "with_reduction": b.info["with_reduction"], "chunk_tiles": b.info["chunk_tiles"]},
+        "traffic": traffic, "traffic_ratio": round(traffic / b.kv_bytes, 4) if traffic else None,
+        "device_status": status,
+    }
+    del b, w
+    torch.cuda.empty_cache()
+    return rec
+
+
+def e2e_pipelined(w, base, dev, knobs, q_mode: str, impl: int, n_steps: int, dist=None) -> dict:
+    """The metric end to end through the C ABI from pinned host buffers.
+
+    Every step: plan on the host (mj_plan_split_kv) and upload it
+    (mj_plan_upload), copy the step's inputs (bf16 Q, seq_lens, the block
+    table: one packed pinned buffer, one copy) to the device, run the
+    kernels, copy O back to pinned host memory and read it on the host. Two
+    sets of device buffers alternate, and the copies run on their own
+    streams, so step n's uploads and step n - 1's download overlap the
+    kernels of the step between them; the host reads step n's result two
+    steps later, before its buffer is reused."""
+    import numpy as np
+    import torch
+
+    from dataclasses import replace
+
+    from paged_fp8_decode_gb300 import DecodeStep, mj_decode_attention, mj_merge_lse, mj_quantize_q
+    from paged_fp8_decode_gb300.step import q_from_workload
+
+    q0 = q_from_workload(w, "cpu")
+    cps, msplit, stages = knobs
+    qb = q0.numel() * 2
+    lb = w.num_seqs * 4
+    bb = w.block_table.size * 4
+
+    def al(n):
+        return (n + 255) // 256 * 256
+
+    off_l, off_b = al(qb), al(qb) + al(lb)
+    nbytes = off_b + bb
+    # the step's inputs, packed in one pinned host buffer (one copy per step)
+    host_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    host_in[:qb].copy_(q0.view(torch.uint8).reshape(-1))
+    host_in[off_l:off_l + lb].copy_(torch.from_numpy(np.ascontiguousarray(w.seq_lens)).view(torch.uint8))
+    host_in[off_b:off_b + bb].copy_(torch.from_numpy(np.ascontiguousarray(w.block_table)).view(torch.uint8).reshape(-1))
+    compute = torch.cuda.current_stream(dev)
+    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    slots = []
+    for k in range(2):
+        dbuf = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        q = dbuf[:qb].view(torch.bfloat16).view(q0.shape)
+        # the resident cache and scales, with this slot's seq_lens and block table
+        kv = replace(base, seq_lens=dbuf[off_l:off_l + lb].view(torch.int32),
+                     block_table=dbuf[off_b:off_b + bb].view(torch.int32).view(w.block_table.shape))
+        out = torch.empty(w.num_seqs * w.q_len, w.h_q, w.d, dtype=torch.bfloat16, device=dev)
+        st = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d, ctas_per_sm=cps,
+                        max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages, device=dev, q_mode=q_mode)
+        slots.append({"dbuf": dbuf, "q": q, "kv": kv, "out": out, "step": st, "args": None,
+                      "out_host": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                      "done": torch.cuda.Event(), "in_ready": torch.cuda.Event(), "out_ready": torch.cuda.Event(),
+                      "pending": False, "used": False})
+    reads = []
+
+    def read(sl):
+        sl["out_ready"].synchronize()
+        reads.append(float(sl["out_host"][0, 0, 0]))  # the host reads the step's result
+        sl["pending"] = False
+
+    def one(n):
+        sl = slots[n & 1]
+        if sl["pending"]:
+            read(sl)  # step n - 2's result, before its buffers are reused
+        if sl["used"]:
+            copy_in.wait_event(sl["done"])  # step n - 2's kernels are done with this slot's inputs
+        info = sl["step"].plan(w.seq_lens, w.num_seqs, copy_in)
+        with torch.cuda.stream(copy_in):
+            sl["dbuf"].copy_(host_in, non_blocking=True)
+        sl["in_ready"].record(copy_in)
+        compute.wait_event(sl["in_ready"])
+        if sl["args"] is None:
+            sl["args"] = sl["step"].args(sl["kv"], sl["out"], w.num_seqs, w.softmax_scale, q=sl["q"])
+        sl["args"].with_reduction = 1 if info["with_reduction"] else 0
+        sl["args"].chunk_tiles = info["chunk_tiles"]
+        if q_mode == "fp8":
+            mj_quantize_q(sl["q"], w.num_seqs, w.q_len, w.h_k, sl["step"].q_codes, sl["step"].q_descale,
+                          q_mul=sl["kv"].q_mul, stream=compute)
+        mj_decode_attention(sl["args"], compute)
+        mj_merge_lse(sl["args"], compute)
+        sl["done"].record(compute)
+        copy_out.wait_event(sl["done"])
+        with torch.cuda.stream(copy_out):
+            sl["out_host"].copy_(sl["out"], non_blocking=True)
+        sl["out_ready"].record(copy_out)
+        sl["pending"] = sl["used"] = True
+
+    def drain():
+        for sl in slots:
+            if sl["pending"]:
+                read(sl)
+
+    for n in range(4):
+        one(n)
+    drain()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for n in range(n_steps):
+        one(n)
+    drain()
+    elapsed = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    assert all(math.isfinite(v) for v in reads), "non-finite result read back"
+    plan_h2d = slots[0]["step"].work_host.numel() * 4 + w.num_seqs * 4
+    return {"seconds": elapsed, "steps": n_steps, "h2d_bytes_per_step": int(nbytes + plan_h2d),
+            "d2h_bytes_per_step": int(slots[0]["out_host"].numel() * 2)}
+
+
+def main_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # N replicas, one process per GPU: start torchrun with this command line
+        import torch
+
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            raise SystemExit(f"--gpus {args.gpus}: only {have} GPU(s) visible")
+        r = subprocess.run(launcher_cmd(sys.argv[1:], args.gpus, _free_port()))
+        raise SystemExit(r.returncode)
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+
+    import torch
+
+    from paged_fp8_decode_gb300 import MJ_IMPL_SIMT, mj_workspace_status
+    from paged_fp8_decode_gb300.build import build
+
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dist = None
@@ -450,137 +699,72 @@ def main_ours(args):
         cpu_base = run_cpu_baseline(args.workload)
 
     build()
+    torch.cuda.set_device(dev)
+    peak, peak_kind = _peaks()
     w = replica_workload(args.workload, rank)
     cps, msplit, stages = DEFAULT_KNOBS.get(args.workload, (2, 64, 0))
-    cps = args.ctas_per_sm or cps
-    msplit = args.max_splits or msplit
-    stages = args.kv_stages if args.kv_stages is not None else stages
-    impl = {"auto": 0, "simt": 1, "tcgen05": 2}[args.variant]
-
-    torch.cuda.set_device(dev)
-    kv = paged_kv_from_workload(w, dev)
-    q = q_from_workload(w, dev)
-    out = torch.empty(w.num_seqs * w.q_len, w.h_q, w.d, dtype=torch.bfloat16, device=dev)
-    step = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d, ctas_per_sm=cps,
-                      max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages, device=dev,
-                      q_mode=args.q_mode)
-    stream = torch.cuda.current_stream(dev)
-    info = step.plan(w.seq_lens, w.num_seqs, stream)
-    a = step.args(kv, out, w.num_seqs, w.softmax_scale, q=q)
-    kv_bytes = kv_bytes_per_step(w)
-    tokens = int((w.seq_lens > 0).sum()) * w.q_len
-    launches_per_step = (1 if args.q_mode == "fp8" else 0) + 1 + (1 if info["with_reduction"] else 0)
-
-    def device_step(ev=None):
-        if args.q_mode == "fp8":  # otherwise the decode kernel quantizes Q itself (or takes it as is)
-            mj_quantize_q(q, w.num_seqs, w.q_len, w.h_k, step.q_codes, step.q_descale, q_mul=kv.q_mul,
-                          stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        mj_decode_attention(a, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        mj_merge_lse(a, stream)
+    knobs = (args.ctas_per_sm or cps, args.max_splits or msplit, args.kv_stages if args.kv_stages is not None else stages)
+    impl = {"auto": 0, "simt": MJ_IMPL_SIMT, "tcgen05": 2}[args.variant]
+    b = Bench(w, dev, knobs, args.q_mode, impl)
 
     for _ in range(max(3, args.warmup)):
-        device_step()
+        b.device_step()
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
 
-    # ---- device-resident timed region: K whole steps, nothing between the
-    # launches (an event between them would break the overlap of quantize and
-    # decode) ------------------------------------------------------------------
+    # ---- device-resident timed region: K whole steps back to back ----------
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         torch.cuda.synchronize(dev)
         if dist is not None:
             dist.barrier()
-        start.record(stream)
-        for i in range(args.steps):
-            device_step()
-        stop.record(stream)
+        start.record(b.stream)
+        for _ in range(args.steps):
+            b.device_step()
+        stop.record(b.stream)
         torch.cuda.synchronize(dev)
         if dist is not None:
             dist.barrier()
     elapsed_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
 
-    # ---- the decode kernel alone (roofline), CUDA events around each launch
-    n_dec = max(10, min(args.steps, 200))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dec)]
-    for i in range(n_dec):
-        device_step(evs[i])
-    torch.cuda.synchronize(dev)
-    decode_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    status = mj_workspace_status(step.workspace, stream)
+    # ---- the decode kernel alone (roofline): back-to-back launches ---------
+    dec_us = b.time_decode(max(20, min(args.steps, 400)))
+    status = mj_workspace_status(b.step.workspace, b.stream)
 
-    # ---- end to end through host buffers ----------------------------------
-    q_host = q.cpu().pin_memory()
-    lens_host = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).pin_memory()
-    bt_host = torch.from_numpy(np.ascontiguousarray(w.block_table)).pin_memory()
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = (q_host.numel() * 2 + lens_host.numel() * 4 + bt_host.numel() * 4 + step.work_host.numel() * 4 +
-           step.nsplit_host.numel() * 4)
-    d2h = out_host.numel() * 2
-    e2e_steps = max(3, min(args.steps, 200))
-
-    def e2e_step():
-        step.plan(w.seq_lens, w.num_seqs, stream)
-        q.copy_(q_host, non_blocking=True)
-        kv.seq_lens.copy_(lens_host, non_blocking=True)
-        kv.block_table.copy_(bt_host, non_blocking=True)
-        device_step()
-        out_host.copy_(out, non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(3):
-        e2e_step()
-    if dist is not None:
-        dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    # ---- end to end through host buffers, pipelined ------------------------
+    e2e = e2e_pipelined(w, b.kv, dev, knobs, args.q_mode, impl, max(20, min(args.steps, 400)), dist)
 
     # the same step with the separate quantize launch, for comparison
     unfused = None
     if args.q_mode == "fp8_fused" and rank == 0:
-        step_u = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d,
-                            ctas_per_sm=cps, max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages,
-                            device=dev)
-        step_u.plan(w.seq_lens, w.num_seqs, stream)
-        a_u = step_u.args(kv, out, w.num_seqs, w.softmax_scale)
-        n_u = max(10, min(args.steps, 500))
-
-        def step_unfused():
-            mj_quantize_q(q, w.num_seqs, w.q_len, w.h_k, step_u.q_codes, step_u.q_descale, q_mul=kv.q_mul,
-                          stream=stream)
-            mj_decode_attention(a_u, stream)
-            mj_merge_lse(a_u, stream)
-
+        bu = Bench(w, dev, knobs, "fp8", impl)
         for _ in range(3):
-            step_unfused()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(n_u):
-            step_unfused()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms_u = e0.elapsed_time(e1) / n_u
-        unfused = {"ms_per_step": round(ms_u, 5), "value": round(whole_job_gbs(kv_bytes, 1, ms_u * 1e-3), 2),
+            bu.device_step()
+        n_u = max(10, min(args.steps, 500))
+        ms_u = bu.time_steps(n_u)
+        unfused = {"ms_per_step": round(ms_u, 5), "value": round(whole_job_gbs(b.kv_bytes, 1, ms_u * 1e-3), 2),
                    "unit": "GB/s", "steps": n_u, "note": "mj_quantize_q as its own launch before the decode"}
+        del bu
 
     # the KV-cache write before the step (its own measurement, outside the timed step)
-    write_kv = measure_write_kv(w, dev, _peaks()[0]) if rank == 0 else None
-    bf16_q = measure_bf16_q(w, kv, dev, _peaks()[0], cps, msplit) if rank == 0 else None
+    write_kv = measure_write_kv(w, dev, peak) if rank == 0 else None
+    bf16_q = measure_bf16_q(w, b.kv, dev, peak, knobs[0], knobs[1]) if rank == 0 else None
 
     # plan host time alone
     t0 = time.perf_counter()
     for _ in range(50):
-        step.plan(w.seq_lens, w.num_seqs, stream)
+        b.step.plan(w.seq_lens, w.num_seqs, b.stream)
     plan_us = (time.perf_counter() - t0) / 50 * 1e6
     torch.cuda.synchronize(dev)
+
+    # the other workloads (one GPU, rank 0 of a single-process run)
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = {}
+        for name, n in CONFIG_STEPS.items():
+            if name != args.workload:
+                configs[name] = measure_config(name, dev, peak, peak_kind, args.q_mode, n)
 
     if rank != 0:
         if dist is not None:
@@ -588,13 +772,9 @@ def main_ours(args):
         return
 
     ms_per_step = elapsed_ms / args.steps
-    value = whole_job_gbs(kv_bytes, world, ms_per_step * 1e-3)
-    peak, peak_kind = _peaks()
-    dec_avg_ms = sum(decode_ms) / len(decode_ms)
-    achieved = kv_bytes / (dec_avg_ms * 1e-3) / 1e9
-    kernel_file = "decode_tc.cu" if impl == 2 or (impl == 0 and os.path.exists(
-        os.path.join(ROOT, "paged_fp8_decode_gb300", "csrc", "decode_tc.cu"))) else "decode_simt.cu"
-    traffic = _traffic(kernel_file, args.workload)
+    value = whole_job_gbs(b.kv_bytes, world, ms_per_step * 1e-3)
+    achieved = b.kv_bytes / (dec_us * 1e-6) / 1e9
+    traffic = _traffic(b.kernel_file, args.workload)
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -604,28 +784,32 @@ def main_ours(args):
             "workload": args.workload, "num_seqs": w.num_seqs, "q_len": w.q_len, "h_q": w.h_q, "h_k": w.h_k,
             "d": w.d, "page_size": w.page_size, "seq_len_total": int(w.seq_lens.sum()), "layout": w.layout,
             "kv_format": w.kv_format, "causal": w.causal, "parallelism": f"replicas{world}",
-            "l2": f"inputs larger than L2: {kv_bytes / 1e6:.0f} MB of KV read per step vs 129 MB L2, no flush",
-            "ctas_per_sm": cps, "max_splits": msplit, "kv_stages": stages, "variant": args.variant,
+            "l2": f"inputs larger than L2: {b.kv_bytes / 1e6:.0f} MB of KV read per step vs 129 MB L2, no flush",
+            "ctas_per_sm": knobs[0], "max_splits": knobs[1], "kv_stages": knobs[2], "variant": args.variant,
             "q_mode": args.q_mode,
-            "with_reduction": info["with_reduction"], "chunk_tiles": info["chunk_tiles"],
-            "num_work": info["num_work"],
+            "with_reduction": b.info["with_reduction"], "chunk_tiles": b.info["chunk_tiles"],
+            "num_work": b.info["num_work"],
         },
-        "kv_bytes_per_step": kv_bytes,
+        "kv_bytes_per_step": b.kv_bytes,
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         f"pct_of_{peak_kind}_hbm": round(100 * value / world / peak, 2),
-        "tokens_per_s": round(tokens * world / (ms_per_step * 1e-3), 1),
+        "tokens_per_s": round(b.tokens * world / (ms_per_step * 1e-3), 1),
         "plan_host_us": round(plan_us, 2),
         "clocks": clocks,
-        "e2e": {"value": round(whole_job_gbs(kv_bytes, world, e2e_s / e2e_steps), 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
-                "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4)},
-        "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": round(whole_job_gbs(b.kv_bytes, world, e2e["seconds"] / e2e["steps"]), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"], "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "steps": e2e["steps"], "ms_per_step": round(e2e["seconds"] / e2e["steps"] * 1e3, 4),
+                "note": "pipelined over two buffer sets: step n's uploads and step n-1's download overlap the "
+                        "kernels; every step plans, uploads, runs, downloads and is read on the host"},
+        "gpu_launches": b.launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_kind": f"of {peak_kind}", "kernel": kernel_file.replace(".cu", ""),
-                     "decode_us": round(dec_avg_ms * 1e3, 3)},
+                     "peak_kind": f"of {peak_kind}", "kernel": b.kernel_file.replace(".cu", ""),
+                     "decode_us": round(dec_us, 3),
+                     "timing": "back-to-back decode launches between two events"},
         "cpu_baseline": cpu_base,
         "device_status": status,
+        "configs": configs,
         "write_kv": write_kv,
         "unfused_step": unfused,
         "bf16_q": bf16_q,
@@ -650,6 +834,7 @@ def main():
     ap.add_argument("--max-splits", type=int, default=0)
     ap.add_argument("--kv-stages", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
     ap.add_argument("--cpu-baseline-child", default=None)
     ap.add_argument("--budget", type=float, default=10.0)
     ap.add_argument("--shard", default="0/1")

@@ -141,6 +141,21 @@ MJ_API int mj_plan_split_kv(const int32_t* seq_lens_host, int num_seqs, int q_le
                      int* with_reduction, int* slots);
 
 /* ------------------------------------------------------------------------
+ * mj_plan_upload — copy a host plan into the fixed-address device plan
+ * buffers the decode call reads, asynchronously on `stream`.
+ * Source: T5DecodeRunner.plan on the runner page (the plan is staged in
+ * pinned host memory and copied without blocking into device buffers that
+ * keep their addresses, so a captured graph replays new plans).
+ * work_host [pad_to][4] and n_splits_host [num_seqs]: the plan
+ * mj_plan_split_kv wrote; pinned (page-locked) host memory, which the caller
+ * must not overwrite before the copies have run (an event after this call).
+ * work_dev / n_splits_dev: device int32 buffers of the same sizes, 16-byte
+ * aligned. Enqueues one cudaMemcpyAsync per buffer; MJ_ERR_CUDA if one fails.
+ * ---------------------------------------------------------------------- */
+MJ_API int mj_plan_upload(const int32_t* work_host, const int32_t* n_splits_host, int32_t* work_dev,
+                   int32_t* n_splits_dev, int pad_to, int num_seqs, void* stream);
+
+/* ------------------------------------------------------------------------
  * mj_quantize_q — dynamic per-(request, KV head) e4m3 quantization of Q.
  * Source: T5DecodeRunner.run, fp8-Q branch of the "Q" block (runner page):
  *   x      = float(q) [* q_mul]                      (float32)
@@ -233,8 +248,9 @@ typedef struct mj_decode_args {
   /* tuning knobs (0 = library default) */
   int impl;          /* mj_impl */
   int kv_stages;     /* KV ring depth of the tensor-core kernel, in K or V tiles (made even,
-                        at most 13, and lowered to what shared memory holds); 0 = 6 at
-                        d = 128, 2 at d = 256 (a tile of 256-byte rows is 32 KB) */
+                        at most 13, and lowered to what shared memory holds); 0 = the
+                        deepest even ring up to 6 that keeps two CTAs per SM (4 query rows
+                        per tile at d = 128: 6; 8 or 16 rows: 4; d = 256: 2) */
   int evict_first;   /* 1 = L2 evict-first hint on KV loads (KV is read once) */
 
   int out_dtype;     /* mj_out_dtype of `out` (0 = bf16); rounding to nearest even */
@@ -282,14 +298,27 @@ MJ_API int mj_workspace_status(void* workspace, void* stream, uint32_t* device_s
  * Rows of requests with seq_lens[b] == 0 and empty work rows write nothing.
  * Grid: num_work x h_k x n_row_tiles CTAs (the tensor-core kernel orders
  * them KV head fastest), fixed by the arguments.
- * Accuracy: the tensor-core kernel holds the softmax weights as two e4m3
- * terms scaled to the row's running max, so a key whose logit is 18 or more
- * binades (about 12.5 nats) below that max weighs zero. A row of N keys can
- * lose up to N * 2^-18 of its top key's weight that way: negligible unless
- * one key dominates a very long row. MJ_IMPL_SIMT keeps the weights in
- * float32 and has no such floor.
+ * Accuracy: the tensor-core kernel scales the softmax weights p to the row's
+ * running max (p <= 2^8.6) and carries each in e4m3 terms: hi = e4m3(p) and
+ * lo = e4m3(p - hi), and where p < 1/4 the same split of (p - hi - lo) * 2^10,
+ * weighed 2^-10; the row sum l adds the p themselves. Every weight is then
+ * within max(2^-8 p, 2^-20) of its value, so keys down to 27 binades (about
+ * 19 nats) below the row's max keep their weight, and the output of a row of
+ * N keys is off by at most (2^-8 + N * 2^-28) * max|V|. MJ_IMPL_SIMT keeps
+ * the weights in float32.
+ * Ordering: with q_mode MJ_Q_FP8 the tensor-core launch may begin before the
+ * preceding kernel on `stream` has finished (programmatic dependent launch:
+ * only its Q reads wait for that kernel), so that kernel must be the
+ * mj_quantize_q call that wrote q_codes, with nothing enqueued in between;
+ * the other Q modes are plainly stream-ordered.
  * ---------------------------------------------------------------------- */
 MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
+
+/* Which kernel mj_decode_attention runs for these arguments: *impl is set to
+ * MJ_IMPL_TCGEN05 or MJ_IMPL_SIMT. Validates like that call and launches
+ * nothing; MJ_ERR_UNSUPPORTED when args->impl asks for the tensor-core kernel
+ * and it cannot take the arguments. */
+MJ_API int mj_decode_kernel(const mj_decode_args* args, int* impl);
 
 /* ------------------------------------------------------------------------
  * mj_merge_lse — combine split-KV partials by log-sum-exp.
@@ -325,10 +354,20 @@ MJ_API int mj_merge_lse(const mj_decode_args* args, void* stream);
  * status header (synchronously); make that first call before any stream
  * capture. All calls share the array and it keeps the last call's contents:
  * calls whose kernels overlap on the GPU race on it, so issue them in order
- * on one stream. The status word in this scratch is not readable by callers.
+ * on one stream. The kernels record anomalies (a page id out of range, a
+ * bounded wait that timed out, a work row outside the partial area) in a
+ * status word in the scratch header; mj_noalloc_status reads it.
  * ---------------------------------------------------------------------- */
 #define MJ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 MJ_API int mj_decode_attention_noalloc(const mj_decode_args* args, void* stream);
+
+/* Read and clear the status word of the current device's allocation-free
+ * scratch, like mj_workspace_status does for a caller workspace: SYNCHRONISES
+ * `stream` (a test and debugging aid, not for the hot path); *device_status = 0
+ * means no anomaly, else the same bit mask; returns MJ_ERR_DEVICE_CHECK when
+ * it is non-zero. Called before any mj_decode_attention_noalloc on the device,
+ * it performs that call's first-call set-up and reads 0. */
+MJ_API int mj_noalloc_status(void* stream, uint32_t* device_status);
 
 /* ------------------------------------------------------------------------
  * mj_write_kv — the KV-cache write that precedes a decode step: quantize the

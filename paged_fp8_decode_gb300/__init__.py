@@ -49,7 +49,8 @@ KV_TILE = 128
 EXPORTS = (
     "mj_status_string", "mj_version", "mj_tile_width", "mj_slots", "mj_plan_split_kv",
     "mj_quantize_q", "mj_workspace_size", "mj_workspace_init", "mj_workspace_status",
-    "mj_decode_attention", "mj_merge_lse", "mj_decode_attention_noalloc", "mj_write_kv",
+    "mj_decode_attention", "mj_merge_lse", "mj_decode_attention_noalloc", "mj_noalloc_status", "mj_write_kv",
+    "mj_plan_upload", "mj_decode_kernel",
 )
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -134,6 +135,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mj_decode_attention.argtypes = [ctypes.POINTER(mj_decode_args), vp]
     lib.mj_merge_lse.argtypes = [ctypes.POINTER(mj_decode_args), vp]
     lib.mj_decode_attention_noalloc.argtypes = [ctypes.POINTER(mj_decode_args), vp]
+    lib.mj_noalloc_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.mj_plan_upload.argtypes = [vp, vp, vp, vp, i32, i32, vp]
+    lib.mj_decode_kernel.argtypes = [ctypes.POINTER(mj_decode_args), ctypes.POINTER(ctypes.c_int)]
     lib.mj_write_kv.argtypes = [ctypes.POINTER(mj_write_kv_args), vp]
     _lib = lib
     return lib
@@ -227,6 +231,26 @@ def mj_plan_split_kv(seq_lens_host, num_seqs: int, q_len: int, h_q: int, h_k: in
             "with_reduction": bool(red.value), "slots": slots.value, "num_work": pad_to}
 
 
+def mj_plan_upload(work_host, n_splits_host, work_dev, n_splits_dev, pad_to: int, num_seqs: int, stream=None):
+    """Copy a host plan (pinned int32 CPU tensors) into the fixed device plan
+    buffers on ``stream`` (one asynchronous copy per buffer)."""
+    import torch
+
+    for t, n, what in ((work_dev, 4 * pad_to, "work_dev"), (n_splits_dev, num_seqs, "n_splits_dev")):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < n:
+            raise ValueError(f"{what}: a contiguous int32 device buffer of at least {n} elements is required")
+    _check("mj_plan_upload", load_library().mj_plan_upload(
+        _host_int32(work_host, 4 * pad_to, "work_host"), _host_int32(n_splits_host, num_seqs, "n_splits_host"),
+        _ptr(work_dev), _ptr(n_splits_dev), pad_to, num_seqs, _stream(stream)))
+
+
+def mj_decode_kernel(args: mj_decode_args) -> int:
+    """The kernel mj_decode_attention runs for ``args``: MJ_IMPL_TCGEN05 or MJ_IMPL_SIMT."""
+    v = ctypes.c_int(0)
+    _check("mj_decode_kernel", load_library().mj_decode_kernel(ctypes.byref(args), ctypes.byref(v)))
+    return v.value
+
+
 def mj_quantize_q(q, num_seqs: int, q_len: int, h_k: int, q_codes, q_descale, q_mul=None, stream=None):
     """``q``: bf16 tensor ``[>= num_seqs*q_len, h_q, d]`` (any token/head
     strides, channel stride 1)."""
@@ -272,6 +296,16 @@ def mj_decode_attention_noalloc(args: mj_decode_args, stream=None):
     include/mj.h)."""
     _check("mj_decode_attention_noalloc",
            load_library().mj_decode_attention_noalloc(ctypes.byref(args), _stream(stream)))
+
+
+def mj_noalloc_status(stream=None) -> int:
+    """Read and clear the status word of the allocation-free call's scratch on
+    the current device (synchronises). 0 = clean."""
+    v = ctypes.c_uint32(0)
+    st = load_library().mj_noalloc_status(_stream(stream), ctypes.byref(v))
+    if st not in (MJ_OK, MJ_ERR_DEVICE_CHECK):
+        _check("mj_noalloc_status", st)
+    return v.value
 
 
 def mj_write_kv(key, value, slot_mapping, k_cache, v_cache, kv_strides, page_size: int, num_pages: int,

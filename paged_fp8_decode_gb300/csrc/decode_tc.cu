@@ -72,10 +72,6 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const DecodeParams& p, in
 
 }  // namespace
 
-// Default ring depth: 6 entries (3 K and 3 V tiles); with D = 256 an entry is
-// 32 KB, and 2 entries keep two CTAs per SM (a deeper ring takes ctas_per_sm = 1).
-int tc_default_stages(int d) { return d == 256 ? 2 : 6; }
-
 bool tc_supported(const DecodeParams& p) {
   if (p.q_mode == MJ_Q_BF16 && p.kv_format != MJ_KV_E4M3) return false;
   if (p.kv_format != MJ_KV_E4M3) {
@@ -97,13 +93,34 @@ bool tc_supported(const DecodeParams& p) {
 
 int tc_max_stages() { return 13; }
 
+namespace {
+
+// The tensor-core kernel's preconditions and its two tensor maps; false when
+// the arguments are outside its envelope.
+bool tc_prepare(DecodeParams& p, CUtensorMap* mk, CUtensorMap* mv) {
+  if (!tc_supported(p)) return false;
+  p.tma_head_inner = (p.k_sh < p.k_st) ? 1 : 0;
+  if (((p.v_sh < p.v_st) ? 1 : 0) != p.tma_head_inner) return false;
+  return encode_kv_map(mk, p.k_cache, p, p.k_sp, p.k_st, p.k_sh, p.tma_head_inner) &&
+         encode_kv_map(mv, p.v_cache, p, p.v_sp, p.v_st, p.v_sh, p.tma_head_inner);
+}
+
+}  // namespace
+
+bool decode_tc_supported(const DecodeParams& p0) {
+  DecodeParams p = p0;
+  CUtensorMap mk, mv;
+  return tc_prepare(p, &mk, &mv);
+}
+
 cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsupported) {
   *unsupported = false;
-  if (!tc_supported(p)) {
+  CUtensorMap mk, mv;
+  if (!tc_prepare(p, &mk, &mv)) {
     *unsupported = true;
     return cudaSuccess;
   }
-  if (p.kv_stages <= 0) p.kv_stages = tc_default_stages(p.d);
+  // kv_stages <= 0: the launcher picks the default depth for the instance
   if (p.kv_stages > tc_max_stages()) p.kv_stages = tc_max_stages();
   // The ring depth is always even, so that K tiles (ring entries u = 2i) and
   // V tiles (u = 2i + 1) never share a slot. Every waiter on full[slot] must
@@ -114,18 +131,7 @@ cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsuppor
   // warps) has already consumed in order. With an odd depth a K slot's
   // previous occupant is a V tile, which the issuer's look-ahead QK probe (up
   // to three tiles ahead of PV) can reach before it has landed.
-  if (p.kv_stages & 1) p.kv_stages = p.kv_stages > 2 ? p.kv_stages - 1 : 2;
-  p.tma_head_inner = (p.k_sh < p.k_st) ? 1 : 0;
-  if (((p.v_sh < p.v_st) ? 1 : 0) != p.tma_head_inner) {
-    *unsupported = true;
-    return cudaSuccess;
-  }
-  CUtensorMap mk, mv;
-  if (!encode_kv_map(&mk, p.k_cache, p, p.k_sp, p.k_st, p.k_sh, p.tma_head_inner) ||
-      !encode_kv_map(&mv, p.v_cache, p, p.v_sp, p.v_st, p.v_sh, p.tma_head_inner)) {
-    *unsupported = true;
-    return cudaSuccess;
-  }
+  if (p.kv_stages > 0 && (p.kv_stages & 1)) p.kv_stages = p.kv_stages > 2 ? p.kv_stages - 1 : 2;
   if (p.num_work == 0) return cudaSuccess;
   // row tile = the plan's tile width (16 or 32 rows)
   if (p.kv_format != MJ_KV_E4M3) {

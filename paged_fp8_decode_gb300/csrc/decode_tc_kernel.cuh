@@ -32,11 +32,14 @@
 //   core even for a handful of query rows:
 //     S^T[key][row] = K[key][:] . Q[row][:]       A = K tile (K-major), B = Q tile
 //     O^T[d][col]  += V^T[d][key] . P^T[key][col] A = V tile (MN-major), B = P tile
-// * P is written as two e4m3 terms, hi = e4m3(p) and lo = e4m3(p - hi), in
-//   separate columns of the same PV product (the query rows leave spare N
-//   columns anyway): O gets P to ~2^-8 relative precision at no extra MMA.
-//   P is scaled by 2^8 (p = 2^(t - m + 8) <= 256) so that its e4m3 terms stay
-//   normal well into the tail of the softmax; the factor cancels in O / l.
+// * P = 2^(t - m + 8) (at most 2^8.6) is written as four e4m3 terms in
+//   separate N columns of the same PV product: pair A, hi = e4m3(p) and
+//   lo = e4m3(p - hi), and, where p < 1/4, pair B, the same split of what
+//   pair A left, (p - hi - lo) * 2^10; the epilogue adds pair B's columns
+//   times 2^-10. Every p is then carried to within max(2^-8 p, 2^-20), so
+//   keys far below the row's max keep their weight (pair A alone would round
+//   everything 18 binades below the max to zero). l sums the p themselves.
+//   The factor 2^8 cancels in O / l.
 // * Keys at or past the device seq_len are masked by select on S; in a
 //   request's last, partial tile the V producer warp also zeroes the V rows
 //   past the end before the PV product (page tails may hold NaN codes, and
@@ -46,6 +49,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cstddef>
 #include <mutex>
@@ -101,7 +105,8 @@ struct Ctrl {
   uint64_t s_full[4];
   uint64_t p_full[4];
   uint64_t o_full[4];
-  uint64_t red_bar[2];  // the 4 softmax warps have posted their row maxima
+  uint64_t red_bar[2];  // the 4 softmax warps have posted their row maxima (or their bound)
+  uint64_t row_bar[2];  // ... their row maxima, after a bound exchange that did not settle
   uint64_t sum_bar;     // ... their row sums
   uint64_t drain;       // MMA drain after an abort
   uint64_t q_ready;     // the softmax warps have written the Q tile
@@ -110,12 +115,14 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort;
   alignas(16) float red[2][4][32];  // per-tile row maxima of the 4 softmax warps (read as float4)
+  alignas(16) float bound[2][4];    // per softmax warp: max over its rows and keys of (tile max - m_ref)
   alignas(16) float lsum[4][32];    // row sums of the 4 softmax warps
   float alpha[4][32];               // per softmax warp: the rescale factors of the current tiles
   float qamax[2][4];                // bf16 Q: per softmax warp, |x| max and |residual| max
 };
 static_assert(sizeof(Ctrl) <= 3072, "control block");
-static_assert(offsetof(Ctrl, red) % 16 == 0 && offsetof(Ctrl, lsum) % 16 == 0, "float4 access to red/lsum");
+static_assert(offsetof(Ctrl, red) % 16 == 0 && offsetof(Ctrl, lsum) % 16 == 0 && offsetof(Ctrl, bound) % 16 == 0,
+              "float4 access to red/lsum/bound");
 
 // Reduce NR per-lane values over the 32 lanes of a warp, one row per lane
 // group: a reduce-scatter (each step halves the rows a lane keeps and
@@ -194,6 +201,18 @@ __host__ __device__ constexpr uint32_t mma_kv_type(int kf) {
   return kf == MJ_KV_E2M3 ? 3u : (kf == MJ_KV_E3M2 ? 4u : (kf == MJ_KV_E2M1 ? 5u : 0u));
 }
 
+// TMEM columns a kernel instance uses: its S buffers (NQK columns each, two
+// or four of them) and its D / 128 O accumulators (NPV columns each); and the
+// power of two it allocates. An instance that needs all 512 columns must run
+// alone on its SM (launch_tc sizes its shared memory so that it does).
+__host__ __device__ constexpr int tc_nsb(int /*nr*/) { return 4; }  // S / P buffers in flight
+__host__ __device__ constexpr int tc_tmem_cols_used(int nqk, int npv, int nr, int d) {
+  return tc_nsb(nr) * nqk + (d / 128) * npv;
+}
+__host__ __device__ constexpr uint32_t tc_tmem_alloc_cols(int cols) {
+  return cols <= 64 ? 64u : (cols <= 128 ? 128u : (cols <= 256 ? 256u : 512u));
+}
+
 // QM, how Q arrives (mj_q_mode): 0 e4m3 codes from mj_quantize_q; 1 bf16 Q
 // as is, represented as two e4m3 terms per value; 2 bf16 Q quantized here
 // with mj_quantize_q's recipe (see the Q staging in the softmax warps).
@@ -207,25 +226,35 @@ template <int NQK, int NPV, int NR, int KF, int QM = 0, int D = 128>
 __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc, (NR <= 16 ? 2 : 1))
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                      DecodeParams p) {
-  constexpr int NH = NPV / 2;  // P columns per half (hi | lo)
   constexpr int DH = D / 128;
   constexpr uint32_t kEntry = DH * kTileBytes;  // one ring entry: a K or V tile
   constexpr uint32_t kQSub = q_sub_bytes(NQK);
-  static_assert(NH <= NQK && NR <= NH && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
+  // P columns: term k (A hi, A lo, B hi, B lo) of row r at column k * NR + r
+  static_assert(NPV == 4 * NR && NR <= NQK && NR >= 4 && (NR & (NR - 1)) == 0, "row tile");
   constexpr bool PK = KF != MJ_KV_E4M3;  // a packed (narrow) format: no NaN codes, V widened
   static_assert(QM != 1 || (!PK && 2 * NR <= NQK), "bf16 Q: e4m3 KV, hi and lo rows in the Q tile");
   static_assert((D == 128 || D == 256) && (!PK || D == 128), "head size (packed formats: 128)");
   // TP tiles per softmax iteration; NSB S and P buffers let QK run up to
-  // NSB - 1 tiles ahead of PV.
+  // NSB - 1 tiles ahead of PV, so the softmax of a tile never waits for
+  // the QK product of the next.
   constexpr int TP = NR <= 8 ? 2 : 1;
-  constexpr int NSB = 2 * TP;
+  constexpr int NSB = tc_nsb(NR);
+  static_assert(NSB >= 2 * TP, "S / P buffers");
   // TMEM: NSB S buffers (NQK columns each), DH O accumulators (NPV columns each)
-  constexpr int kCols = NSB * NQK + DH * NPV;
-  static_assert(kCols <= 256, "TMEM columns");
-  constexpr uint32_t kTmemCols = kCols <= 64 ? 64 : (kCols <= 128 ? 128 : 256);
+  constexpr int kCols = tc_tmem_cols_used(NQK, NPV, NR, D);
+  constexpr uint32_t kTmemCols = tc_tmem_alloc_cols(kCols);
+  static_assert(kCols <= 512, "TMEM columns");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  // The launch may overlap the end of the preceding kernel on the stream
+  // (programmatic dependent launch). With bf16 Q (as is, or quantized here)
+  // that kernel may have written anything read below (seq_lens, the KV
+  // cache, the plan), so every thread waits for it before reading. With fp8
+  // codes the preceding kernel is mj_quantize_q, which wrote only the Q
+  // codes and descales: only the softmax warps wait, before they read them.
+  if constexpr (QM != 0) tc::grid_dependency_wait();
 
   // CTA x = (work row, KV head) with the head fastest: the CTAs that run
   // together stream the same requests' pages (with token-major layouts the
@@ -271,6 +300,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
       tc::mbar_init(tc::smem_u32(&ctl.o_full[s]), 1);
     }
     for (int s = 0; s < 2; ++s) tc::mbar_init(tc::smem_u32(&ctl.red_bar[s]), 4);
+    for (int s = 0; s < 2; ++s) tc::mbar_init(tc::smem_u32(&ctl.row_bar[s]), 4);
     tc::mbar_init(tc::smem_u32(&ctl.sum_bar), 4);
     tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
     tc::mbar_init(tc::smem_u32(&ctl.q_ready), 128);
@@ -481,6 +511,9 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
             ok = false;
             break;
           }
+          // back off: this warp shares its SM sub-partition with a softmax
+          // warp, whose issue slots a tight polling loop would take
+          __nanosleep(64);
         }
       }
       if (!ok) {
@@ -652,7 +685,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
     // m_ref: the reference max each row's P is scaled by; it only moves when a
     // tile's max exceeds it by more than kTau (log2 units), and then O (kept
     // in TMEM across tiles) is rescaled in place. P = 2^(t - m_ref + 8) stays
-    // <= 2^(8 + kTau) < 448, so both e4m3 terms of P stay finite.
+    // <= 2^(8 + kTau) < 448, so every e4m3 term of P stays finite.
     constexpr float kTau = 0.6f;
     float m_ref[NR], l_part[NR];
 #pragma unroll
@@ -663,6 +696,12 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
     bool ok = true;
     constexpr int kGroup = 32 / NR;  // lanes that share a row after rs_reduce
     const int my_row = lane / kGroup;
+    constexpr bool kBound = NR >= 8;  // the single-bound check before the per-row maxima
+    int xr = 0;                       // per-row exchanges so far (kBound; the same count in every thread)
+    // P buffers whose pair-B blocks may hold nonzero codes in this thread's
+    // chunk (bit j: buffer j); at first every buffer (shared memory starts
+    // with arbitrary contents)
+    uint32_t b_dirty = (1u << NSB) - 1u;
 
     // TP tiles per iteration: with few rows, the two S buffers are processed
     // together (256 keys), so the row-max reduction, the cross-warp exchange
@@ -736,45 +775,105 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
         }
       }
       const int xi = i / TP;  // exchange sequence number
-      const float wmax = rs_reduce<NR, true>(tmp, lane);
-      if (lane % kGroup == 0) ctl.red[xi & 1][qd][my_row] = wmax;
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.red_bar[xi & 1]));
-      ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[xi & 1]), uint32_t(xi >> 1) & 1u, abort, kWaitLimitNs);
-      if (!ok) break;
-
-      // new reference maxima (the same decision in every thread)
       bool rescale = false;
+      // With 8 or more rows, one bound first: the largest (tile max - m_ref)
+      // over the rows and keys of the four warps. A row's reference only
+      // moves when its tile max exceeds it by more than kTau, so a bound
+      // <= kTau (the common case once the references have settled) skips the
+      // per-row reductions. A row with no visible key so far gives
+      // -inf - -inf = NaN, which fmaxf drops; its first visible key gives +inf.
+      bool settled = false;
+      if constexpr (kBound) {
+        float dmax = -INFINITY;
 #pragma unroll
-      for (int r = 0; r < NR; r += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][0][r]);
-        const float4 b4 = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][1][r]);
-        const float4 c4 = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][2][r]);
-        const float4 d4 = *reinterpret_cast<const float4*>(&ctl.red[xi & 1][3][r]);
-        const float tm[4] = {fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x)), fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y)),
-                             fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z)), fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w))};
+        for (int r = 0; r < NR; ++r) dmax = fmaxf(dmax, tmp[r] - m_ref[r]);
+        dmax = warp_max(dmax);
+        if (lane == 0) ctl.bound[xi & 1][qd] = dmax;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.red_bar[xi & 1]));
+        ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[xi & 1]), uint32_t(xi >> 1) & 1u, abort, kWaitLimitNs);
+        if (!ok) break;
+        const float4 bd = *reinterpret_cast<const float4*>(&ctl.bound[xi & 1][0]);
+        settled = fmaxf(fmaxf(bd.x, bd.y), fmaxf(bd.z, bd.w)) <= kTau;  // the same in every thread
+      }
+      if (!settled) {
+        // per-row maxima over the four warps: exchange number xe (counted
+        // apart from the bound exchanges when there are both)
+        const int xe = kBound ? xr++ : xi;
+        const uint32_t xbar = tc::smem_u32(kBound ? &ctl.row_bar[xe & 1] : &ctl.red_bar[xe & 1]);
+        const float wmax = rs_reduce<NR, true>(tmp, lane);
+        if (lane % kGroup == 0) ctl.red[xe & 1][qd][my_row] = wmax;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(xbar);
+        ok = tc::mbar_wait(xbar, uint32_t(xe >> 1) & 1u, abort, kWaitLimitNs);
+        if (!ok) break;
+
+        // new reference maxima (the same decision in every thread)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float alpha = 1.f;
-          if (tm[j] > m_ref[r + j] + kTau) {  // false for -inf tiles
-            alpha = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
-            rescale |= m_ref[r + j] != -INFINITY;
-            m_ref[r + j] = tm[j];
-            l_part[r + j] *= alpha;
+        for (int r = 0; r < NR; r += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][0][r]);
+          const float4 b4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][1][r]);
+          const float4 c4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][2][r]);
+          const float4 d4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][3][r]);
+          const float tm[4] = {fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x)), fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y)),
+                               fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z)), fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w))};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float alpha = 1.f;
+            if (tm[j] > m_ref[r + j] + kTau) {  // false for -inf tiles
+              alpha = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
+              rescale |= m_ref[r + j] != -INFINITY;
+              m_ref[r + j] = tm[j];
+              l_part[r + j] *= alpha;
+            }
+            // the O rescale below reads the factors back from shared memory
+            if (lane == 0) ctl.alpha[qd][r + j] = alpha;
           }
-          // the O rescale below reads the factors back from shared memory
-          if (lane == 0) ctl.alpha[qd][r + j] = alpha;
         }
       }
-      // P = 2^(t - m_ref + 8) as hi + lo e4m3 terms; this key's column of
-      // P^T: hi of row r at byte r, lo at byte NH + r of the key's 16-byte
-      // chunk in 16-column block (byte / 16).
-      // (one body, instantiated masked and unmasked: a select would make
-      // fully visible tiles pay for the masks)
-      auto make_p = [&](auto masked) {
+
+      // p = 2^(t - m_ref + 8) of every (key, row) of the iteration, in place
+      // of s; 0 where the row does not see the key
+      {
         float c8[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) c8[r] = 8.f - m_ref[r];
+        if (all_vis) {
+#pragma unroll
+          for (int a = 0; a < TP; ++a)
+#pragma unroll
+            for (int r = 0; r < NR; ++r) s[a][r] = fast_exp2(fmaf(s[a][r], scale, c8[r]));
+        } else {
+#pragma unroll
+          for (int a = 0; a < TP; ++a)
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+              const bool vis = valid[a] && key[a] <= lim[r] && m_ref[r] != -INFINITY;
+              s[a][r] = vis ? fast_exp2(fmaf(s[a][r], scale, c8[r])) : 0.f;
+            }
+        }
+      }
+      // Pair B is only needed where some p of the warp lies in (0, 1/4);
+      // the same choice for the whole warp, so the common case (every key of
+      // the warp within 10 binades of its row's max) pays nothing for it:
+      // there pair A alone is within 2^-8 p of every p.
+      bool need_b = false;
+#pragma unroll
+      for (int a = 0; a < TP; ++a)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) need_b |= s[a][r] > 0.f && s[a][r] < 0.25f;
+      need_b = __any_sync(0xFFFFFFFFu, need_b);
+
+      // This key's column of P^T: term k of row r at byte k * NR + r (k: A hi,
+      // A lo, B hi, B lo) of 16-column block (byte / 16), the key's 16-byte
+      // chunk in it. Pair A is hi = e4m3(p), lo = e4m3(p - hi); pair B the
+      // same split of (p - hi - lo) * 2^10 where p < 1/4, else 0. (One body,
+      // instantiated with and without pair B.) With 8 or more rows pair B has
+      // blocks of its own: without pair B only pair A's blocks are stored,
+      // and pair B's are cleared only where this thread's chunk of the buffer
+      // may still hold nonzero codes (b_dirty).
+      auto make_p = [&](auto with_b) {
+        constexpr bool WB = decltype(with_b)::value;
 #pragma unroll
         for (int a = 0; a < TP; ++a) {
           if (a >= nt) break;
@@ -783,38 +882,53 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
           for (int w2 = 0; w2 < NPV / 4; ++w2) words[w2] = 0u;
 #pragma unroll
           for (int r = 0; r < NR; r += 2) {
-            float pr[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              if constexpr (decltype(masked)::value) {
-                const bool vis = valid[a] && key[a] <= lim[r + j] && m_ref[r + j] != -INFINITY;
-                pr[j] = vis ? fast_exp2(fmaf(s[a][r + j], scale, c8[r + j])) : 0.f;
-              } else {
-                pr[j] = fast_exp2(fmaf(s[a][r + j], scale, c8[r + j]));
-              }
-            }
-            const __nv_fp8x2_storage_t hi2 =
-                __nv_cvt_float2_to_fp8x2(make_float2(pr[0], pr[1]), __NV_SATFINITE, __NV_E4M3);
+            const float x0 = s[a][r], x1 = s[a][r + 1];
+            const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
             const float2 hf = e4m3x2_to_float2(hi2);
-            const __nv_fp8x2_storage_t lo2 =
-                __nv_cvt_float2_to_fp8x2(make_float2(pr[0] - hf.x, pr[1] - hf.y), __NV_SATFINITE, __NV_E4M3);
-            const float2 lf = e4m3x2_to_float2(lo2);
-            l_part[r] += hf.x + lf.x;
-            l_part[r + 1] += hf.y + lf.y;
-            words[r / 4] |= uint32_t(hi2) << ((r % 4) * 8);
-            words[(NH + r) / 4] |= uint32_t(lo2) << (((NH + r) % 4) * 8);
+            const float d0 = x0 - hf.x, d1 = x1 - hf.y;  // exact
+            const __nv_fp8x2_storage_t lo2 = __nv_cvt_float2_to_fp8x2(make_float2(d0, d1), __NV_SATFINITE, __NV_E4M3);
+            const int sh = (r % 4) * 8;  // the pair's two bytes in their word
+            words[r / 4] |= uint32_t(hi2) << sh;
+            words[(NR + r) / 4] |= uint32_t(lo2) << sh;
+            if constexpr (WB) {
+              // pair B: what pair A left of p (exact), times 2^10, where p < 1/4
+              const float2 lf = e4m3x2_to_float2(lo2);
+              const float y0 = x0 < 0.25f ? (d0 - lf.x) * 1024.f : 0.f;
+              const float y1 = x1 < 0.25f ? (d1 - lf.y) * 1024.f : 0.f;
+              const __nv_fp8x2_storage_t bh2 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+              const float2 bhf = e4m3x2_to_float2(bh2);
+              const __nv_fp8x2_storage_t bl2 =
+                  __nv_cvt_float2_to_fp8x2(make_float2(y0 - bhf.x, y1 - bhf.y), __NV_SATFINITE, __NV_E4M3);
+              words[(2 * NR + r) / 4] |= uint32_t(bh2) << sh;
+              words[(3 * NR + r) / 4] |= uint32_t(bl2) << sh;
+            }
+            // l sums the weights themselves; O gets them to within
+            // max(2^-8 p, 2^-20) each
+            l_part[r] += x0;
+            l_part[r + 1] += x1;
           }
           uint8_t* pt = smem + lay.p0 + bs(i + a) * p_stride;
+          constexpr int kBlkA = NR >= 8 ? NPV / 32 : NPV / 16;  // blocks always stored
 #pragma unroll
-          for (int bk = 0; bk < NPV / 16; ++bk)
+          for (int bk = 0; bk < kBlkA; ++bk)
             *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
                 make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
+          if constexpr (kBlkA < NPV / 16) {
+            const uint32_t bit = 1u << bs(i + a);
+            if (WB || (b_dirty & bit)) {
+#pragma unroll
+              for (int bk = kBlkA; bk < NPV / 16; ++bk)
+                *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
+                    make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
+              b_dirty = WB ? (b_dirty | bit) : (b_dirty & ~bit);
+            }
+          }
         }
       };
-      if (all_vis)
-        make_p(std::false_type{});
-      else
+      if (need_b)
         make_p(std::true_type{});
+      else
+        make_p(std::false_type{});
       if (rescale) {
         // O holds the PV sums up to tile i-1, scaled by the old references:
         // wait for the last of them and rescale O in TMEM before PV_i (which
@@ -824,17 +938,13 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
         if (!ok) break;
         __syncwarp();  // lane 0's factors
         tc::tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < DH * NPV; c += 16) {
           float v[16];
           tc::tmem_ld16(tO + lane_off + c, v);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = (c + j) % NPV;            // column within its O accumulator
-            const int r = col < NH ? col : col - NH;  // hi column r, lo column NH + r
-            if (r < NR) v[j] *= ctl.alpha[qd][r];
-          }
+          for (int j = 0; j < 16; ++j) v[j] *= ctl.alpha[qd][((c + j) % NPV) % NR];  // column k * NR + r: row r
           tc::tmem_st16(tO + lane_off + c, v);
         }
         tc::tmem_wait_st();
@@ -847,7 +957,8 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
         if (a < nt) tc::mbar_arrive(tc::smem_u32(&ctl.p_full[bs(i + a)]));
       if (!ok) break;
     }
-    // the final O: wait for the last PV product; o_acc[dh][r] is channel 128 dh + x
+    // the final O: wait for the last PV product; o_acc[dh][r] is channel
+    // 128 dh + x: pair A's two columns of row r plus 2^-10 times pair B's
     float o_acc[DH][NR];
 #pragma unroll
     for (int dh = 0; dh < DH; ++dh)
@@ -858,6 +969,9 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
       tc::tc_fence_after();
 #pragma unroll
       for (int dh = 0; dh < DH; ++dh) {
+        float ob[NR];  // pair B's sum
+#pragma unroll
+        for (int r = 0; r < NR; ++r) ob[r] = 0.f;
 #pragma unroll
         for (int c = 0; c < NPV; c += 16) {
           float v[16];
@@ -866,10 +980,14 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c + j;
-            const int r = col < NH ? col : col - NH;
-            if (r < NR) o_acc[dh][r] += v[j];
+            if (col < 2 * NR)
+              o_acc[dh][col % NR] += v[j];
+            else
+              ob[col % NR] += v[j];
           }
         }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) o_acc[dh][r] = fmaf(ob[r], 1.f / 1024.f, o_acc[dh][r]);
       }
     }
 
@@ -932,22 +1050,44 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
 
 
 constexpr int kMaxDynSmem = 227 * 1024;  // per-block opt-in limit of sm_100-class GPUs
+constexpr int kSmemPerSm = 228 * 1024;   // shared memory of one SM (each block also takes 1 KB)
+constexpr int kMaxDevices = 64;
 
 template <int NQK, int NPV, int NR, int KF, int QM, int D>
 cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p0, cudaStream_t stream) {
   DecodeParams p = p0;
   // the ring depth the shared memory holds (even, at least 2)
   auto smem_bytes = [&](int stages) {
-    return int(tc_smem_layout(stages, NQK, NPV, NR <= 8 ? 4 : 2, D / 128).total) + 1024;
+    return int(tc_smem_layout(stages, NQK, NPV, tc_nsb(NR), D / 128).total) + 1024;
   };
+  if (p.kv_stages <= 0) {
+    // default: the deepest ring up to 6 entries that keeps two CTAs per SM
+    // (one for the 32-row tiles, whose registers allow only one)
+    p.kv_stages = 6;
+    if (NR <= 16)
+      while (p.kv_stages > 2 && 2 * (smem_bytes(p.kv_stages) + 1024) > kSmemPerSm) p.kv_stages -= 2;
+  }
   while (p.kv_stages > 2 && smem_bytes(p.kv_stages) > kMaxDynSmem) p.kv_stages -= 2;
-  const int bytes = smem_bytes(p.kv_stages);
-  static int configured = 0;  // largest dynamic smem size set so far
-  if (bytes > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, KF, QM, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  int bytes = smem_bytes(p.kv_stages);
+  // An instance that allocates all 512 TMEM columns must be alone on its SM:
+  // a second CTA's allocation would wait for the first to finish. Asking for
+  // more than half of the SM's shared memory guarantees that.
+  constexpr uint32_t kTmemCols = tc_tmem_alloc_cols(tc_tmem_cols_used(NQK, NPV, NR, D));
+  if (kTmemCols == 512 && bytes <= kSmemPerSm / 2) bytes = kSmemPerSm / 2 + 1024;
+  // The dynamic shared-memory limit is an attribute of the kernel on each
+  // device: raise it once per device (atomically: host threads may race).
+  static std::atomic<int> configured[kMaxDevices];  // largest size set so far, per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int have = configured[dev].load(std::memory_order_acquire);
+  if (bytes > have) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<NQK, NPV, NR, KF, QM, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes);
     if (e != cudaSuccess) return e;
-    configured = bytes;
+    while (bytes > have && !configured[dev].compare_exchange_weak(have, bytes, std::memory_order_acq_rel)) {
+    }
   }
   cudaLaunchConfig_t cfg = {};
   if (int64_t(p.num_work) * p.h_k > INT32_MAX || p.n_row_tiles > 65535) return cudaErrorInvalidConfiguration;
@@ -955,8 +1095,13 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   cfg.blockDim = dim3(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc);
   cfg.dynamicSmemBytes = size_t(bytes);
   cfg.stream = stream;
+  // Programmatic dependent launch: the grid may start before the preceding
+  // kernel on the stream has finished; the kernel waits for it
+  // (griddepcontrol.wait) before it reads anything that kernel may have
+  // written (with fp8 Q codes, whose writer mj_quantize_q must precede it
+  // directly, only before it reads the codes).
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with mj_quantize_q
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -965,16 +1110,17 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
 
 // The kernel instance for the row tile (the plan's tile width, 16 or 32
 // rows; fewer rows take the 4- or 8-row variants). With bf16 Q as two terms
-// the Q tile holds two rows (hi, lo) per query row.
+// the Q tile holds two rows (hi, lo) per query row. P takes 4 columns per
+// row (two pairs of e4m3 terms).
 template <int KF, int QM, int D = 128>
 cudaError_t launch_rows(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p, cudaStream_t stream) {
   constexpr int K = QM == 1 ? 2 : 1;
   if (p.tw <= 16) {
     if (p.n_q <= 4) return launch_tc<16, 16, 4, KF, QM, D>(mk, mv, p, stream);
-    if (p.n_q <= 8) return launch_tc<16, 16, 8, KF, QM, D>(mk, mv, p, stream);
-    return launch_tc<16 * K, 32, 16, KF, QM, D>(mk, mv, p, stream);
+    if (p.n_q <= 8) return launch_tc<16, 32, 8, KF, QM, D>(mk, mv, p, stream);
+    return launch_tc<16 * K, 64, 16, KF, QM, D>(mk, mv, p, stream);
   }
-  return launch_tc<32 * K, 64, 32, KF, QM, D>(mk, mv, p, stream);
+  return launch_tc<32 * K, 128, 32, KF, QM, D>(mk, mv, p, stream);
 }
 
 // packed KV takes fp8 Q only: codes, or quantized here

@@ -255,6 +255,42 @@ int mj_plan_split_kv(const int32_t* seq_lens_host, int num_seqs, int q_len, int 
   return MJ_OK;
 }
 
+int mj_plan_upload(const int32_t* work_host, const int32_t* n_splits_host, int32_t* work_dev, int32_t* n_splits_dev,
+                   int pad_to, int num_seqs, void* stream) {
+  if (pad_to < 0 || num_seqs < 0) return MJ_ERR_INVALID_ARG;
+  if ((pad_to > 0 && (!work_host || !work_dev)) || (num_seqs > 0 && (!n_splits_host || !n_splits_dev)))
+    return MJ_ERR_INVALID_ARG;
+  if ((work_dev && !aligned(work_dev, 16)) || (n_splits_dev && !aligned(n_splits_dev, 16))) return MJ_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // one copy per buffer
+  if (pad_to > 0) {
+    const cudaError_t e =
+        cudaMemcpyAsync(work_dev, work_host, size_t(pad_to) * 4 * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return MJ_ERR_CUDA;
+  }
+  if (num_seqs > 0) {
+    const cudaError_t e =
+        cudaMemcpyAsync(n_splits_dev, n_splits_host, size_t(num_seqs) * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return MJ_ERR_CUDA;
+  }
+  return MJ_OK;
+}
+
+int mj_decode_kernel(const mj_decode_args* args, int* impl) {
+  if (!impl) return MJ_ERR_INVALID_ARG;
+  DecodeParams p;
+  const int st = make_params(args, &p);
+  if (st != MJ_OK) return st;
+  if (args->impl == MJ_IMPL_SIMT) {
+    *impl = MJ_IMPL_SIMT;
+    return MJ_OK;
+  }
+  const bool tc = mj::decode_tc_supported(p);
+  if (!tc && args->impl == MJ_IMPL_TCGEN05) return MJ_ERR_UNSUPPORTED;
+  *impl = tc ? MJ_IMPL_TCGEN05 : MJ_IMPL_SIMT;
+  return MJ_OK;
+}
+
 int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, int num_seqs, int q_len,
                   int h_q, int h_k, int d, const float* q_mul, uint8_t* q_codes, float* q_descale,
                   void* stream) {

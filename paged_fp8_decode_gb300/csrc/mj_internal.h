@@ -113,5 +113,7 @@ cudaError_t launch_write_kv(const mj_write_kv_args& a, cudaStream_t stream);
 // Tensor-core kernel; sets *unsupported (and launches nothing) when the
 // arguments are outside its envelope.
 cudaError_t launch_decode_tc(DecodeParams p, cudaStream_t stream, bool* unsupported);
+// Whether the tensor-core kernel takes these arguments (launches nothing).
+bool decode_tc_supported(const DecodeParams& p);
 
 }  // namespace mj

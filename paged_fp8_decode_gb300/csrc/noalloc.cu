@@ -14,10 +14,12 @@
 // code its name is only a host-side stand-in for the device symbol; the
 // device address is looked up once per device with cudaGetSymbolAddress (with
 // that device current) and passed to the kernels. The lookup, and the zeroing
-// of the status header, happen on the first call on each device, which should
-// therefore come before any stream capture. All calls share the one array, so
-// calls whose kernels overlap on the GPU (different streams, concurrent
-// threads) race on it; issue them in order on one stream.
+// of the status header (enqueued on the caller's stream, ahead of that call's
+// kernels), happen on the first call on each device, which should therefore
+// come before any stream capture. All calls share the one array, so calls
+// whose kernels overlap on the GPU (different streams, concurrent threads)
+// race on it; issue them in order on one stream. mj_noalloc_status reads and
+// clears the status word the kernels record anomalies in.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -33,8 +35,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once).
-int scratch_on_current_device(void** out) {
+// Device address of the scratch array on the current device (set up once:
+// the first call on a device also zeroes the header on `stream`).
+int scratch_on_current_device(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MJ_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MJ_ERR_UNSUPPORTED;
@@ -43,8 +46,10 @@ int scratch_on_current_device(void** out) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return MJ_ERR_CUDA;
     // the status word (header) is the only part that must start at zero;
-    // the partials are always written before they are read within a call
-    if (cudaMemset(ptr, 0, mj::kWsHeader) != cudaSuccess) return MJ_ERR_CUDA;
+    // the partials are always written before they are read within a call.
+    // Zeroed on the caller's stream, so that it is ordered before this
+    // call's kernels whatever kind of stream that is.
+    if (cudaMemsetAsync(ptr, 0, mj::kWsHeader, stream) != cudaSuccess) return MJ_ERR_CUDA;
     g_scratch_ptr[dev] = ptr;
   }
   *out = g_scratch_ptr[dev];
@@ -63,7 +68,7 @@ extern "C" int mj_decode_attention_noalloc(const mj_decode_args* args, void* str
   }
   if (need > kScratchBytes) return MJ_ERR_CAPACITY;  // the plan needs more than the fixed array holds
   void* scratch = nullptr;
-  int st = scratch_on_current_device(&scratch);
+  int st = scratch_on_current_device(static_cast<cudaStream_t>(stream), &scratch);
   if (st != MJ_OK) return st;
   mj_decode_args a = *args;
   a.workspace = scratch;
@@ -71,4 +76,12 @@ extern "C" int mj_decode_attention_noalloc(const mj_decode_args* args, void* str
   st = mj_decode_attention(&a, stream);
   if (st != MJ_OK) return st;
   return mj_merge_lse(&a, stream);
+}
+
+extern "C" int mj_noalloc_status(void* stream, uint32_t* device_status) {
+  if (!device_status) return MJ_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const int st = scratch_on_current_device(static_cast<cudaStream_t>(stream), &scratch);
+  if (st != MJ_OK) return st;
+  return mj_workspace_status(scratch, stream, device_status);
 }

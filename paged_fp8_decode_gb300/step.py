@@ -4,7 +4,7 @@
 between steps (``__init__``: persistent, fixed-address plan buffers, the
 partial/workspace area sized by slots, the packed-Q buffer and its
 descales) and issues the four calls of a step: ``plan`` (host plan plus a
-pinned, asynchronous copy into the fixed device buffers), then
+pinned, asynchronous copy into the fixed device buffers, mj_plan_upload), then
 ``mj_quantize_q``, ``mj_decode_attention`` and ``mj_merge_lse`` on one
 stream. It holds no arithmetic of its own.
 """
@@ -17,7 +17,7 @@ import numpy as np
 import torch
 
 from . import (KV_FORMATS, MJ_IMPL_AUTO, mj_decode_args, mj_decode_attention, mj_merge_lse,
-               mj_plan_split_kv, mj_quantize_q, mj_slots, mj_workspace_init, mj_workspace_size)
+               mj_plan_split_kv, mj_plan_upload, mj_quantize_q, mj_slots, mj_workspace_init, mj_workspace_size)
 
 
 @dataclass
@@ -89,11 +89,10 @@ class DecodeStep:
                                 self.h_k, self.sm_count, self.ctas_per_sm, self.max_splits, self.margin,
                                 self.pad_to, work_out=self.work_host, n_splits_out=self.nsplit_host)
         s = stream or torch.cuda.current_stream(self.device)
-        with torch.cuda.stream(s):
-            self.work_dev.copy_(self.work_host, non_blocking=True)
-            self.nsplit_dev.copy_(self.nsplit_host, non_blocking=True)
+        mj_plan_upload(self.work_host, self.nsplit_host, self.work_dev, self.nsplit_dev, self.pad_to, num_seqs, s)
+        if self._staged is None:
             self._staged = torch.cuda.Event()
-            self._staged.record(s)
+        self._staged.record(s)
         info["num_seqs"] = num_seqs
         self.plan_info = info
         return info

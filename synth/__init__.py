@@ -31,6 +31,8 @@ five benchmark configurations; :func:`make_case` builds any smaller case.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -189,7 +191,8 @@ def pack_e2m3(codes: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------
 def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_lens, layout="HND",
               kv_format="fp8", scale_mode="head", causal=True, pool_pages=None, seed=0,
-              outlier_channels=0, outlier_gain=10.0, extra_block_cols=0) -> Workload:
+              outlier_channels=0, outlier_gain=10.0, extra_block_cols=0, kv_values=None,
+              q_values=None) -> Workload:
     """Build a seeded workload.
 
     ``seq_lens``: lengths of all ``num_seqs`` requests (0 = padding request).
@@ -198,6 +201,11 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
     order. ``scale_mode``: "tensor" | "head" (e4m3) — the narrow formats
     (e2m3, e3m2, e2m1) always use per-(KV head, channel) scales folded into
     ``q_mul`` / ``o_mul``.
+    ``kv_values``: optional ``(which, g, tok_req, tok_pos) -> float32 [n_tok, d]``
+    giving the K ("k") or V ("v") values of KV head ``g`` for the valid
+    tokens (request index and position of each) in place of N(0,1) draws;
+    ``q_values``: optional float32 ``[num_seqs*q_len, h_q, d]`` in place of
+    the N(0,1) Q (rounded to bf16 like it).
     """
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     assert seq_lens.shape == (num_seqs,)
@@ -217,13 +225,17 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
         off += n
 
     # (page, slot) of every valid token, request-major
-    tok_pages, tok_slots = [], []
+    tok_pages, tok_slots, tok_req, tok_pos = [], [], [], []
     for b, L in enumerate(seq_lens):
         j = np.arange(int(L))
         tok_pages.append(block_table[b, j // page_size])
         tok_slots.append(j % page_size)
+        tok_req.append(np.full(int(L), b, dtype=np.int64))
+        tok_pos.append(j)
     tok_pages = np.concatenate(tok_pages) if tok_pages else np.zeros(0, np.int32)
     tok_slots = np.concatenate(tok_slots) if tok_slots else np.zeros(0, np.int64)
+    tok_req = np.concatenate(tok_req) if tok_req else np.zeros(0, np.int64)
+    tok_pos = np.concatenate(tok_pos) if tok_pos else np.zeros(0, np.int64)
     n_tok = len(tok_pages)
 
     row_bytes = d if kv_format == "fp8" else d * NARROW[kv_format][1] // 8
@@ -251,52 +263,65 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
 
     meta = {}
     caches, scales, chans = {}, {}, {}
+    chunk = 1 << 16  # tokens per encode pass (bounds the temporaries)
     for which, stream, ostream in (("k", _S_K, _S_OUTLIER_K), ("v", _S_V, _S_OUTLIER_V)):
         buf = np.empty(shape, dtype=np.uint8)
         buf[...] = poison_row
         rows = buf.reshape(-1, row_bytes)
-        rng = _rng(seed, stream)
-        orng = _rng(seed, ostream)
         per_head_scale = np.zeros(h_k, dtype=np.float32)
         ch_scale = np.zeros((h_k, d), dtype=np.float32)
+        outl = [None] * h_k
 
-        xbuf = np.empty((n_tok, d), dtype=np.float32)
-
-        def draw(out=None):
-            x = rng.standard_normal((n_tok, d), dtype=np.float32, out=xbuf if out is None else out)
+        def draw(g):
+            """KV head g's values: its own seeded streams (the heads draw in parallel)."""
+            if kv_values is not None:
+                return np.asarray(kv_values(which, g, tok_req, tok_pos), dtype=np.float32).reshape(n_tok, d)
+            x = _rng(seed, 1000 * stream + g).standard_normal((n_tok, d), dtype=np.float32)
             if outlier_channels:
-                ch = orng.choice(d, size=outlier_channels, replace=False)
+                ch = _rng(seed, 1000 * ostream + g).choice(d, size=outlier_channels, replace=False)
                 x[:, ch] *= np.float32(outlier_gain)
-                meta.setdefault(f"{which}_outlier_channels", []).append(sorted(int(c) for c in ch))
+                outl[g] = sorted(int(c) for c in ch)
             return x
 
-        tensor_scale = np.float32(1.0)
-        xs = None
-        if kv_format == "fp8" and scale_mode == "tensor":
-            xs = [draw(np.empty((n_tok, d), dtype=np.float32)) for _ in range(h_k)]
-            amax = max([_absmax(x) for x in xs] + [1e-30])
-            tensor_scale = np.float32(amax / 448.0)
-        for g in range(h_k):
-            x = xs[g] if xs is not None else draw()
+        def encode(g, x, s_):
+            """Scale and encode head g's rows in chunks and write them into the cache."""
+            fr = flat_rows(g)
+            for a in range(0, n_tok, chunk):
+                xs_ = x[a:a + chunk] / s_
+                codes = _e4m3_codes(xs_) if kv_format == "fp8" else _narrow_rows(xs_, kv_format)
+                rows[fr[a:a + chunk]] = codes
+
+        def head(g, tensor_scale=None):
+            x = xs[g] if xs is not None else draw(g)
             if kv_format == "fp8":
-                if scale_mode == "tensor":
+                if tensor_scale is not None:
                     s_ = tensor_scale
                 else:
                     s_ = np.float32((_absmax(x) if x.size else 1.0) / 448.0)
                     per_head_scale[g] = s_
-                np.divide(x, s_, out=x)
-                codes = _e4m3_codes(x)
             else:
                 s_c = (np.maximum(x.max(axis=0), -x.min(axis=0)) if x.size
                        else np.ones(d, np.float32)).astype(np.float32)
                 s_c = np.maximum(s_c / np.float32(NARROW[kv_format][0]), np.float32(1e-30))
                 ch_scale[g] = s_c
-                np.divide(x, s_c[None, :], out=x)
-                codes = _narrow_rows(x, kv_format)
-            rows[flat_rows(g)] = codes
+                s_ = s_c[None, :]
+            encode(g, x, s_)
             if xs is not None:
                 xs[g] = None
-            del x, codes
+
+        workers = max(1, min(h_k, os.cpu_count() or 1, 8))
+        tensor_scale = np.float32(1.0)
+        xs = None
+        with ThreadPoolExecutor(max_workers=workers) as ex:
+            if kv_format == "fp8" and scale_mode == "tensor":
+                xs = list(ex.map(draw, range(h_k)))
+                amax = max([_absmax(x) for x in xs] + [1e-30])
+                tensor_scale = np.float32(amax / 448.0)
+                list(ex.map(lambda g: head(g, tensor_scale), range(h_k)))
+            else:
+                list(ex.map(head, range(h_k)))
+        if outlier_channels and kv_values is None:
+            meta[f"{which}_outlier_channels"] = outl
         caches[which] = buf
         if kv_format == "fp8":
             scales[which] = (np.array([tensor_scale], dtype=np.float32) if scale_mode == "tensor"
@@ -307,6 +332,8 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
 
     qrng = _rng(seed, _S_Q)
     q = qrng.standard_normal((num_seqs * q_len, h_q, d), dtype=np.float32)
+    if q_values is not None:
+        q = np.ascontiguousarray(q_values, dtype=np.float32).reshape(num_seqs * q_len, h_q, d)
     import torch
 
     qb = torch.from_numpy(q).to(torch.bfloat16)
@@ -331,6 +358,46 @@ def make_case(*, name="case", num_seqs, q_len, h_q, h_k, d=128, page_size, seq_l
 # ----------------------------------------------------------------------------
 def _uniform_lens(seed, n, lo, hi):
     return _rng(seed, _S_LENS).integers(lo, hi + 1, size=n).astype(np.int32)
+
+
+def sink_case(*, name="sink", seq_lens, sink_pos, gap_binades=20.0, h_q=32, h_k=8, d=128, page_size=64,
+              layout="NHD", seed=1020) -> Workload:
+    """One dominant key per request (an attention sink) over many near-equal
+    others, e4m3 KV with per-KV-head scales.
+
+    Q = 1 + 0.05 N(0,1) (every channel near 1). The other keys' K rows are
+    0.01 N(0,1), so their logits sit near 0 and close to one another; the
+    sink's K row is the constant kappa = gap * ln 2 / sqrt(d), so with the
+    softmax scale 1/sqrt(d) its logit is about ``gap_binades`` binades (gap *
+    ln 2 nats) above the others for every query row. V: the others
+    1 + 0.25 N(0,1), the sink -2 in every channel, so the output is a visible
+    mix of the two whenever the others' share of the weight is not tiny.
+    ``sink_pos[b]``: the sink's position in request b (negative: from the end).
+    """
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    B = len(seq_lens)
+    pos = np.array([int(p_) if p_ >= 0 else int(L) + int(p_) for p_, L in zip(sink_pos, seq_lens)], np.int64)
+    kappa = np.float32(gap_binades * math.log(2.0) / math.sqrt(d))
+
+    def kv_values(which, g, tok_req, tok_pos):
+        rng = _rng(seed, 100 + 2 * g + (which == "v"))
+        n = len(tok_req)
+        is_sink = tok_pos == pos[tok_req]
+        if which == "k":
+            x = rng.standard_normal((n, d), dtype=np.float32) * np.float32(0.01)
+            x[is_sink] = kappa
+        else:
+            x = np.float32(1.0) + rng.standard_normal((n, d), dtype=np.float32) * np.float32(0.25)
+            x[is_sink] = np.float32(-2.0)
+        return x
+
+    q = np.float32(1.0) + np.float32(0.05) * _rng(seed, _S_Q).standard_normal((B, h_q, d), dtype=np.float32)
+    w = make_case(name=name, num_seqs=B, q_len=1, h_q=h_q, h_k=h_k, d=d, page_size=page_size,
+                  seq_lens=seq_lens, layout=layout, scale_mode="head", seed=seed, kv_values=kv_values,
+                  q_values=q)
+    w.meta["sink_pos"] = pos.tolist()
+    w.meta["gap_binades"] = float(gap_binades)
+    return w
 
 
 def tiny(seed: int = 1001) -> Workload:

@@ -14,6 +14,20 @@ ATOL_MAX = 2e-2  # max |err| <= 2e-2 * max|V|
 ATOL_MEAN = 2e-3  # mean |err| <= 2e-3 * max|V|
 
 
+_last_workload = {}
+
+
+def full_workload(name):
+    """synth.WORKLOADS[name](), kept while consecutive tests use the same
+    one (a full-size batch takes seconds to generate and GBs to hold)."""
+    import synth
+
+    if name not in _last_workload:
+        _last_workload.clear()
+        _last_workload[name] = synth.WORKLOADS[name]()
+    return _last_workload[name]
+
+
 def run_gpu(w, *, impl=0, ctas_per_sm=2, max_splits=16, margin=0, plan_lens=None, sm_count=None,
             kv_stages=0, out_strided=False, descale_per_seq=False, steps=1, out_dtype=None, q_mode="fp8"):
     import torch

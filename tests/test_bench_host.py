@@ -75,3 +75,35 @@ def test_source_hash_follows_code_not_comments():
     recoded = lambda t: t.replace("constexpr float kTau = 0.6f;", "constexpr float kTau = 0.5f;")
     assert "constexpr float kTau = 0.6f;" in read("decode_tc_kernel.cuh")
     assert bench._kernel_source_hash("decode_tc.cu", read=lambda p: read(p, recoded)) != base
+
+
+def test_launcher_runs_n_ranks_of_this_script():
+    cmd = bench.launcher_cmd(["--gpus", "4", "--steps", "10"], 4, 29512)
+    i = cmd.index("torch.distributed.run")
+    assert cmd[i - 1] == "-m"
+    assert cmd[cmd.index("--nproc-per-node") + 1] == "4" and cmd[cmd.index("--nnodes") + 1] == "1"
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1" and cmd[cmd.index("--master-port") + 1] == "29512"
+    assert cmd[-4:] == [bench.__file__.replace(".pyc", ".py"), "--gpus", "4", "--steps", "10"][-4:]
+    assert cmd[-5].endswith("bench.py")
+
+
+def test_more_gpus_than_visible_fail_loudly(monkeypatch):
+    import argparse
+
+    import torch
+
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(torch.cuda, "device_count", lambda: 1)
+    args = argparse.Namespace(gpus=2)
+    with pytest.raises(SystemExit) as e:
+        bench.main_ours(args)
+    assert "only 1 GPU" in str(e.value)
+
+
+def test_world_size_must_match_gpus(monkeypatch):
+    import argparse
+
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit) as e:
+        bench.main_ours(argparse.Namespace(gpus=4))
+    assert "WORLD_SIZE=2" in str(e.value)

@@ -9,7 +9,12 @@ kernel's design relies on; the GPU parity tests check the kernel itself.
 * P = 2^(t - m_ref + 8) with t <= m_ref + 0.6 (the rescale threshold) stays
   below e4m3's largest value, so the hi term never saturates.
 * P as two e4m3 terms, hi = e4m3(p) and lo = e4m3(p - hi), is within
-  max(2^-8 p, 2^-10) of p.
+  max(2^-8 p, 2^-10) of p (pair A).
+* P as the kernel carries it, pair A and, where p < 1/4, pair B (the same
+  split of what pair A left, times 2^10, weighed 2^-10), is within
+  max(2^-8 p, 2^-20) of p, so keys down to 27 binades below the reference
+  max keep their weight; on a long row with one dominant key that keeps the
+  output within tolerance of exact softmax, where pair A alone does not.
 * bf16 Q as two e4m3 terms with per-unit scales amax/448 and
   max|residual|/448 is within amax/28^2 of q: each term's rounding error is at
   most half a step of e4m3's top binade, 16/448 = 1/28 of its scale.
@@ -75,23 +80,77 @@ def test_bf16_q_as_two_e4m3_terms():
         assert err.max() <= amax / 784.0 * (1 + 2.0 ** -16)
 
 
-def test_range_of_p_in_two_e4m3_terms():
-    """P = 2^(t - m_ref + 8) in two e4m3 terms keeps every key down to 17
-    binades below the reference max (p = 2^-9, e4m3's smallest subnormal)
-    and loses every key 18 or more binades below it (p = 2^-10 is a tie
-    between 0 and 2^-9 and rounds to the even code, 0). So a row of N keys
-    loses at most a share N * 2^-18 of the top key's weight, a limit of the
-    representation that long rows with one dominant key can reach."""
-    def two_terms(p):
-        hi = F.e4m3_decode(F.e4m3_encode(np.float32(p)))
-        return hi + F.e4m3_decode(F.e4m3_encode(np.float32(p - hi)))
+def _e4(x):
+    return F.e4m3_decode(F.e4m3_encode(np.asarray(x, dtype=np.float32)))
 
+
+def _pair(x):
+    """hi + lo: x as two e4m3 terms (float32 arithmetic, as in the kernel)."""
+    x = np.asarray(x, dtype=np.float32)
+    hi = _e4(x)
+    return hi + _e4((x - hi.astype(np.float32)).astype(np.float32))
+
+
+def _kernel_p(p):
+    """p as the tensor-core kernel carries it: pair A, hi = e4m3(p) and
+    lo = e4m3(p - hi); where p < 1/4 also pair B, the same split of
+    (p - hi - lo) * 2^10 (exact in float32), weighed 2^-10."""
+    p = np.asarray(p, dtype=np.float32)
+    hi = _e4(p)
+    d = (p - hi.astype(np.float32)).astype(np.float32)
+    lo = _e4(d)
+    y = np.where(p < np.float32(0.25), ((d - lo.astype(np.float32)) * np.float32(1024.0)).astype(np.float32),
+                 np.float32(0.0))
+    return hi + lo + _pair(y) / 1024.0
+
+
+def test_p_as_four_e4m3_terms():
+    p = (2.0 ** np.linspace(-40.0, 8.6, 400001)).astype(np.float32).astype(np.float64)
+    err = np.abs(_kernel_p(p) - p)
+    assert np.all(err <= np.maximum(2.0 ** -8 * p, 2.0 ** -20))
+    keep = p >= 2.0 ** -8  # full relative precision down to 16 binades below the max
+    assert np.all(err[keep] <= 2.0 ** -8 * p[keep])
+    # pair B never saturates: below 1/4, p * 2^10 < 256 < 448
+    assert _e4(np.float32(0.25 * 1024.0 * (1 - 2.0 ** -24))) < 448.0
+
+
+def test_range_of_p():
+    """Pair A alone keeps every key down to 17 binades below the reference
+    max (p = 2^-9, e4m3's smallest subnormal) and loses every key 18 or more
+    binades below it (p = 2^-10 ties between 0 and 2^-9 and rounds to the
+    even code, 0). With pair B the same holds 10 binades further down: keys
+    to 27 binades below the max keep their weight exactly."""
     for gap in range(0, 18):
-        p = 2.0 ** (8 - gap)
-        assert two_terms(p) == p
+        assert _pair(2.0 ** (8 - gap)) == 2.0 ** (8 - gap)
     for gap in range(18, 30):
-        assert two_terms(2.0 ** (8 - gap)) == 0.0
-    # one key 18 binades above N others: the others' whole share is lost
-    n = 131072
-    lost = n * 2.0 ** -18 / (1 + n * 2.0 ** -18)
-    assert abs(lost - 1 / 3) < 1e-12
+        assert _pair(2.0 ** (8 - gap)) == 0.0
+    for gap in range(0, 28):
+        assert _kernel_p(2.0 ** (8 - gap)) == 2.0 ** (8 - gap)
+    for gap in range(28, 40):
+        assert _kernel_p(2.0 ** (8 - gap)) == 0.0
+
+
+@pytest.mark.parametrize("n", [32768, 131072])
+def test_dominant_key_over_a_long_row(n):
+    """One key 20 binades above n near-equal others (an attention sink over
+    a long row): the kernel's P arithmetic against exact softmax. With pair
+    A alone the others round to zero and the output is the sink's V; their
+    true share, n * 2^-20 of the sink's weight, is then lost."""
+    rng = np.random.default_rng(7)
+    t = rng.standard_normal(n) * 0.05  # log2 units; the others near 0
+    t[0] = 20.0
+    v = 1.0 + 0.25 * rng.standard_normal((n, 8))
+    v[0] = -2.0
+    vmax = np.abs(v).max()
+    p = 2.0 ** (t - t.max())
+    exact = (p[:, None] * v).sum(0) / p.sum()
+    pk = (2.0 ** (t - t.max() + 8)).astype(np.float32)
+
+    def out(w, l):
+        return (w[:, None] * v).sum(0) / l.sum()
+
+    a = _pair(pk)
+    err_a = np.abs(out(a, a) - exact).max() / vmax  # l from the represented weights
+    err_k = np.abs(out(_kernel_p(pk), pk) - exact).max() / vmax  # the kernel: l sums the p themselves
+    assert err_a > 2e-2, "the case must lie beyond pair A's reach"
+    assert err_k < 2e-3, f"four terms: {err_k:.2e} of max|V|"

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import synth
-from tests._harness import SENTINEL, all_units, compare, run_gpu, run_oracle, sample_units
+from tests._harness import SENTINEL, all_units, compare, full_workload, run_gpu, run_oracle, sample_units
 
 pytestmark = pytest.mark.gpu
 
@@ -160,12 +160,15 @@ def test_fp16_output_split(impl):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-def test_full_size_sampled(impl):
+def test_full_size(impl):
     """The 64 x 4096-token batch at head size 256, in the benchmark's launch
-    settings (fused Q quantization), sampled (request, KV head) units."""
-    w = synth.WORKLOADS["d256_decode"]()
+    settings (fused Q quantization): a seeded tenth of the (request, KV head)
+    units plus the first and the last."""
+    w = full_workload("d256_decode")
     got = run_gpu(w, impl=impl, ctas_per_sm=2, max_splits=64, q_mode="fp8_fused")
-    units = sorted(set(sample_units(w, 6, seed=3)) | {(w.num_seqs - 1, w.h_k - 1), (0, 0)})
+    units = sorted(set(sample_units(w, -(-w.num_seqs * w.h_k // 10), seed=3)) | {(w.num_seqs - 1, w.h_k - 1),
+                                                                                  (0, 0)})
+    assert 10 * len(units) >= w.num_seqs * w.h_k
     ref, _, _, _ = run_oracle(w, units=units)
     compare(w, got["out"], ref, units, "d256_decode")
     assert np.all(np.isfinite(got["out"]))

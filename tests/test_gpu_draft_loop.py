@@ -38,8 +38,12 @@ def _built():
     build()
 
 
+@pytest.mark.parametrize("q_mode", ["fp8", "fp8_fused"])
 @pytest.mark.parametrize("ctas_per_sm,max_splits", [(2, 1), (8, 16)], ids=["unsplit", "split"])
-def test_draft_steps_in_one_graph(ctas_per_sm, max_splits):
+def test_draft_steps_in_one_graph(ctas_per_sm, max_splits, q_mode):
+    """q_mode fp8: cache write, length advance, mj_quantize_q, decode, merge;
+    fp8_fused: the decode kernel quantizes Q and follows the length advance
+    directly, so it must see that kernel's write."""
     import torch
 
     import paged_fp8_decode_gb300 as mj
@@ -69,14 +73,15 @@ def test_draft_steps_in_one_graph(ctas_per_sm, max_splits):
     kv = paged_kv_from_workload(w, dev)
     kv.seq_lens.copy_(torch.from_numpy(base))
     step = DecodeStep(max_num_seqs=B, q_len=1, h_q=w.h_q, h_k=hk, d=d, ctas_per_sm=ctas_per_sm,
-                      max_splits=max_splits, margin=K, causal=w.causal, impl=mj.MJ_IMPL_AUTO)
+                      max_splits=max_splits, margin=K, causal=w.causal, impl=mj.MJ_IMPL_AUTO, q_mode=q_mode)
     step.plan(base, B)  # once, with K tokens of headroom
     torch.cuda.synchronize()
     q_dev = [q.to(dev) for q in q_steps]
     kv_dev = [t.to(dev) for t in kv_new]
     slot_dev = [torch.from_numpy(s_).to(dev) for s_ in slots]
     outs = [torch.zeros(B, w.h_q, d, dtype=torch.bfloat16, device=dev) for _ in range(K)]
-    args = [step.args(kv, outs[s], B, w.softmax_scale) for s in range(K)]
+    args = [step.args(kv, outs[s], B, w.softmax_scale, q=q_dev[s] if q_mode == "fp8_fused" else None)
+            for s in range(K)]
 
     def draft_steps():
         for s in range(K):

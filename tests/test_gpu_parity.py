@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import synth
-from tests._harness import SENTINEL, all_units, compare, run_gpu, run_oracle, sample_units
+from tests._harness import SENTINEL, all_units, compare, full_workload, run_gpu, run_oracle, sample_units
 
 pytestmark = pytest.mark.gpu
 
@@ -145,24 +145,41 @@ FULL = {
     "long_single": dict(ctas_per_sm=2, max_splits=64),
     "spec_verify": dict(ctas_per_sm=4, max_splits=64, kv_stages=4),
     "spec_verify_noncausal": dict(ctas_per_sm=4, max_splits=64, kv_stages=4),
-    "fp6_decode": dict(ctas_per_sm=2, max_splits=64, kv_stages=6),
+    "fp6_decode": dict(ctas_per_sm=2, max_splits=64, kv_stages=4),
 }
+
+
+# which units each full-size configuration compares with the oracle: all of
+# them where the oracle finishes in seconds, else a seeded tenth plus the
+# first and last request (the last is padding in spec_verify)
+ALL_UNITS = {"qwen3_8b_decode", "spec_verify", "spec_verify_noncausal"}
+
+
+def full_size_units(w, name, seed=3):
+    if name in ALL_UNITS:
+        return all_units(w)
+    n = max(1, -(-w.num_seqs * w.h_k // 10))
+    units = set(sample_units(w, n, seed=seed)) | {(w.num_seqs - 1, 0), (0, w.h_k - 1)}
+    return sorted(units)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("name", list(FULL))
-def test_full_size_sampled(impl, name):
-    w = synth.WORKLOADS[name]()
+def test_full_size(impl, name):
+    w = full_workload(name)
     _skip_unsupported(impl, w)
     got = run_gpu(w, impl=impl, **FULL[name])
-    units = sample_units(w, 6, seed=3)
-    # always include the last request (padding in spec_verify) and request 0
-    units = sorted(set(units) | {(w.num_seqs - 1, 0), (0, w.h_k - 1)})
-    ref, _, _, _ = run_oracle(w, units=units)
+    units = full_size_units(w, name)
+    total = w.num_seqs * w.h_k
+    assert len(units) == total if name in ALL_UNITS else 10 * len(units) >= total
+    ref, lse, _, _ = run_oracle(w, units=units)
     compare(w, got["out"], ref, units, name)
     real_rows = np.repeat(w.seq_lens > 0, w.q_len)
     assert np.all(np.isfinite(got["out"][real_rows]))
     assert np.all(got["out"][~real_rows] == SENTINEL)
+    for b, g in units:
+        if w.seq_lens[b] > 0:
+            np.testing.assert_allclose(got["lse"][b, g], lse[b, g], atol=2e-3, rtol=1e-4)
     assert got["status"] == 0
 
 
@@ -250,7 +267,7 @@ def test_bf16_q_split_and_full_size(impl):
     assert got["info"]["with_reduction"]
     ref, _, _, _ = run_oracle(w, q_mode="bf16")
     compare(w, got["out"], ref, all_units(w), "split bf16 Q")
-    w = synth.WORKLOADS["qwen3_8b_decode"]()
+    w = full_workload("qwen3_8b_decode")
     got = run_gpu(w, impl=impl, ctas_per_sm=2, max_splits=64, kv_stages=6, q_mode="bf16")
     units = sorted(set(sample_units(w, 6, seed=5)) | {(w.num_seqs - 1, w.h_k - 1)})
     ref, _, _, _ = run_oracle(w, units=units, q_mode="bf16")
@@ -295,7 +312,7 @@ def test_fused_quantize_is_bit_identical(impl, name):
 
 
 def test_fused_quantize_full_size():
-    w = synth.WORKLOADS["qwen3_8b_decode"]()
+    w = full_workload("qwen3_8b_decode")
     a = run_gpu(w, impl=2, **FULL["qwen3_8b_decode"])
     b = run_gpu(w, impl=2, q_mode="fp8_fused", **FULL["qwen3_8b_decode"])
     assert np.array_equal(a["out"], b["out"]) and b["status"] == 0

@@ -4,8 +4,10 @@ It serves callers that cannot allocate device memory (an engine whose
 KV-cache pool owns nearly all of HBM, a plugin under a framework's own
 caching allocator): the split-KV partials live in a fixed array compiled into
 the library. Checked here against the workspace-based entry points
-(mj_decode_attention + mj_merge_lse) on a workload that really splits, on
-two calls in a row, within the tolerance of the parity tests. This file is
+(mj_decode_attention + mj_merge_lse) and against the CPU oracle on a
+workload that really splits, on two calls in a row, within the tolerance of
+the parity tests; and its status word (mj_noalloc_status) reports a page id
+out of range and is cleared by the read. This file is
 collected last so that a run stopping at the first failure has run every
 other test first; it also passes on its own in a fresh process.
 """
@@ -16,7 +18,7 @@ import numpy as np
 import pytest
 
 import synth
-from tests._harness import SENTINEL, all_units, compare
+from tests._harness import SENTINEL, all_units, compare, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -58,6 +60,7 @@ def test_noalloc_matches_workspace_entry_points(ready):
     torch.cuda.synchronize()
     ref_np = ref.float().cpu().numpy()
 
+    oracle_out, _, _, _ = run_oracle(w)
     lib = mj.load_library()
     stream = torch.cuda.current_stream()
     for call in range(2):
@@ -69,7 +72,9 @@ def test_noalloc_matches_workspace_entry_points(ready):
         torch.cuda.synchronize()
         got = out.float().cpu().numpy()
         assert np.all(np.isfinite(got))
-        compare(w, got, ref_np, all_units(w), f"no-alloc call {call}")
+        compare(w, got, ref_np, all_units(w), f"no-alloc call {call} vs the workspace path")
+        compare(w, got, oracle_out, all_units(w), f"no-alloc call {call} vs the oracle")
+    assert mj.mj_noalloc_status(stream) == 0
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch(ready):
@@ -86,3 +91,23 @@ def test_noalloc_rejects_plans_beyond_its_scratch(ready):
     assert e.value.status == mj.MJ_ERR_CAPACITY
     torch.cuda.synchronize()
     assert np.all(out.float().cpu().numpy() == SENTINEL)  # nothing was enqueued
+
+
+def test_noalloc_status_reports_a_bad_page(ready):
+    """A block-table entry past the pool: the CUDA-core kernel skips that
+    page and records it in the scratch's status word, which
+    mj_noalloc_status reads (bit 1) and clears."""
+    torch = ready
+    import paged_fp8_decode_gb300 as mj
+
+    w, kv, q, step, info = _setup(torch, max_splits=16)
+    stream = torch.cuda.current_stream()
+    assert mj.mj_noalloc_status(stream) == 0
+    kv.block_table[0, 3] = w.num_pages + 5
+    out = torch.full((w.num_seqs * w.q_len, w.h_q, w.d), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    mj.mj_quantize_q(q, w.num_seqs, w.q_len, w.h_k, step.q_codes, step.q_descale, stream=stream)
+    a = step.args(kv, out, w.num_seqs, w.softmax_scale)
+    a.impl = mj.MJ_IMPL_SIMT
+    mj.mj_decode_attention_noalloc(a, stream)
+    assert mj.mj_noalloc_status(stream) & 1
+    assert mj.mj_noalloc_status(stream) == 0  # the read cleared it

@@ -300,12 +300,13 @@ MJ_API int mj_workspace_status(void* workspace, void* stream, uint32_t* device_s
  * them KV head fastest), fixed by the arguments.
  * Accuracy: the tensor-core kernel scales the softmax weights p to the row's
  * running max (p <= 2^8.6) and carries each in e4m3 terms: hi = e4m3(p) and
- * lo = e4m3(p - hi), and where p < 1/4 the same split of (p - hi - lo) * 2^10,
- * weighed 2^-10; the row sum l adds the p themselves. Every weight is then
- * within max(2^-8 p, 2^-20) of its value, so keys down to 27 binades (about
- * 19 nats) below the row's max keep their weight, and the output of a row of
- * N keys is off by at most (2^-8 + N * 2^-28) * max|V|. MJ_IMPL_SIMT keeps
- * the weights in float32.
+ * lo = e4m3(p - hi), within max(2^-8 p, 2^-10) of p; where weights below 1/4
+ * are many (more than 1024 per row in a CTA's key range) it adds, for them,
+ * the same split of (p - hi - lo) * 2^10 weighed 2^-10, which brings every
+ * weight within max(2^-8 p, 2^-20). The row sum l adds the p themselves. So
+ * keys down to 27 binades (about 19 nats) below the row's max keep their
+ * weight, and the output of a row of N keys is off by at most
+ * (2^-7 + N * 2^-28) * max|V|. MJ_IMPL_SIMT keeps the weights in float32.
  * Ordering: with q_mode MJ_Q_FP8 the tensor-core launch may begin before the
  * preceding kernel on `stream` has finished (programmatic dependent launch:
  * only its Q reads wait for that kernel), so that kernel must be the

@@ -702,6 +702,8 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
     // chunk (bit j: buffer j); at first every buffer (shared memory starts
     // with arbitrary contents)
     uint32_t b_dirty = (1u << NSB) - 1u;
+    constexpr int kSmallBudget = 8 / TP;  // iterations whose weights below 1/4 went with pair A alone
+    int n_small = 0;
 
     // TP tiles per iteration: with few rows, the two S buffers are processed
     // together (256 keys), so the row-max reduction, the cross-warp exchange
@@ -853,16 +855,23 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
             }
         }
       }
-      // Pair B is only needed where some p of the warp lies in (0, 1/4);
-      // the same choice for the whole warp, so the common case (every key of
-      // the warp within 10 binades of its row's max) pays nothing for it:
-      // there pair A alone is within 2^-8 p of every p.
-      bool need_b = false;
+      // Pair A alone is within 2^-8 p of every p >= 1/4 and within 2^-10 of
+      // every smaller one. A thread lets up to kSmallBudget of its
+      // iterations with a weight below 1/4 (the smallest nonzero one tells)
+      // go with pair A alone: that is at most TP kSmallBudget = 8 such keys
+      // per row and thread, 1024 per row, 2^-10 each against a row sum of at
+      // least 2^8: 2^-8 of it. Past that budget its warp adds pair B to every
+      // iteration that holds small weights. Typical rows (keys within 10
+      // binades of their max, bar a few) never pay for pair B; long rows far
+      // below one dominant key do.
+      float pmin = INFINITY;
 #pragma unroll
       for (int a = 0; a < TP; ++a)
 #pragma unroll
-        for (int r = 0; r < NR; ++r) need_b |= s[a][r] > 0.f && s[a][r] < 0.25f;
-      need_b = __any_sync(0xFFFFFFFFu, need_b);
+        for (int r = 0; r < NR; ++r) pmin = fminf(pmin, (all_vis || s[a][r] > 0.f) ? s[a][r] : INFINITY);
+      const int small = pmin < 0.25f ? 1 : 0;
+      const bool need_b = __any_sync(0xFFFFFFFFu, n_small + small > kSmallBudget);
+      if (!need_b) n_small += small;
 
       // This key's column of P^T: term k of row r at byte k * NR + r (k: A hi,
       // A lo, B hi, B lo) of 16-column block (byte / 16), the key's 16-byte

@@ -37,9 +37,20 @@ __global__ void __launch_bounds__(D) merge_kernel(DecodeParams p) {
   const int64_t span = int64_t(p.chunk_tiles) * kKvTile;
   const int live = int(min(int64_t(ns), (int64_t(L) + span - 1) / span));  // splits with >= 1 key
 
-  // max logit over the live splits
-  float mloc = -INFINITY;
-  for (int s = c; s < live; s += D) mloc = fmaxf(mloc, p.m_part[part_index(p, b, s, g, row)]);
+  // each thread loads the (m, l) of its first two splits once (any further
+  // ones, beyond 2 D splits, twice): max logit over the live splits
+  float ml[2] = {-INFINITY, -INFINITY}, ll[2] = {0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int s = c + k * D;
+    if (s < live) {
+      const int64_t idx = part_index(p, b, s, g, row);
+      ml[k] = p.m_part[idx];
+      ll[k] = p.l_part[idx];
+    }
+  }
+  float mloc = fmaxf(ml[0], ml[1]);
+  for (int s = c + 2 * D; s < live; s += D) mloc = fmaxf(mloc, p.m_part[part_index(p, b, s, g, row)]);
   mloc = warp_max(mloc);
   if (lane == 0) red[warp] = mloc;
   __syncthreads();
@@ -49,11 +60,20 @@ __global__ void __launch_bounds__(D) merge_kernel(DecodeParams p) {
   __syncthreads();
 
   // split weights
+  auto weight = [&](float ms, float ls) { return (M == -INFINITY || ms == -INFINITY) ? 0.f : fast_exp2(ms - M) * ls; };
   float wloc = 0.f;
-  for (int s = c; s < live; s += D) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int s = c + k * D;
+    if (s < live) {
+      const float wgt = weight(ml[k], ll[k]);
+      wsh[s] = wgt;
+      wloc += wgt;
+    }
+  }
+  for (int s = c + 2 * D; s < live; s += D) {
     const int64_t idx = part_index(p, b, s, g, row);
-    const float ms = p.m_part[idx];
-    const float wgt = (M == -INFINITY || ms == -INFINITY) ? 0.f : fast_exp2(ms - M) * p.l_part[idx];
+    const float wgt = weight(p.m_part[idx], p.l_part[idx]);
     wsh[s] = wgt;
     wloc += wgt;
   }
@@ -64,19 +84,17 @@ __global__ void __launch_bounds__(D) merge_kernel(DecodeParams p) {
 #pragma unroll
   for (int w2 = 0; w2 < kWarps; ++w2) wsum += red[w2];
 
-  // weighted channel sum
+  // weighted channel sum: eight independent loads in flight per thread
   const float* op = p.o_part + part_index(p, b, 0, g, row) * D + c;
   const int64_t split_stride = int64_t(p.h_k) * p.n_q * D;  // part_index step per split
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int s = 0;
-  for (; s + 4 <= live; s += 4) {
-    a0 = fmaf(wsh[s + 0], op[int64_t(s + 0) * split_stride], a0);
-    a1 = fmaf(wsh[s + 1], op[int64_t(s + 1) * split_stride], a1);
-    a2 = fmaf(wsh[s + 2], op[int64_t(s + 2) * split_stride], a2);
-    a3 = fmaf(wsh[s + 3], op[int64_t(s + 3) * split_stride], a3);
+  for (; s + 8 <= live; s += 8) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = fmaf(wsh[s + k], op[int64_t(s + k) * split_stride], a[k]);
   }
-  for (; s < live; ++s) a0 = fmaf(wsh[s], op[int64_t(s) * split_stride], a0);
-  const float acc = (a0 + a1) + (a2 + a3);
+  for (; s < live; ++s) a[0] = fmaf(wsh[s], op[int64_t(s) * split_stride], a[0]);
+  const float acc = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 
   const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
   const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;

@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   // TP tiles per softmax iteration; NSB S and P buffers let QK run up to
   // NSB - 1 tiles ahead of PV, so the softmax of a tile never waits for
   // the QK product of the next.
-  constexpr int TP = NR <= 8 ? 2 : 1;
+  constexpr int TP = (NR <= 8 || (NR == 16 && QM != 1 && !PK)) ? 2 : 1;
   constexpr int NSB = tc_nsb(NR);
   static_assert(NSB >= 2 * TP, "S / P buffers");
   // TMEM: NSB S buffers (NQK columns each), DH O accumulators (NPV columns each)
@@ -248,36 +248,6 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  // The launch may overlap the end of the preceding kernel on the stream
-  // (programmatic dependent launch). With bf16 Q (as is, or quantized here)
-  // that kernel may have written anything read below (seq_lens, the KV
-  // cache, the plan), so every thread waits for it before reading. With fp8
-  // codes the preceding kernel is mj_quantize_q, which wrote only the Q
-  // codes and descales: only the softmax warps wait, before they read them.
-  if constexpr (QM != 0) tc::grid_dependency_wait();
-
-  // CTA x = (work row, KV head) with the head fastest: the CTAs that run
-  // together stream the same requests' pages (with token-major layouts the
-  // heads of a page interleave, so they share DRAM rows)
-  const int g = int(blockIdx.x % unsigned(p.h_k));
-  const int4 w = reinterpret_cast<const int4*>(p.work)[blockIdx.x / unsigned(p.h_k)];
-  const int b = w.x;
-  if (w.z <= w.y || b < 0 || b >= p.num_seqs) return;
-  if (p.with_reduction && (w.w < 0 || w.w >= p.max_splits || b >= p.part_seqs)) {
-    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPlan);
-    return;
-  }
-  const int L = p.seq_lens[b];
-  if (L <= 0) return;
-  const int64_t k0 = int64_t(w.y) * kKvTile;
-  const int64_t k1 = min(int64_t(w.z) * kKvTile, int64_t(L));
-  if (k1 <= k0) return;
-  const int r0 = blockIdx.y * p.tw;
-  const int nr = min(min(p.tw, p.n_q - r0), NR);
-  if (nr <= 0) return;
-  const int ntiles = int((k1 - k0 + kKvTile - 1) / kKvTile);
-  // the last tile ends before k0 + ntiles * 128: its V rows past the end get zeroed
-  const bool last_partial = k0 + int64_t(ntiles) * kKvTile > k1;
   const int stages = p.kv_stages;
 
   const TcSmem lay = tc_smem_layout(stages, NQK, NPV, NSB, DH);
@@ -324,6 +294,38 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort = &ctl.abort;
 
+  // The launch may overlap the end of the preceding kernel on the stream
+  // (programmatic dependent launch): the set-up above reads nothing that
+  // kernel writes. With bf16 Q (as is, or quantized here) that kernel may
+  // have written anything read below (seq_lens, the KV cache, the plan), so
+  // every thread waits for it here. With fp8 codes the preceding kernel is
+  // mj_quantize_q, which wrote only the Q codes and descales: only the
+  // softmax warps wait, before they read them.
+  if constexpr (QM != 0) tc::grid_dependency_wait();
+
+  // CTA x = (work row, KV head) with the head fastest: the CTAs that run
+  // together stream the same requests' pages (with token-major layouts the
+  // heads of a page interleave, so they share DRAM rows). A CTA with
+  // nothing to do (an empty work row, a padding request, a split past the
+  // end, no rows in its tile) goes straight to the teardown.
+  const int g = int(blockIdx.x % unsigned(p.h_k));
+  const int4 w = reinterpret_cast<const int4*>(p.work)[blockIdx.x / unsigned(p.h_k)];
+  const int b = w.x;
+  bool active = w.z > w.y && b >= 0 && b < p.num_seqs;
+  if (active && p.with_reduction && (w.w < 0 || w.w >= p.max_splits || b >= p.part_seqs)) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPlan);
+    active = false;
+  }
+  const int L = active ? p.seq_lens[b] : 0;
+  const int64_t k0 = int64_t(w.y) * kKvTile;
+  const int64_t k1 = min(int64_t(w.z) * kKvTile, int64_t(L));
+  const int r0 = blockIdx.y * p.tw;
+  const int nr = min(min(p.tw, p.n_q - r0), NR);
+  active = active && L > 0 && k1 > k0 && nr > 0;
+  const int ntiles = active ? int((k1 - k0 + kKvTile - 1) / kKvTile) : 0;
+  // the last tile ends before k0 + ntiles * 128: its V rows past the end get zeroed
+  const bool last_partial = k0 + int64_t(ntiles) * kKvTile > k1;
+
   // TMEM columns: S buffer j % NSB at [(j % NSB) NQK, ...), the O accumulators
   // after them (sub-tile dh at tO + dh * NPV)
   auto tS = [&](int j) { return tmem + uint32_t((j % NSB) * NQK); };
@@ -332,6 +334,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   auto bs = [&](int j) { return j % NSB; };
   auto bp = [&](int j) { return uint32_t(j / NSB) & 1u; };
 
+  if (active) {
   if (warp == 0 || warp == kVProducerWarp) {
     // ======================= TMA producers ==================================
     // warp 0 loads the K tiles (ring entries u = 2i), warp kVProducerWarp the
@@ -1046,6 +1049,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
       }
     }
   }
+  }  // active
 
   // ---- teardown ------------------------------------------------------------
   if (*abort && tid == 0) atomicOr(p.status, kStatusTimeout);

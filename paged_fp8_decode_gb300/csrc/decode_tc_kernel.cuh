@@ -838,7 +838,9 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
       }
 
       // p = 2^(t - m_ref + 8) of every (key, row) of the iteration, in place
-      // of s; 0 where the row does not see the key
+      // of s; 0 where the row does not see the key. pmin: the smallest
+      // weight of a visible key (for the pair-B budget below).
+      float pmin = INFINITY;
       {
         float c8[NR];
 #pragma unroll
@@ -847,7 +849,10 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
 #pragma unroll
           for (int a = 0; a < TP; ++a)
 #pragma unroll
-            for (int r = 0; r < NR; ++r) s[a][r] = fast_exp2(fmaf(s[a][r], scale, c8[r]));
+            for (int r = 0; r < NR; ++r) {
+              s[a][r] = fast_exp2(fmaf(s[a][r], scale, c8[r]));
+              pmin = fminf(pmin, s[a][r]);
+            }
         } else {
 #pragma unroll
           for (int a = 0; a < TP; ++a)
@@ -855,6 +860,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
             for (int r = 0; r < NR; ++r) {
               const bool vis = valid[a] && key[a] <= lim[r] && m_ref[r] != -INFINITY;
               s[a][r] = vis ? fast_exp2(fmaf(s[a][r], scale, c8[r])) : 0.f;
+              pmin = fminf(pmin, vis ? s[a][r] : INFINITY);
             }
         }
       }
@@ -867,11 +873,6 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
       // iteration that holds small weights. Typical rows (keys within 10
       // binades of their max, bar a few) never pay for pair B; long rows far
       // below one dominant key do.
-      float pmin = INFINITY;
-#pragma unroll
-      for (int a = 0; a < TP; ++a)
-#pragma unroll
-        for (int r = 0; r < NR; ++r) pmin = fminf(pmin, (all_vis || s[a][r] > 0.f) ? s[a][r] : INFINITY);
       const int small = pmin < 0.25f ? 1 : 0;
       const bool need_b = __any_sync(0xFFFFFFFFu, n_small + small > kSmallBudget);
       if (!need_b) n_small += small;

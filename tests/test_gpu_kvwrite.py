@@ -151,3 +151,33 @@ def test_write_full_size_sampled(kv_format):
             off = (s // c.page_size) * sp + (s % c.page_size) * stt + g * sh
             assert np.array_equal(gk[off:off + rb], c.k_pool[off:off + rb])
     del torch, mj
+
+
+@pytest.mark.parametrize("scale_bits", [0x3F800000, 0x40E00000, 0x40400000, 0x3DCCCCCD, 0x3FFFFFFF, 0x42EEEEEF,
+                                        0x35800000, 0x4493E000, 0x3F7FFFFF, 0x3C23D70A])
+def test_e4m3_write_every_bf16_value(scale_bits):
+    """Every finite bf16 value through the e4m3 write with one scale: the
+    codes must be those of the IEEE float32 quotient, rounded to nearest even
+    and saturated (the oracle). The scales include 1, 7 (the hand-worked tie
+    case of the Q quantization), 3, 0.1, the largest and the smallest
+    significands (0x3FFFFFFF, 0x3F7FFFFF), and tiny and large values."""
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = (bits & 0x7F80) != 0x7F80
+    vals = bits[finite].astype(np.uint16)
+    n = -(-vals.size // 128) * 128
+    row = np.zeros(n, dtype=np.uint16)
+    row[: vals.size] = vals
+    kb = row.reshape(-1, 1, 128)
+    vb = kb[::-1].copy()
+    T = kb.shape[0]
+    scale = np.array([scale_bits], dtype=np.uint32).view(np.float32)
+    c = synth.WriteCase(name=f"every_bf16_{scale_bits:08x}", key_bf16=kb, value_bf16=vb,
+                        key=(kb.astype(np.uint32) << 16).view(np.float32), value=(vb.astype(np.uint32) << 16).view(np.float32),
+                        slots=np.arange(T, dtype=np.int64), k_pool=np.zeros(T * 128, np.uint8),
+                        v_pool=np.zeros(T * 128, np.uint8), kv_strides=(16 * 128, 128, 16 * 128), page_size=16,
+                        num_pages=T // 16 + 1, kv_format="fp8", k_scale=scale, v_scale=scale, scale_per_head=False)
+    c.k_pool = np.zeros(c.num_pages * 16 * 128, np.uint8)
+    c.v_pool = np.zeros(c.num_pages * 16 * 128, np.uint8)
+    kp, vp, _ = run_gpu_write(c)
+    okp, ovp = run_oracle_write(c)
+    assert np.array_equal(kp, okp) and np.array_equal(vp, ovp)

@@ -19,8 +19,9 @@ scales, HND, 16384 pages drawn from a 20000-page pool). Prints ONE JSON line.
 * ``e2e``: the same metric end to end through the C ABI from pinned host
   buffers: every step plans on the host, uploads its inputs (Q, seq_lens,
   block table) and its plan, runs the kernels and copies O back to pinned
-  host memory, where the host reads it. Two sets of buffers let step n's
-  copies overlap step n - 1's kernels (a serving loop's pipelining).
+  host memory, where the host reads it. Two sets of buffers, each replaying
+  one captured CUDA graph of that device work on its own stream, let
+  consecutive steps overlap (a serving loop's pipelining).
 * ``roofline``: the kernel the dispatch runs (``mj_decode_kernel``), KV
   bytes per launch / the average duration of back-to-back decode launches,
   against the measured HBM copy bandwidth.
@@ -561,20 +562,22 @@ def measure_config(name: str, dev, peak: float, peak_kind: str, q_mode: str, ste
 def e2e_pipelined(w, base, dev, knobs, q_mode: str, impl: int, n_steps: int, dist=None) -> dict:
     """The metric end to end through the C ABI from pinned host buffers.
 
-    Every step: plan on the host (mj_plan_split_kv) and upload it
-    (mj_plan_upload), copy the step's inputs (bf16 Q, seq_lens, the block
-    table: one packed pinned buffer, one copy) to the device, run the
-    kernels, copy O back to pinned host memory and read it on the host. Two
-    sets of device buffers alternate, and the copies run on their own
-    streams, so step n's uploads and step n - 1's download overlap the
-    kernels of the step between them; the host reads step n's result two
-    steps later, before its buffer is reused."""
+    Every step plans on the host (mj_plan_split_kv into pinned staging),
+    copies the step's inputs (bf16 Q, seq_lens, the block table: one packed
+    pinned buffer, one copy) and its plan (mj_plan_upload) to the device,
+    runs the kernels, copies O back to pinned host memory and reads it on the
+    host. Two sets of buffers alternate, each with its own stream, and each
+    set's device work (the uploads, the kernels, the download) is one CUDA
+    graph captured once and replayed every step, so step n's copies and
+    kernels overlap step n - 1's; the host reads step n's result two steps
+    later, before it plans into that set's buffers again."""
     import numpy as np
     import torch
 
     from dataclasses import replace
 
-    from paged_fp8_decode_gb300 import DecodeStep, mj_decode_attention, mj_merge_lse, mj_quantize_q
+    import paged_fp8_decode_gb300 as mj
+    from paged_fp8_decode_gb300 import DecodeStep
     from paged_fp8_decode_gb300.step import q_from_workload
 
     q0 = q_from_workload(w, "cpu")
@@ -593,55 +596,67 @@ def e2e_pipelined(w, base, dev, knobs, q_mode: str, impl: int, n_steps: int, dis
     host_in[:qb].copy_(q0.view(torch.uint8).reshape(-1))
     host_in[off_l:off_l + lb].copy_(torch.from_numpy(np.ascontiguousarray(w.seq_lens)).view(torch.uint8))
     host_in[off_b:off_b + bb].copy_(torch.from_numpy(np.ascontiguousarray(w.block_table)).view(torch.uint8).reshape(-1))
-    compute = torch.cuda.current_stream(dev)
-    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    lens_np = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
     slots = []
     for k in range(2):
+        stream = torch.cuda.Stream(dev)
         dbuf = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         q = dbuf[:qb].view(torch.bfloat16).view(q0.shape)
-        # the resident cache and scales, with this slot's seq_lens and block table
+        # the resident cache and scales, with this set's seq_lens and block table
         kv = replace(base, seq_lens=dbuf[off_l:off_l + lb].view(torch.int32),
                      block_table=dbuf[off_b:off_b + bb].view(torch.int32).view(w.block_table.shape))
         out = torch.empty(w.num_seqs * w.q_len, w.h_q, w.d, dtype=torch.bfloat16, device=dev)
         st = DecodeStep(max_num_seqs=w.num_seqs, q_len=w.q_len, h_q=w.h_q, h_k=w.h_k, d=w.d, ctas_per_sm=cps,
                         max_splits=msplit, causal=w.causal, impl=impl, kv_stages=stages, device=dev, q_mode=q_mode)
-        slots.append({"dbuf": dbuf, "q": q, "kv": kv, "out": out, "step": st, "args": None,
+        slots.append({"stream": stream, "dbuf": dbuf, "q": q, "kv": kv, "out": out, "step": st,
                       "out_host": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
-                      "done": torch.cuda.Event(), "in_ready": torch.cuda.Event(), "out_ready": torch.cuda.Event(),
-                      "pending": False, "used": False})
+                      "done": torch.cuda.Event(), "pending": False, "graph": torch.cuda.CUDAGraph()})
+
+    def host_plan(sl):
+        st = sl["step"]
+        return mj.mj_plan_split_kv(lens_np, w.num_seqs, w.q_len, w.h_q, w.h_k, st.sm_count, st.ctas_per_sm,
+                                   st.max_splits, st.margin, st.pad_to, work_out=st.work_host,
+                                   n_splits_out=st.nsplit_host)
+
+    def device_work(sl, info):
+        st, s_ = sl["step"], sl["stream"]
+        sl["dbuf"].copy_(host_in, non_blocking=True)
+        mj.mj_plan_upload(st.work_host, st.nsplit_host, st.work_dev, st.nsplit_dev, st.pad_to, w.num_seqs, s_)
+        st.plan_info = dict(info, num_seqs=w.num_seqs)
+        a = st.args(sl["kv"], sl["out"], w.num_seqs, w.softmax_scale, q=sl["q"])
+        if q_mode == "fp8":
+            mj.mj_quantize_q(sl["q"], w.num_seqs, w.q_len, w.h_k, st.q_codes, st.q_descale, q_mul=sl["kv"].q_mul,
+                             stream=s_)
+        mj.mj_decode_attention(a, s_)
+        mj.mj_merge_lse(a, s_)
+        sl["out_host"].copy_(sl["out"], non_blocking=True)
+
+    # one eager step per set (first-call set-up happens outside the graphs),
+    # then the capture of each set's device work
+    for sl in slots:
+        info = host_plan(sl)
+        with torch.cuda.stream(sl["stream"]):
+            device_work(sl, info)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(sl["graph"], stream=sl["stream"]):
+            device_work(sl, info)
+        torch.cuda.synchronize(dev)
     reads = []
 
     def read(sl):
-        sl["out_ready"].synchronize()
+        sl["done"].synchronize()
         reads.append(float(sl["out_host"][0, 0, 0]))  # the host reads the step's result
         sl["pending"] = False
 
     def one(n):
         sl = slots[n & 1]
         if sl["pending"]:
-            read(sl)  # step n - 2's result, before its buffers are reused
-        if sl["used"]:
-            copy_in.wait_event(sl["done"])  # step n - 2's kernels are done with this slot's inputs
-        info = sl["step"].plan(w.seq_lens, w.num_seqs, copy_in)
-        with torch.cuda.stream(copy_in):
-            sl["dbuf"].copy_(host_in, non_blocking=True)
-        sl["in_ready"].record(copy_in)
-        compute.wait_event(sl["in_ready"])
-        if sl["args"] is None:
-            sl["args"] = sl["step"].args(sl["kv"], sl["out"], w.num_seqs, w.softmax_scale, q=sl["q"])
-        sl["args"].with_reduction = 1 if info["with_reduction"] else 0
-        sl["args"].chunk_tiles = info["chunk_tiles"]
-        if q_mode == "fp8":
-            mj_quantize_q(sl["q"], w.num_seqs, w.q_len, w.h_k, sl["step"].q_codes, sl["step"].q_descale,
-                          q_mul=sl["kv"].q_mul, stream=compute)
-        mj_decode_attention(sl["args"], compute)
-        mj_merge_lse(sl["args"], compute)
-        sl["done"].record(compute)
-        copy_out.wait_event(sl["done"])
-        with torch.cuda.stream(copy_out):
-            sl["out_host"].copy_(sl["out"], non_blocking=True)
-        sl["out_ready"].record(copy_out)
-        sl["pending"] = sl["used"] = True
+            read(sl)  # step n - 2's result, before this set's buffers are reused
+        host_plan(sl)
+        with torch.cuda.stream(sl["stream"]):
+            sl["graph"].replay()
+        sl["done"].record(sl["stream"])
+        sl["pending"] = True
 
     def drain():
         for sl in slots:
@@ -799,8 +814,9 @@ def main_ours(args):
         "e2e": {"value": round(whole_job_gbs(b.kv_bytes, world, e2e["seconds"] / e2e["steps"]), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"], "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
                 "steps": e2e["steps"], "ms_per_step": round(e2e["seconds"] / e2e["steps"] * 1e3, 4),
-                "note": "pipelined over two buffer sets: step n's uploads and step n-1's download overlap the "
-                        "kernels; every step plans, uploads, runs, downloads and is read on the host"},
+                "note": "every step plans on the host, uploads its inputs and plan, runs, downloads O and is read "
+                        "on the host; two buffer sets, each replaying one captured CUDA graph of its uploads, "
+                        "kernels and download on its own stream, so consecutive steps overlap"},
         "gpu_launches": b.launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

@@ -185,6 +185,7 @@ int mj_plan_split_kv(const int32_t* seq_lens_host, int num_seqs, int q_len, int 
                      int sm_count, int ctas_per_sm, int max_splits, int margin, int pad_to,
                      int32_t* work_host, int32_t* n_splits_host, int* chunk_tiles,
                      int* with_reduction, int* slots_out) {
+  const mj::NvtxRange range("mj_plan_split_kv");
   if (num_seqs < 0 || q_len < 1 || h_k < 1 || h_q < 1 || h_q % h_k || sm_count < 1 || ctas_per_sm < 1 ||
       max_splits < 1 || margin < 0 || pad_to < 0)
     return MJ_ERR_INVALID_ARG;
@@ -257,6 +258,7 @@ int mj_plan_split_kv(const int32_t* seq_lens_host, int num_seqs, int q_len, int 
 
 int mj_plan_upload(const int32_t* work_host, const int32_t* n_splits_host, int32_t* work_dev, int32_t* n_splits_dev,
                    int pad_to, int num_seqs, void* stream) {
+  const mj::NvtxRange range("mj_plan_upload");
   if (pad_to < 0 || num_seqs < 0) return MJ_ERR_INVALID_ARG;
   if ((pad_to > 0 && (!work_host || !work_dev)) || (num_seqs > 0 && (!n_splits_host || !n_splits_dev)))
     return MJ_ERR_INVALID_ARG;
@@ -294,6 +296,7 @@ int mj_decode_kernel(const mj_decode_args* args, int* impl) {
 int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, int num_seqs, int q_len,
                   int h_q, int h_k, int d, const float* q_mul, uint8_t* q_codes, float* q_descale,
                   void* stream) {
+  const mj::NvtxRange range("mj_quantize_q");
   if (num_seqs < 0 || q_len < 1 || h_k < 1 || h_q < 1 || h_q % h_k) return MJ_ERR_INVALID_ARG;
   if (!mj::head_dim_ok(d)) return MJ_ERR_UNSUPPORTED;
   if (num_seqs == 0) return MJ_OK;
@@ -319,6 +322,7 @@ int mj_quantize_q(const void* q, int64_t q_tok_stride, int64_t q_head_stride, in
 }
 
 int mj_write_kv(const mj_write_kv_args* a, void* stream) {
+  const mj::NvtxRange range("mj_write_kv");
   if (!a) return MJ_ERR_INVALID_ARG;
   if (a->num_tokens < 0 || a->h_k < 1 || a->num_pages < 0) return MJ_ERR_INVALID_ARG;
   if (!mj::head_dim_ok(a->d)) return MJ_ERR_UNSUPPORTED;
@@ -357,12 +361,14 @@ int mj_workspace_size(int part_seqs, int max_splits, int max_q_len, int h_q, int
 }
 
 int mj_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  const mj::NvtxRange range("mj_workspace_init");
   if (!workspace || workspace_bytes < mj::kWsHeader) return MJ_ERR_INVALID_ARG;
   if (!aligned(workspace, 16)) return MJ_ERR_ALIGNMENT;
   return status_of(cudaMemsetAsync(workspace, 0, mj::kWsHeader, static_cast<cudaStream_t>(stream)));
 }
 
 int mj_workspace_status(void* workspace, void* stream, uint32_t* device_status) {
+  const mj::NvtxRange range("mj_workspace_status");
   if (!workspace || !device_status) return MJ_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t v = 0;
@@ -375,6 +381,7 @@ int mj_workspace_status(void* workspace, void* stream, uint32_t* device_status) 
 }
 
 int mj_decode_attention(const mj_decode_args* args, void* stream) {
+  const mj::NvtxRange range("mj_decode_attention");
   DecodeParams p;
   int st = make_params(args, &p);
   if (st != MJ_OK) return st;
@@ -393,6 +400,7 @@ int mj_decode_attention(const mj_decode_args* args, void* stream) {
 }
 
 int mj_merge_lse(const mj_decode_args* args, void* stream) {
+  const mj::NvtxRange range("mj_merge_lse");
   DecodeParams p;
   int st = make_params(args, &p);
   if (st != MJ_OK) return st;

@@ -3,11 +3,22 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/mj.h"
 
 namespace mj {
+
+// An NVTX range over an exported call (header-only NVTX: a few instructions
+// when no tool is attached), so that a profiler timeline shows which call
+// enqueued which kernels.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kKvTile = 128;   // tokens per KV tile (the plan's unit)
 constexpr int kMaxHeadDim = 256;

@@ -59,6 +59,7 @@ int scratch_on_current_device(cudaStream_t stream, void** out) {
 }  // namespace
 
 extern "C" int mj_decode_attention_noalloc(const mj_decode_args* args, void* stream) {
+  const mj::NvtxRange range("mj_decode_attention_noalloc");
   if (!args) return MJ_ERR_INVALID_ARG;
   size_t need = mj::kWsHeader;
   if (args->with_reduction) {

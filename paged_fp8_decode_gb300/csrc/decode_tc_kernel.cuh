@@ -335,721 +335,721 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   auto bp = [&](int j) { return uint32_t(j / NSB) & 1u; };
 
   if (active) {
-  if (warp == 0 || warp == kVProducerWarp) {
-    // ======================= TMA producers ==================================
-    // warp 0 loads the K tiles (ring entries u = 2i), warp kVProducerWarp the
-    // V tiles (u = 2i + 1), concurrently: a CTA's TMA issue rate, not HBM,
-    // bounds small-page streaming, and two issuing warps double it.
-    const int half = warp == 0 ? 0 : 1;
-    const CUtensorMap* map = half ? &tmap_v : &tmap_k;
-    const uint64_t pol = p.evict_first ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
-    const int ps = p.page_size;
-    const int ppt = kKvTile / ps;
-    const int64_t first_page = k0 / ps;
-    const int64_t npages = (k1 + ps - 1) / ps - first_page;
-    const int32_t* bt = p.block_table + int64_t(b) * p.bt_stride + first_page;
-    const uint32_t page_bytes = uint32_t(ps) * 128u;                 // shared-memory footprint
-    const uint32_t page_tx = uint32_t(ps) * uint32_t(p.row_bytes);  // bytes the copy delivers
-    int64_t batch = -1;
-    int entry = -1;
-    bool ok = true;
-    int issued = 0;  // tiles whose load this warp issued
-    for (int i = 0; i < ntiles && ok; ++i) {
-      // lane j < nvalid issues the load of page j of tile i (one page id per lane)
-      const int nvalid = int(min(int64_t(ppt), npages - int64_t(i) * ppt));
-      const int64_t e0 = int64_t(i) * ppt;
-      if (batch < 0 || e0 + nvalid > batch + 32) {
-        batch = e0;
-        entry = (e0 + lane < npages) ? bt[e0 + lane] : -1;
-      }
-      const int pg = __shfl_sync(0xFFFFFFFFu, entry, int(e0 - batch) + (lane & 7));
-      if (half == 0 && lane < nvalid && (pg < 0 || int64_t(pg) >= p.num_pages)) atomicOr(p.status, kStatusBadPage);
-      const int u = 2 * i + half;
-      const int slot = u % stages;
-      const uint32_t round = uint32_t(u / stages);
-      const uint32_t full = tc::smem_u32(&ctl.full[slot]);
-      if (lane == 0) {
-        ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
-        if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_tx);
-      }
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-      if (ok && lane < nvalid) {
-        // sub-tile dh: channels 128 dh .. 128 dh + 127 (x = 128 dh bytes, 16-byte aligned)
-#pragma unroll
-        for (int dh = 0; dh < DH; ++dh) {
-          const uint32_t dst = ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes + uint32_t(lane) * page_bytes;
-          if (p.tma_head_inner)
-            tc::tma_load_4d(dst, map, full, 128 * dh, g, 0, pg, pol);
-          else
-            tc::tma_load_4d(dst, map, full, 128 * dh, 0, g, pg, pol);
+    if (warp == 0 || warp == kVProducerWarp) {
+      // ======================= TMA producers ==================================
+      // warp 0 loads the K tiles (ring entries u = 2i), warp kVProducerWarp the
+      // V tiles (u = 2i + 1), concurrently: a CTA's TMA issue rate, not HBM,
+      // bounds small-page streaming, and two issuing warps double it.
+      const int half = warp == 0 ? 0 : 1;
+      const CUtensorMap* map = half ? &tmap_v : &tmap_k;
+      const uint64_t pol = p.evict_first ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
+      const int ps = p.page_size;
+      const int ppt = kKvTile / ps;
+      const int64_t first_page = k0 / ps;
+      const int64_t npages = (k1 + ps - 1) / ps - first_page;
+      const int32_t* bt = p.block_table + int64_t(b) * p.bt_stride + first_page;
+      const uint32_t page_bytes = uint32_t(ps) * 128u;                 // shared-memory footprint
+      const uint32_t page_tx = uint32_t(ps) * uint32_t(p.row_bytes);  // bytes the copy delivers
+      int64_t batch = -1;
+      int entry = -1;
+      bool ok = true;
+      int issued = 0;  // tiles whose load this warp issued
+      for (int i = 0; i < ntiles && ok; ++i) {
+        // lane j < nvalid issues the load of page j of tile i (one page id per lane)
+        const int nvalid = int(min(int64_t(ppt), npages - int64_t(i) * ppt));
+        const int64_t e0 = int64_t(i) * ppt;
+        if (batch < 0 || e0 + nvalid > batch + 32) {
+          batch = e0;
+          entry = (e0 + lane < npages) ? bt[e0 + lane] : -1;
         }
-      }
-      if (ok) ++issued;
-      __syncwarp();
-    }
-    if (!PK && half == 1 && ok && last_partial) {
-      // Last, partial V tile: zero its rows past the end (page tails and
-      // stale ring contents may hold NaN codes, and 0 * NaN would reach O
-      // through the PV product), then release it to the MMA issuer. This warp
-      // may wait on the slot's full barrier: its own wait on the slot's empty
-      // barrier showed that the previous occupant has landed and been consumed.
-      const int u = 2 * (ntiles - 1) + 1;
-      const int slot = u % stages;
-      if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-      if (ok) {
-        const int first_dead = int(k1 - (k0 + int64_t(ntiles - 1) * kKvTile));  // rows >= this are past the end
-#pragma unroll
-        for (int dh = 0; dh < DH; ++dh) {
-          uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry + dh * kTileBytes);
-          for (int c = first_dead * 8 + lane; c < kKvTile * 8; c += 32) tile[c] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        tc::fence_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.v_tail));
-      }
-    }
-    if (!ok && lane == 0) {
-      // abort: wait (bounded) for this warp's loads still in flight before the CTA exits
-      const uint64_t t0 = tc::globaltimer_ns();
-      for (int i = max(0, issued - stages); i < issued; ++i) {
+        const int pg = __shfl_sync(0xFFFFFFFFu, entry, int(e0 - batch) + (lane & 7));
+        if (half == 0 && lane < nvalid && (pg < 0 || int64_t(pg) >= p.num_pages)) atomicOr(p.status, kStatusBadPage);
         const int u = 2 * i + half;
-        while (!tc::mbar_try_wait(tc::smem_u32(&ctl.full[u % stages]), uint32_t(u / stages) & 1u) &&
-               tc::globaltimer_ns() - t0 < 100000000ull) {
+        const int slot = u % stages;
+        const uint32_t round = uint32_t(u / stages);
+        const uint32_t full = tc::smem_u32(&ctl.full[slot]);
+        if (lane == 0) {
+          ok = tc::mbar_wait(tc::smem_u32(&ctl.empty[slot]), (round & 1u) ^ 1u, abort, kWaitLimitNs);
+          if (ok) tc::mbar_arrive_expect_tx(full, uint32_t(nvalid) * page_tx);
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (ok && lane < nvalid) {
+          // sub-tile dh: channels 128 dh .. 128 dh + 127 (x = 128 dh bytes, 16-byte aligned)
+#pragma unroll
+          for (int dh = 0; dh < DH; ++dh) {
+            const uint32_t dst = ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes + uint32_t(lane) * page_bytes;
+            if (p.tma_head_inner)
+              tc::tma_load_4d(dst, map, full, 128 * dh, g, 0, pg, pol);
+            else
+              tc::tma_load_4d(dst, map, full, 128 * dh, 0, g, pg, pol);
+          }
+        }
+        if (ok) ++issued;
+        __syncwarp();
+      }
+      if (!PK && half == 1 && ok && last_partial) {
+        // Last, partial V tile: zero its rows past the end (page tails and
+        // stale ring contents may hold NaN codes, and 0 * NaN would reach O
+        // through the PV product), then release it to the MMA issuer. This warp
+        // may wait on the slot's full barrier: its own wait on the slot's empty
+        // barrier showed that the previous occupant has landed and been consumed.
+        const int u = 2 * (ntiles - 1) + 1;
+        const int slot = u % stages;
+        if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (ok) {
+          const int first_dead = int(k1 - (k0 + int64_t(ntiles - 1) * kKvTile));  // rows >= this are past the end
+#pragma unroll
+          for (int dh = 0; dh < DH; ++dh) {
+            uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry + dh * kTileBytes);
+            for (int c = first_dead * 8 + lane; c < kKvTile * 8; c += 32) tile[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          tc::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.v_tail));
         }
       }
-    }
-  } else if (PK && warp >= kConvWarp0) {
-    // ======================= V widening (packed KV) ===========================
-    // Each V tile is widened in place, chunk by chunk, once its load lands.
-    const int ct = tid - kConvWarp0 * 32;  // 0 .. kConvThreads - 1
-    bool ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      const int u = 2 * i + 1;
-      const int slot = u % stages;
-      ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
-      if (!ok) break;
-      uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry);
-#pragma unroll 4
-      for (int k = ct; k < kTileBytes / 16; k += kConvThreads) tile[k] = widen_chunk<KF>(tile[k]);
-      tc::fence_async_smem();
-      tc::mbar_arrive(tc::smem_u32(&ctl.vconv[slot]));
-    }
-  } else if (warp == 1) {
-    // ======================= MMA issuer ======================================
-    if (lane == 0) {
-      // K is read in its own format straight from the packed TMA layout
-      // (kind::f8f6f4 mixes an e2m3 / e3m2 / e2m1 A with the e4m3 Q); V
-      // always arrives as e4m3.
-      constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false) | (mma_kv_type(KF) << 7);
-      // PV: A = V tile (MN-major), B = P (MN-major, no swizzle: [key][16 columns] blocks)
-      constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, true);
-      const uint64_t qdesc = tc::smem_desc(q_addr, 16, 1024, tc::kSwizzle128B);
-      // Event loop: issue QK_nq as soon as K tile nq has landed (at most one
-      // tile ahead of PV: two S buffers), and PV_np as soon as P_np is
-      // written and V tile np has landed. Neither product waits behind the
-      // other's operands.
-      bool ok = tc::mbar_wait(tc::smem_u32(&ctl.q_ready), 0, abort, kWaitLimitNs);
-      int nq = 0, np = 0;
-      uint64_t t_idle = 0;
-      while (ok && np < ntiles) {
-        bool progressed = false;
-        if (nq < ntiles && nq <= np + NSB - 1) {
-          const int u = 2 * nq;
-          const int slot = u % stages;
-          if (tc::mbar_test_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u)) {
-            tc::tc_fence_after();
-#pragma unroll
-            for (int dh = 0; dh < DH; ++dh) {
-              const uint64_t kdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes, 16,
-                                                   1024, tc::kSwizzle128B);
-              const uint64_t qd = qdesc + uint64_t((uint32_t(dh) * kQSub) >> 4);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)  // 128 channels of the sub-tile in steps of 32 bytes
-                tc::umma_f8f6f4(tS(nq), kdesc + uint64_t(2 * k), qd + uint64_t(2 * k), idesc_qk, dh > 0 || k > 0);
-            }
-            tc::umma_commit(tc::smem_u32(&ctl.s_full[bs(nq)]));
-            tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
-            ++nq;
-            progressed = true;
-          }
-        }
-        if (np < nq) {
-          const int u = 2 * np + 1;
-          const int slot = u % stages;
-          // V tile ready: widened (packed), tail-zeroed (last partial e4m3 tile, a
-          // one-shot barrier), else landed
-          const bool tail = !PK && last_partial && np == ntiles - 1;
-          const uint32_t vbar = tc::smem_u32(PK ? &ctl.vconv[slot] : (tail ? &ctl.v_tail : &ctl.full[slot]));
-          const uint32_t vpar = tail ? 0u : uint32_t(u / stages) & 1u;
-          if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[bs(np)]), bp(np)) && tc::mbar_test_wait(vbar, vpar)) {
-            tc::tc_fence_after();
-            // P, MN-major without swizzle: 8-key core groups 128 B apart (LBO),
-            // 16-column blocks 2 KB apart (SBO)
-            const uint64_t pdesc =
-                tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(bs(np)) * p_stride, 128, 2048, 0);
-#pragma unroll
-            for (int dh = 0; dh < DH; ++dh) {
-              const uint64_t vdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes,
-                                                   kTileBytes, 1024, tc::kSwizzle128B);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V, 32 x 16 B of P)
-                tc::umma_f8f6f4(tO + uint32_t(dh * NPV), vdesc + uint64_t(256 * k), pdesc + uint64_t(32 * k), idesc_pv,
-                                (np > 0 || k > 0));
-            }
-            tc::umma_commit(tc::smem_u32(&ctl.o_full[bs(np)]));
-            tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
-            ++np;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_idle = 0;
-        } else {
-          const uint64_t now = tc::globaltimer_ns();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > kWaitLimitNs || *abort) {
-            *abort = 1;
-            ok = false;
-            break;
-          }
-          // back off: this warp shares its SM sub-partition with a softmax
-          // warp, whose issue slots a tight polling loop would take
-          __nanosleep(64);
-        }
-      }
-      if (!ok) {
-        // abort: wait (bounded) until every MMA issued so far has completed
-        tc::umma_commit(tc::smem_u32(&ctl.drain));
+      if (!ok && lane == 0) {
+        // abort: wait (bounded) for this warp's loads still in flight before the CTA exits
         const uint64_t t0 = tc::globaltimer_ns();
-        while (!tc::mbar_try_wait(tc::smem_u32(&ctl.drain), 0) && tc::globaltimer_ns() - t0 < 100000000ull) {
+        for (int i = max(0, issued - stages); i < issued; ++i) {
+          const int u = 2 * i + half;
+          while (!tc::mbar_try_wait(tc::smem_u32(&ctl.full[u % stages]), uint32_t(u / stages) & 1u) &&
+                 tc::globaltimer_ns() - t0 < 100000000ull) {
+          }
         }
       }
-    }
-  } else {
-    // ======================= softmax warpgroup ===============================
-    // Q codes and descales come from the preceding grid (mj_quantize_q) when
-    // it is launched just before: wait for it here only, so that the TMA
-    // producers stream KV meanwhile.
-    tc::grid_dependency_wait();
-    const int xq = tid - kSoftmaxWarp0 * 32;
-    float sc_hi = 0.f, sc_lo = 0.f;  // bf16 Q: logit scales of its hi and lo terms
-    float sq = 1.f;                  // Q quantized here: its descale
-    // max over the 128 softmax threads (the four softmax warps always reach this barrier)
-    auto block_max = [&](float v, int slot) {
-      v = warp_max(v);
-      if (lane == 0) ctl.qamax[slot][warp & 3] = v;
-      tc::named_bar_sync(1, 128);
-      return fmaxf(fmaxf(ctl.qamax[slot][0], ctl.qamax[slot][1]), fmaxf(ctl.qamax[slot][2], ctl.qamax[slot][3]));
-    };
-    // Q tile: DH sub-tiles (channels 128 dh ..) of [NQK rows][128 B], K-major,
-    // 128-byte swizzle: byte c of row r in sub-tile c >> 7, 16-byte chunk
-    // ((c & 127) >> 4) ^ (r & 7)
-    auto q_off = [&](int r, int c) {
-      return lay.q + uint32_t(c >> 7) * kQSub + uint32_t(r * 128 + ((((c & 127) >> 4) ^ (r & 7)) << 4) + (c & 15));
-    };
-    // zero rows r_from .. NQK-1 of every sub-tile
-    auto zero_rows = [&](int r_from) {
-      for (int i = xq; i < (NQK - r_from) * 8 * DH; i += 128) {
-        const int dh = i / ((NQK - r_from) * 8), j = i % ((NQK - r_from) * 8);
-        *reinterpret_cast<uint4*>(smem + lay.q + dh * kQSub + r_from * 128 + j * 16) = make_uint4(0u, 0u, 0u, 0u);
+    } else if (PK && warp >= kConvWarp0) {
+      // ======================= V widening (packed KV) ===========================
+      // Each V tile is widened in place, chunk by chunk, once its load lands.
+      const int ct = tid - kConvWarp0 * 32;  // 0 .. kConvThreads - 1
+      bool ok = true;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        const int u = 2 * i + 1;
+        const int slot = u % stages;
+        ok = tc::mbar_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u, abort, kWaitLimitNs);
+        if (!ok) break;
+        uint4* tile = reinterpret_cast<uint4*>(smem + lay.ring + slot * kEntry);
+#pragma unroll 4
+        for (int k = ct; k < kTileBytes / 16; k += kConvThreads) tile[k] = widen_chunk<KF>(tile[k]);
+        tc::fence_async_smem();
+        tc::mbar_arrive(tc::smem_u32(&ctl.vconv[slot]));
       }
-    };
-    if constexpr (QM == 0) {
-      // Q codes rows r0 .. r0+nr-1 into the Q tile; other rows 0
-      const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * D;
-      for (int i = xq; i < NQK * 8 * DH; i += 128) {
-        const int r = i / (8 * DH), c = (i % (8 * DH)) * 16;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * D + c);
-        *reinterpret_cast<uint4*>(smem + q_off(r, c)) = v;
-      }
-    } else if constexpr (QM == 2) {
-      // mj_quantize_q's recipe, in the kernel: x = bf16 Q (times q_mul), the
-      // scale from the amax over all q_len*h_r rows of (b, g), then e4m3
-      // round-to-nearest-even satfinite, every step an IEEE float32 operation,
-      // so the codes and the descale are the ones that call writes. Thread xq
-      // takes channels xq + 128 dh of every row.
-      auto q_in = [&](int rr, int c) {
-        const int tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
-        float v = bf16_bits_to_float(p.q_bf16[int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c]);
-        if (p.q_mul) v = __fmul_rn(v, p.q_mul[int64_t(h) * D + c]);
-        return v;
-      };
-      // the tile's rows once, into registers (independent loads); the rows of
-      // (b, g) outside the tile only count towards the amax
-      float xr[DH][NR];
-      float am = 0.f;
+    } else if (warp == 1) {
+      // ======================= MMA issuer ======================================
+      if (lane == 0) {
+        // K is read in its own format straight from the packed TMA layout
+        // (kind::f8f6f4 mixes an e2m3 / e3m2 / e2m1 A with the e4m3 Q); V
+        // always arrives as e4m3.
+        constexpr uint32_t idesc_qk = tc::idesc_e4m3(128, NQK, false, false) | (mma_kv_type(KF) << 7);
+        // PV: A = V tile (MN-major), B = P (MN-major, no swizzle: [key][16 columns] blocks)
+        constexpr uint32_t idesc_pv = tc::idesc_e4m3(128, NPV, true, true);
+        const uint64_t qdesc = tc::smem_desc(q_addr, 16, 1024, tc::kSwizzle128B);
+        // Event loop: issue QK_nq as soon as K tile nq has landed (at most one
+        // tile ahead of PV: two S buffers), and PV_np as soon as P_np is
+        // written and V tile np has landed. Neither product waits behind the
+        // other's operands.
+        bool ok = tc::mbar_wait(tc::smem_u32(&ctl.q_ready), 0, abort, kWaitLimitNs);
+        int nq = 0, np = 0;
+        uint64_t t_idle = 0;
+        while (ok && np < ntiles) {
+          bool progressed = false;
+          if (nq < ntiles && nq <= np + NSB - 1) {
+            const int u = 2 * nq;
+            const int slot = u % stages;
+            if (tc::mbar_test_wait(tc::smem_u32(&ctl.full[slot]), uint32_t(u / stages) & 1u)) {
+              tc::tc_fence_after();
 #pragma unroll
-      for (int dh = 0; dh < DH; ++dh) {
-        const int c = xq + 128 * dh;
+              for (int dh = 0; dh < DH; ++dh) {
+                const uint64_t kdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes, 16,
+                                                     1024, tc::kSwizzle128B);
+                const uint64_t qd = qdesc + uint64_t((uint32_t(dh) * kQSub) >> 4);
 #pragma unroll
-        for (int r = 0; r < NR; ++r) xr[dh][r] = r < nr ? q_in(r0 + r, c) : 0.f;
+                for (int k = 0; k < 4; ++k)  // 128 channels of the sub-tile in steps of 32 bytes
+                  tc::umma_f8f6f4(tS(nq), kdesc + uint64_t(2 * k), qd + uint64_t(2 * k), idesc_qk, dh > 0 || k > 0);
+              }
+              tc::umma_commit(tc::smem_u32(&ctl.s_full[bs(nq)]));
+              tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
+              ++nq;
+              progressed = true;
+            }
+          }
+          if (np < nq) {
+            const int u = 2 * np + 1;
+            const int slot = u % stages;
+            // V tile ready: widened (packed), tail-zeroed (last partial e4m3 tile, a
+            // one-shot barrier), else landed
+            const bool tail = !PK && last_partial && np == ntiles - 1;
+            const uint32_t vbar = tc::smem_u32(PK ? &ctl.vconv[slot] : (tail ? &ctl.v_tail : &ctl.full[slot]));
+            const uint32_t vpar = tail ? 0u : uint32_t(u / stages) & 1u;
+            if (tc::mbar_test_wait(tc::smem_u32(&ctl.p_full[bs(np)]), bp(np)) && tc::mbar_test_wait(vbar, vpar)) {
+              tc::tc_fence_after();
+              // P, MN-major without swizzle: 8-key core groups 128 B apart (LBO),
+              // 16-column blocks 2 KB apart (SBO)
+              const uint64_t pdesc =
+                  tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(bs(np)) * p_stride, 128, 2048, 0);
 #pragma unroll
-        for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[dh][r]));
-        for (int rr = 0; rr < p.n_q; ++rr)
-          if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr, c)));
-      }
-      sq = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.0f);
+              for (int dh = 0; dh < DH; ++dh) {
+                const uint64_t vdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes,
+                                                     kTileBytes, 1024, tc::kSwizzle128B);
 #pragma unroll
-      for (int dh = 0; dh < DH; ++dh) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          uint8_t code = 0;
-          if (r < nr) code = __nv_cvt_float_to_fp8(__fdiv_rn(xr[dh][r], sq), __NV_SATFINITE, __NV_E4M3);
-          smem[q_off(r, xq + 128 * dh)] = code;
+                for (int k = 0; k < 4; ++k)  // K = 128 keys in steps of 32 (32 rows x 128 B of V, 32 x 16 B of P)
+                  tc::umma_f8f6f4(tO + uint32_t(dh * NPV), vdesc + uint64_t(256 * k), pdesc + uint64_t(32 * k), idesc_pv,
+                                  (np > 0 || k > 0));
+              }
+              tc::umma_commit(tc::smem_u32(&ctl.o_full[bs(np)]));
+              tc::umma_commit(tc::smem_u32(&ctl.empty[slot]));
+              ++np;
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            t_idle = 0;
+          } else {
+            const uint64_t now = tc::globaltimer_ns();
+            if (t_idle == 0) {
+              t_idle = now;
+            } else if (now - t_idle > kWaitLimitNs || *abort) {
+              *abort = 1;
+              ok = false;
+              break;
+            }
+            // back off: this warp shares its SM sub-partition with a softmax
+            // warp, whose issue slots a tight polling loop would take
+            __nanosleep(64);
+          }
+        }
+        if (!ok) {
+          // abort: wait (bounded) until every MMA issued so far has completed
+          tc::umma_commit(tc::smem_u32(&ctl.drain));
+          const uint64_t t0 = tc::globaltimer_ns();
+          while (!tc::mbar_try_wait(tc::smem_u32(&ctl.drain), 0) && tc::globaltimer_ns() - t0 < 100000000ull) {
+          }
         }
       }
-      zero_rows(NR);  // the rows past the tile
     } else {
-      // bf16 Q as two e4m3 terms: hi = e4m3(x / s_hi) with s_hi = amax/448,
-      // lo = e4m3((x - hi*s_hi) / s_lo) with s_lo = (max |residual|)/448.
-      // hi fills rows 0 .. NR-1 of the Q tile and lo rows NR .. 2NR-1, so one
-      // QK product gives both terms; the logit is s_hi*S_hi + s_lo*S_lo.
-      // Thread xq owns EPT consecutive channels of one row (NR x D values
-      // over 128 threads; EPT divides 128, so they share one sub-tile).
-      constexpr int EPT = NR * DH;
-      const int row = (xq * EPT) / D, c0 = (xq * EPT) % D;
-      float xv[EPT];
+      // ======================= softmax warpgroup ===============================
+      // Q codes and descales come from the preceding grid (mj_quantize_q) when
+      // it is launched just before: wait for it here only, so that the TMA
+      // producers stream KV meanwhile.
+      tc::grid_dependency_wait();
+      const int xq = tid - kSoftmaxWarp0 * 32;
+      float sc_hi = 0.f, sc_lo = 0.f;  // bf16 Q: logit scales of its hi and lo terms
+      float sq = 1.f;                  // Q quantized here: its descale
+      // max over the 128 softmax threads (the four softmax warps always reach this barrier)
+      auto block_max = [&](float v, int slot) {
+        v = warp_max(v);
+        if (lane == 0) ctl.qamax[slot][warp & 3] = v;
+        tc::named_bar_sync(1, 128);
+        return fmaxf(fmaxf(ctl.qamax[slot][0], ctl.qamax[slot][1]), fmaxf(ctl.qamax[slot][2], ctl.qamax[slot][3]));
+      };
+      // Q tile: DH sub-tiles (channels 128 dh ..) of [NQK rows][128 B], K-major,
+      // 128-byte swizzle: byte c of row r in sub-tile c >> 7, 16-byte chunk
+      // ((c & 127) >> 4) ^ (r & 7)
+      auto q_off = [&](int r, int c) {
+        return lay.q + uint32_t(c >> 7) * kQSub + uint32_t(r * 128 + ((((c & 127) >> 4) ^ (r & 7)) << 4) + (c & 15));
+      };
+      // zero rows r_from .. NQK-1 of every sub-tile
+      auto zero_rows = [&](int r_from) {
+        for (int i = xq; i < (NQK - r_from) * 8 * DH; i += 128) {
+          const int dh = i / ((NQK - r_from) * 8), j = i % ((NQK - r_from) * 8);
+          *reinterpret_cast<uint4*>(smem + lay.q + dh * kQSub + r_from * 128 + j * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
+      if constexpr (QM == 0) {
+        // Q codes rows r0 .. r0+nr-1 into the Q tile; other rows 0
+        const uint8_t* qsrc = p.q_codes + ((int64_t(b) * p.h_k + g) * p.n_q + r0) * D;
+        for (int i = xq; i < NQK * 8 * DH; i += 128) {
+          const int r = i / (8 * DH), c = (i % (8 * DH)) * 16;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (r < nr) v = *reinterpret_cast<const uint4*>(qsrc + r * D + c);
+          *reinterpret_cast<uint4*>(smem + q_off(r, c)) = v;
+        }
+      } else if constexpr (QM == 2) {
+        // mj_quantize_q's recipe, in the kernel: x = bf16 Q (times q_mul), the
+        // scale from the amax over all q_len*h_r rows of (b, g), then e4m3
+        // round-to-nearest-even satfinite, every step an IEEE float32 operation,
+        // so the codes and the descale are the ones that call writes. Thread xq
+        // takes channels xq + 128 dh of every row.
+        auto q_in = [&](int rr, int c) {
+          const int tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
+          float v = bf16_bits_to_float(p.q_bf16[int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c]);
+          if (p.q_mul) v = __fmul_rn(v, p.q_mul[int64_t(h) * D + c]);
+          return v;
+        };
+        // the tile's rows once, into registers (independent loads); the rows of
+        // (b, g) outside the tile only count towards the amax
+        float xr[DH][NR];
+        float am = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) xv[e] = 0.f;
-      if (row < nr) {
-        const int rr = r0 + row, tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
-        const uint16_t* src = p.q_bf16 + int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c0;
+        for (int dh = 0; dh < DH; ++dh) {
+          const int c = xq + 128 * dh;
+#pragma unroll
+          for (int r = 0; r < NR; ++r) xr[dh][r] = r < nr ? q_in(r0 + r, c) : 0.f;
+#pragma unroll
+          for (int r = 0; r < NR; ++r) am = fmaxf(am, fabsf(xr[dh][r]));
+          for (int rr = 0; rr < p.n_q; ++rr)
+            if (rr < r0 || rr >= r0 + nr) am = fmaxf(am, fabsf(q_in(rr, c)));
+        }
+        sq = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.0f);
+#pragma unroll
+        for (int dh = 0; dh < DH; ++dh) {
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            uint8_t code = 0;
+            if (r < nr) code = __nv_cvt_float_to_fp8(__fdiv_rn(xr[dh][r], sq), __NV_SATFINITE, __NV_E4M3);
+            smem[q_off(r, xq + 128 * dh)] = code;
+          }
+        }
+        zero_rows(NR);  // the rows past the tile
+      } else {
+        // bf16 Q as two e4m3 terms: hi = e4m3(x / s_hi) with s_hi = amax/448,
+        // lo = e4m3((x - hi*s_hi) / s_lo) with s_lo = (max |residual|)/448.
+        // hi fills rows 0 .. NR-1 of the Q tile and lo rows NR .. 2NR-1, so one
+        // QK product gives both terms; the logit is s_hi*S_hi + s_lo*S_lo.
+        // Thread xq owns EPT consecutive channels of one row (NR x D values
+        // over 128 threads; EPT divides 128, so they share one sub-tile).
+        constexpr int EPT = NR * DH;
+        const int row = (xq * EPT) / D, c0 = (xq * EPT) % D;
+        float xv[EPT];
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) xv[e] = 0.f;
+        if (row < nr) {
+          const int rr = r0 + row, tq = rr / p.h_r, h = g * p.h_r + rr % p.h_r;
+          const uint16_t* src = p.q_bf16 + int64_t(b * p.q_len + tq) * p.q_ts + int64_t(h) * p.q_hs + c0;
+#pragma unroll
+          for (int e = 0; e < EPT; e += 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(src + e);
+            xv[e] = __uint_as_float(u.x << 16);
+            xv[e + 1] = __uint_as_float(u.x & 0xFFFF0000u);
+            xv[e + 2] = __uint_as_float(u.y << 16);
+            xv[e + 3] = __uint_as_float(u.y & 0xFFFF0000u);
+          }
+        }
+        float am = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) am = fmaxf(am, fabsf(xv[e]));
+        const float s_hi = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.f);
+        uint32_t hw[EPT / 4];
+        float rm = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPT; e += 2) {
+          const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fdiv_rn(xv[e], s_hi), __fdiv_rn(xv[e + 1], s_hi)), __NV_SATFINITE, __NV_E4M3);
+          const float2 hv = e4m3x2_to_float2(h2);
+          xv[e] -= hv.x * s_hi;  // the residual
+          xv[e + 1] -= hv.y * s_hi;
+          rm = fmaxf(rm, fmaxf(fabsf(xv[e]), fabsf(xv[e + 1])));
+          if ((e & 3) == 0)
+            hw[e / 4] = uint32_t(h2);
+          else
+            hw[e / 4] |= uint32_t(h2) << 16;
+        }
+        const float rmax = block_max(rm, 1);
+        const float s_lo = rmax > 0.f ? __fdiv_rn(rmax, 448.f) : 1.f;
+        uint32_t lw[EPT / 4];
+#pragma unroll
+        for (int e = 0; e < EPT; e += 2) {
+          const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fdiv_rn(xv[e], s_lo), __fdiv_rn(xv[e + 1], s_lo)), __NV_SATFINITE, __NV_E4M3);
+          if ((e & 3) == 0)
+            lw[e / 4] = uint32_t(l2);
+          else
+            lw[e / 4] |= uint32_t(l2) << 16;
+        }
+        // 4 codes per word (c is a multiple of 4: one 16-byte chunk)
 #pragma unroll
         for (int e = 0; e < EPT; e += 4) {
-          const uint2 u = *reinterpret_cast<const uint2*>(src + e);
-          xv[e] = __uint_as_float(u.x << 16);
-          xv[e + 1] = __uint_as_float(u.x & 0xFFFF0000u);
-          xv[e + 2] = __uint_as_float(u.y << 16);
-          xv[e + 3] = __uint_as_float(u.y & 0xFFFF0000u);
+          const int c = c0 + e;
+          *reinterpret_cast<uint32_t*>(smem + q_off(row, c)) = hw[e / 4];
+          *reinterpret_cast<uint32_t*>(smem + q_off(NR + row, c)) = lw[e / 4];
         }
+        zero_rows(2 * NR);  // the rows past the two terms
+        const float kq = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g) * p.qk_scale_log2;
+        sc_hi = s_hi * kq;
+        sc_lo = s_lo * kq;
       }
-      float am = 0.f;
+      tc::fence_async_smem();
+      tc::mbar_arrive(tc::smem_u32(&ctl.q_ready));
+      const int qd = warp & 3;          // TMEM lane quadrant of this warp
+      const int x = qd * 32 + lane;     // key of the tile (S) / channel (O)
+      const uint32_t lane_off = uint32_t(qd * 32) << 16;
+      const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
+      // bf16 Q as two terms: the logits are formed when S is read (scale 1 below)
+      const float scale =
+          QM == 1 ? 1.f : (QM == 2 ? sq : p.q_descale[int64_t(b) * p.h_k + g]) * kd * p.qk_scale_log2;
+      // last visible key of each row (query token t sees keys j <= L - q_len + t)
+      int lim[NR];
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) am = fmaxf(am, fabsf(xv[e]));
-      const float s_hi = __fdiv_rn(fmaxf(block_max(am, 0), 1e-6f), 448.f);
-      uint32_t hw[EPT / 4];
-      float rm = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPT; e += 2) {
-        const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(xv[e], s_hi), __fdiv_rn(xv[e + 1], s_hi)), __NV_SATFINITE, __NV_E4M3);
-        const float2 hv = e4m3x2_to_float2(h2);
-        xv[e] -= hv.x * s_hi;  // the residual
-        xv[e + 1] -= hv.y * s_hi;
-        rm = fmaxf(rm, fmaxf(fabsf(xv[e]), fabsf(xv[e + 1])));
-        if ((e & 3) == 0)
-          hw[e / 4] = uint32_t(h2);
-        else
-          hw[e / 4] |= uint32_t(h2) << 16;
-      }
-      const float rmax = block_max(rm, 1);
-      const float s_lo = rmax > 0.f ? __fdiv_rn(rmax, 448.f) : 1.f;
-      uint32_t lw[EPT / 4];
-#pragma unroll
-      for (int e = 0; e < EPT; e += 2) {
-        const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(xv[e], s_lo), __fdiv_rn(xv[e + 1], s_lo)), __NV_SATFINITE, __NV_E4M3);
-        if ((e & 3) == 0)
-          lw[e / 4] = uint32_t(l2);
-        else
-          lw[e / 4] |= uint32_t(l2) << 16;
-      }
-      // 4 codes per word (c is a multiple of 4: one 16-byte chunk)
-#pragma unroll
-      for (int e = 0; e < EPT; e += 4) {
-        const int c = c0 + e;
-        *reinterpret_cast<uint32_t*>(smem + q_off(row, c)) = hw[e / 4];
-        *reinterpret_cast<uint32_t*>(smem + q_off(NR + row, c)) = lw[e / 4];
-      }
-      zero_rows(2 * NR);  // the rows past the two terms
-      const float kq = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g) * p.qk_scale_log2;
-      sc_hi = s_hi * kq;
-      sc_lo = s_lo * kq;
-    }
-    tc::fence_async_smem();
-    tc::mbar_arrive(tc::smem_u32(&ctl.q_ready));
-    const int qd = warp & 3;          // TMEM lane quadrant of this warp
-    const int x = qd * 32 + lane;     // key of the tile (S) / channel (O)
-    const uint32_t lane_off = uint32_t(qd * 32) << 16;
-    const float kd = kv_descale(p.k_descale, p.ds_seq, p.ds_head, b, g);
-    // bf16 Q as two terms: the logits are formed when S is read (scale 1 below)
-    const float scale =
-        QM == 1 ? 1.f : (QM == 2 ? sq : p.q_descale[int64_t(b) * p.h_k + g]) * kd * p.qk_scale_log2;
-    // last visible key of each row (query token t sees keys j <= L - q_len + t)
-    int lim[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-      lim[r] = r < nr ? (p.causal ? L - p.q_len + (r0 + r) / p.h_r : INT_MAX) : -1;
-    const int lim_min = lim[0];  // the tile's first row has the smallest limit
+      for (int r = 0; r < NR; ++r)
+        lim[r] = r < nr ? (p.causal ? L - p.q_len + (r0 + r) / p.h_r : INT_MAX) : -1;
+      const int lim_min = lim[0];  // the tile's first row has the smallest limit
 
-    // m_ref: the reference max each row's P is scaled by; it only moves when a
-    // tile's max exceeds it by more than kTau (log2 units), and then O (kept
-    // in TMEM across tiles) is rescaled in place. P = 2^(t - m_ref + 8) stays
-    // <= 2^(8 + kTau) < 448, so every e4m3 term of P stays finite.
-    constexpr float kTau = 0.6f;
-    float m_ref[NR], l_part[NR];
+      // m_ref: the reference max each row's P is scaled by; it only moves when a
+      // tile's max exceeds it by more than kTau (log2 units), and then O (kept
+      // in TMEM across tiles) is rescaled in place. P = 2^(t - m_ref + 8) stays
+      // <= 2^(8 + kTau) < 448, so every e4m3 term of P stays finite.
+      constexpr float kTau = 0.6f;
+      float m_ref[NR], l_part[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      m_ref[r] = -INFINITY;
-      l_part[r] = 0.f;
-    }
-    bool ok = true;
-    constexpr int kGroup = 32 / NR;  // lanes that share a row after rs_reduce
-    const int my_row = lane / kGroup;
-    constexpr bool kBound = NR >= 8;  // the single-bound check before the per-row maxima
-    int xr = 0;                       // per-row exchanges so far (kBound; the same count in every thread)
-    // P buffers whose pair-B blocks may hold nonzero codes in this thread's
-    // chunk (bit j: buffer j); at first every buffer (shared memory starts
-    // with arbitrary contents)
-    uint32_t b_dirty = (1u << NSB) - 1u;
-    constexpr int kSmallBudget = 8 / TP;  // iterations whose weights below 1/4 went with pair A alone
-    int n_small = 0;
-
-    // TP tiles per iteration: with few rows, the two S buffers are processed
-    // together (256 keys), so the row-max reduction, the cross-warp exchange
-    // and the fences are paid once per pair and the two tiles' arithmetic
-    // interleaves.
-    for (int i = 0; i < ntiles; i += TP) {
-      const int nt = min(TP, ntiles - i);
-      float s[TP][NR];  // S columns of the real rows only
-#pragma unroll
-      for (int a = 0; a < TP; ++a) {
-        if (a < nt) {
-          ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.s_full[bs(i + a)]), bp(i + a), abort, kWaitLimitNs);
-        }
+      for (int r = 0; r < NR; ++r) {
+        m_ref[r] = -INFINITY;
+        l_part[r] = 0.f;
       }
-      if (!ok) break;
-      tc::tc_fence_after();
-      if constexpr (QM != 1) {
+      bool ok = true;
+      constexpr int kGroup = 32 / NR;  // lanes that share a row after rs_reduce
+      const int my_row = lane / kGroup;
+      constexpr bool kBound = NR >= 8;  // the single-bound check before the per-row maxima
+      int xr = 0;                       // per-row exchanges so far (kBound; the same count in every thread)
+      // P buffers whose pair-B blocks may hold nonzero codes in this thread's
+      // chunk (bit j: buffer j); at first every buffer (shared memory starts
+      // with arbitrary contents)
+      uint32_t b_dirty = (1u << NSB) - 1u;
+      constexpr int kSmallBudget = 8 / TP;  // iterations whose weights below 1/4 went with pair A alone
+      int n_small = 0;
+
+      // TP tiles per iteration: with few rows, the two S buffers are processed
+      // together (256 keys), so the row-max reduction, the cross-warp exchange
+      // and the fences are paid once per pair and the two tiles' arithmetic
+      // interleaves.
+      for (int i = 0; i < ntiles; i += TP) {
+        const int nt = min(TP, ntiles - i);
+        float s[TP][NR];  // S columns of the real rows only
 #pragma unroll
         for (int a = 0; a < TP; ++a) {
           if (a < nt) {
-            tc::tmem_ld_cols<NR>(tS(i + a) + lane_off, s[a]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < NR; ++c) s[a][c] = -INFINITY;
+            ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.s_full[bs(i + a)]), bp(i + a), abort, kWaitLimitNs);
           }
         }
-        tc::tmem_wait_ld();
-      } else {
-        // columns 0 .. NR-1: the hi term's products, NR .. 2NR-1: the lo term's
-        float s2[TP][2 * NR];
-#pragma unroll
-        for (int a = 0; a < TP; ++a)
-          if (a < nt) tc::tmem_ld_cols<2 * NR>(tS(i + a) + lane_off, s2[a]);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int a = 0; a < TP; ++a)
-#pragma unroll
-          for (int c = 0; c < NR; ++c) s[a][c] = a < nt ? fmaf(s2[a][NR + c], sc_lo, s2[a][c] * sc_hi) : -INFINITY;
-      }
-
-      int key[TP];
-      bool valid[TP];
-#pragma unroll
-      for (int a = 0; a < TP; ++a) {
-        key[a] = int(k0) + (i + a) * kKvTile + x;
-        valid[a] = a < nt && key[a] < int(k1);
-      }
-      // Every key of the iteration visible to every row (the common case:
-      // no tile past the end, no causal limit inside): no per-row masks.
-      // Rows past nr then see S = 0 (their Q rows are zero); their P only
-      // reaches O columns that are never written out.
-      const int64_t it_end = k0 + int64_t(i + nt) * kKvTile;  // one past the iteration's last key
-      const bool all_vis = nt == TP && it_end <= k1 && it_end - 1 <= int64_t(lim_min);
-      float tmp[NR];
-      if (all_vis) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          float v = s[0][r] * scale;
-#pragma unroll
-          for (int a = 1; a < TP; ++a) v = fmaxf(v, s[a][r] * scale);
-          tmp[r] = v;
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          float v = -INFINITY;
-#pragma unroll
-          for (int a = 0; a < TP; ++a)
-            v = fmaxf(v, (valid[a] && key[a] <= lim[r]) ? s[a][r] * scale : -INFINITY);
-          tmp[r] = v;
-        }
-      }
-      const int xi = i / TP;  // exchange sequence number
-      bool rescale = false;
-      // With 8 or more rows, one bound first: the largest (tile max - m_ref)
-      // over the rows and keys of the four warps. A row's reference only
-      // moves when its tile max exceeds it by more than kTau, so a bound
-      // <= kTau (the common case once the references have settled) skips the
-      // per-row reductions. A row with no visible key so far gives
-      // -inf - -inf = NaN, which fmaxf drops; its first visible key gives +inf.
-      bool settled = false;
-      if constexpr (kBound) {
-        float dmax = -INFINITY;
-#pragma unroll
-        for (int r = 0; r < NR; ++r) dmax = fmaxf(dmax, tmp[r] - m_ref[r]);
-        dmax = warp_max(dmax);
-        if (lane == 0) ctl.bound[xi & 1][qd] = dmax;
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.red_bar[xi & 1]));
-        ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[xi & 1]), uint32_t(xi >> 1) & 1u, abort, kWaitLimitNs);
         if (!ok) break;
-        const float4 bd = *reinterpret_cast<const float4*>(&ctl.bound[xi & 1][0]);
-        settled = fmaxf(fmaxf(bd.x, bd.y), fmaxf(bd.z, bd.w)) <= kTau;  // the same in every thread
-      }
-      if (!settled) {
-        // per-row maxima over the four warps: exchange number xe (counted
-        // apart from the bound exchanges when there are both)
-        const int xe = kBound ? xr++ : xi;
-        const uint32_t xbar = tc::smem_u32(kBound ? &ctl.row_bar[xe & 1] : &ctl.red_bar[xe & 1]);
-        const float wmax = rs_reduce<NR, true>(tmp, lane);
-        if (lane % kGroup == 0) ctl.red[xe & 1][qd][my_row] = wmax;
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(xbar);
-        ok = tc::mbar_wait(xbar, uint32_t(xe >> 1) & 1u, abort, kWaitLimitNs);
-        if (!ok) break;
-
-        // new reference maxima (the same decision in every thread)
+        tc::tc_fence_after();
+        if constexpr (QM != 1) {
 #pragma unroll
-        for (int r = 0; r < NR; r += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][0][r]);
-          const float4 b4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][1][r]);
-          const float4 c4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][2][r]);
-          const float4 d4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][3][r]);
-          const float tm[4] = {fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x)), fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y)),
-                               fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z)), fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w))};
+          for (int a = 0; a < TP; ++a) {
+            if (a < nt) {
+              tc::tmem_ld_cols<NR>(tS(i + a) + lane_off, s[a]);
+            } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float alpha = 1.f;
-            if (tm[j] > m_ref[r + j] + kTau) {  // false for -inf tiles
-              alpha = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
-              rescale |= m_ref[r + j] != -INFINITY;
-              m_ref[r + j] = tm[j];
-              l_part[r + j] *= alpha;
+              for (int c = 0; c < NR; ++c) s[a][c] = -INFINITY;
             }
-            // the O rescale below reads the factors back from shared memory
-            if (lane == 0) ctl.alpha[qd][r + j] = alpha;
           }
-        }
-      }
-
-      // p = 2^(t - m_ref + 8) of every (key, row) of the iteration, in place
-      // of s; 0 where the row does not see the key. pmin: the smallest
-      // weight of a visible key (for the pair-B budget below).
-      float pmin = INFINITY;
-      {
-        float c8[NR];
-#pragma unroll
-        for (int r = 0; r < NR; ++r) c8[r] = 8.f - m_ref[r];
-        if (all_vis) {
-#pragma unroll
-          for (int a = 0; a < TP; ++a)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-              s[a][r] = fast_exp2(fmaf(s[a][r], scale, c8[r]));
-              pmin = fminf(pmin, s[a][r]);
-            }
+          tc::tmem_wait_ld();
         } else {
+          // columns 0 .. NR-1: the hi term's products, NR .. 2NR-1: the lo term's
+          float s2[TP][2 * NR];
+#pragma unroll
+          for (int a = 0; a < TP; ++a)
+            if (a < nt) tc::tmem_ld_cols<2 * NR>(tS(i + a) + lane_off, s2[a]);
+          tc::tmem_wait_ld();
 #pragma unroll
           for (int a = 0; a < TP; ++a)
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
-              const bool vis = valid[a] && key[a] <= lim[r] && m_ref[r] != -INFINITY;
-              s[a][r] = vis ? fast_exp2(fmaf(s[a][r], scale, c8[r])) : 0.f;
-              pmin = fminf(pmin, vis ? s[a][r] : INFINITY);
-            }
+            for (int c = 0; c < NR; ++c) s[a][c] = a < nt ? fmaf(s2[a][NR + c], sc_lo, s2[a][c] * sc_hi) : -INFINITY;
         }
-      }
-      // Pair A alone is within 2^-8 p of every p >= 1/4 and within 2^-10 of
-      // every smaller one. A thread lets up to kSmallBudget of its
-      // iterations with a weight below 1/4 (the smallest nonzero one tells)
-      // go with pair A alone: that is at most TP kSmallBudget = 8 such keys
-      // per row and thread, 1024 per row, 2^-10 each against a row sum of at
-      // least 2^8: 2^-8 of it. Past that budget its warp adds pair B to every
-      // iteration that holds small weights. Typical rows (keys within 10
-      // binades of their max, bar a few) never pay for pair B; long rows far
-      // below one dominant key do.
-      const int small = pmin < 0.25f ? 1 : 0;
-      const bool need_b = __any_sync(0xFFFFFFFFu, n_small + small > kSmallBudget);
-      if (!need_b) n_small += small;
 
-      // This key's column of P^T: term k of row r at byte k * NR + r (k: A hi,
-      // A lo, B hi, B lo) of 16-column block (byte / 16), the key's 16-byte
-      // chunk in it. Pair A is hi = e4m3(p), lo = e4m3(p - hi); pair B the
-      // same split of (p - hi - lo) * 2^10 where p < 1/4, else 0. (One body,
-      // instantiated with and without pair B.) With 8 or more rows pair B has
-      // blocks of its own: without pair B only pair A's blocks are stored,
-      // and pair B's are cleared only where this thread's chunk of the buffer
-      // may still hold nonzero codes (b_dirty).
-      auto make_p = [&](auto with_b) {
-        constexpr bool WB = decltype(with_b)::value;
+        int key[TP];
+        bool valid[TP];
 #pragma unroll
         for (int a = 0; a < TP; ++a) {
-          if (a >= nt) break;
-          uint32_t words[NPV / 4];
+          key[a] = int(k0) + (i + a) * kKvTile + x;
+          valid[a] = a < nt && key[a] < int(k1);
+        }
+        // Every key of the iteration visible to every row (the common case:
+        // no tile past the end, no causal limit inside): no per-row masks.
+        // Rows past nr then see S = 0 (their Q rows are zero); their P only
+        // reaches O columns that are never written out.
+        const int64_t it_end = k0 + int64_t(i + nt) * kKvTile;  // one past the iteration's last key
+        const bool all_vis = nt == TP && it_end <= k1 && it_end - 1 <= int64_t(lim_min);
+        float tmp[NR];
+        if (all_vis) {
 #pragma unroll
-          for (int w2 = 0; w2 < NPV / 4; ++w2) words[w2] = 0u;
+          for (int r = 0; r < NR; ++r) {
+            float v = s[0][r] * scale;
 #pragma unroll
-          for (int r = 0; r < NR; r += 2) {
-            const float x0 = s[a][r], x1 = s[a][r + 1];
-            const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
-            const float2 hf = e4m3x2_to_float2(hi2);
-            const float d0 = x0 - hf.x, d1 = x1 - hf.y;  // exact
-            const __nv_fp8x2_storage_t lo2 = __nv_cvt_float2_to_fp8x2(make_float2(d0, d1), __NV_SATFINITE, __NV_E4M3);
-            const int sh = (r % 4) * 8;  // the pair's two bytes in their word
-            words[r / 4] |= uint32_t(hi2) << sh;
-            words[(NR + r) / 4] |= uint32_t(lo2) << sh;
-            if constexpr (WB) {
-              // pair B: what pair A left of p (exact), times 2^10, where p < 1/4
-              const float2 lf = e4m3x2_to_float2(lo2);
-              const float y0 = x0 < 0.25f ? (d0 - lf.x) * 1024.f : 0.f;
-              const float y1 = x1 < 0.25f ? (d1 - lf.y) * 1024.f : 0.f;
-              const __nv_fp8x2_storage_t bh2 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
-              const float2 bhf = e4m3x2_to_float2(bh2);
-              const __nv_fp8x2_storage_t bl2 =
-                  __nv_cvt_float2_to_fp8x2(make_float2(y0 - bhf.x, y1 - bhf.y), __NV_SATFINITE, __NV_E4M3);
-              words[(2 * NR + r) / 4] |= uint32_t(bh2) << sh;
-              words[(3 * NR + r) / 4] |= uint32_t(bl2) << sh;
-            }
-            // l sums the weights themselves; O gets them to within
-            // max(2^-8 p, 2^-20) each
-            l_part[r] += x0;
-            l_part[r + 1] += x1;
+            for (int a = 1; a < TP; ++a) v = fmaxf(v, s[a][r] * scale);
+            tmp[r] = v;
           }
-          uint8_t* pt = smem + lay.p0 + bs(i + a) * p_stride;
-          constexpr int kBlkA = NR >= 8 ? NPV / 32 : NPV / 16;  // blocks always stored
+        } else {
 #pragma unroll
-          for (int bk = 0; bk < kBlkA; ++bk)
-            *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
-                make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
-          if constexpr (kBlkA < NPV / 16) {
-            const uint32_t bit = 1u << bs(i + a);
-            if (WB || (b_dirty & bit)) {
+          for (int r = 0; r < NR; ++r) {
+            float v = -INFINITY;
 #pragma unroll
-              for (int bk = kBlkA; bk < NPV / 16; ++bk)
-                *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
-                    make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
-              b_dirty = WB ? (b_dirty | bit) : (b_dirty & ~bit);
+            for (int a = 0; a < TP; ++a)
+              v = fmaxf(v, (valid[a] && key[a] <= lim[r]) ? s[a][r] * scale : -INFINITY);
+            tmp[r] = v;
+          }
+        }
+        const int xi = i / TP;  // exchange sequence number
+        bool rescale = false;
+        // With 8 or more rows, one bound first: the largest (tile max - m_ref)
+        // over the rows and keys of the four warps. A row's reference only
+        // moves when its tile max exceeds it by more than kTau, so a bound
+        // <= kTau (the common case once the references have settled) skips the
+        // per-row reductions. A row with no visible key so far gives
+        // -inf - -inf = NaN, which fmaxf drops; its first visible key gives +inf.
+        bool settled = false;
+        if constexpr (kBound) {
+          float dmax = -INFINITY;
+#pragma unroll
+          for (int r = 0; r < NR; ++r) dmax = fmaxf(dmax, tmp[r] - m_ref[r]);
+          dmax = warp_max(dmax);
+          if (lane == 0) ctl.bound[xi & 1][qd] = dmax;
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.red_bar[xi & 1]));
+          ok = tc::mbar_wait(tc::smem_u32(&ctl.red_bar[xi & 1]), uint32_t(xi >> 1) & 1u, abort, kWaitLimitNs);
+          if (!ok) break;
+          const float4 bd = *reinterpret_cast<const float4*>(&ctl.bound[xi & 1][0]);
+          settled = fmaxf(fmaxf(bd.x, bd.y), fmaxf(bd.z, bd.w)) <= kTau;  // the same in every thread
+        }
+        if (!settled) {
+          // per-row maxima over the four warps: exchange number xe (counted
+          // apart from the bound exchanges when there are both)
+          const int xe = kBound ? xr++ : xi;
+          const uint32_t xbar = tc::smem_u32(kBound ? &ctl.row_bar[xe & 1] : &ctl.red_bar[xe & 1]);
+          const float wmax = rs_reduce<NR, true>(tmp, lane);
+          if (lane % kGroup == 0) ctl.red[xe & 1][qd][my_row] = wmax;
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(xbar);
+          ok = tc::mbar_wait(xbar, uint32_t(xe >> 1) & 1u, abort, kWaitLimitNs);
+          if (!ok) break;
+
+          // new reference maxima (the same decision in every thread)
+#pragma unroll
+          for (int r = 0; r < NR; r += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][0][r]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][1][r]);
+            const float4 c4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][2][r]);
+            const float4 d4 = *reinterpret_cast<const float4*>(&ctl.red[xe & 1][3][r]);
+            const float tm[4] = {fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d4.x)), fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d4.y)),
+                                 fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d4.z)), fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d4.w))};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float alpha = 1.f;
+              if (tm[j] > m_ref[r + j] + kTau) {  // false for -inf tiles
+                alpha = fast_exp2(m_ref[r + j] - tm[j]);  // 0 when m_ref = -inf
+                rescale |= m_ref[r + j] != -INFINITY;
+                m_ref[r + j] = tm[j];
+                l_part[r + j] *= alpha;
+              }
+              // the O rescale below reads the factors back from shared memory
+              if (lane == 0) ctl.alpha[qd][r + j] = alpha;
             }
           }
         }
-      };
-      if (need_b)
-        make_p(std::true_type{});
-      else
-        make_p(std::false_type{});
-      if (rescale) {
-        // O holds the PV sums up to tile i-1, scaled by the old references:
-        // wait for the last of them and rescale O in TMEM before PV_i (which
-        // waits for p_full, signalled below). Done after P is written, when
-        // S no longer occupies registers.
-        ok = tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(i - 1)]), bp(i - 1), abort, kWaitLimitNs);
-        if (!ok) break;
-        __syncwarp();  // lane 0's factors
-        tc::tc_fence_after();
+
+        // p = 2^(t - m_ref + 8) of every (key, row) of the iteration, in place
+        // of s; 0 where the row does not see the key. pmin: the smallest
+        // weight of a visible key (for the pair-B budget below).
+        float pmin = INFINITY;
+        {
+          float c8[NR];
+#pragma unroll
+          for (int r = 0; r < NR; ++r) c8[r] = 8.f - m_ref[r];
+          if (all_vis) {
+#pragma unroll
+            for (int a = 0; a < TP; ++a)
+#pragma unroll
+              for (int r = 0; r < NR; ++r) {
+                s[a][r] = fast_exp2(fmaf(s[a][r], scale, c8[r]));
+                pmin = fminf(pmin, s[a][r]);
+              }
+          } else {
+#pragma unroll
+            for (int a = 0; a < TP; ++a)
+#pragma unroll
+              for (int r = 0; r < NR; ++r) {
+                const bool vis = valid[a] && key[a] <= lim[r] && m_ref[r] != -INFINITY;
+                s[a][r] = vis ? fast_exp2(fmaf(s[a][r], scale, c8[r])) : 0.f;
+                pmin = fminf(pmin, vis ? s[a][r] : INFINITY);
+              }
+          }
+        }
+        // Pair A alone is within 2^-8 p of every p >= 1/4 and within 2^-10 of
+        // every smaller one. A thread lets up to kSmallBudget of its
+        // iterations with a weight below 1/4 (the smallest nonzero one tells)
+        // go with pair A alone: that is at most TP kSmallBudget = 8 such keys
+        // per row and thread, 1024 per row, 2^-10 each against a row sum of at
+        // least 2^8: 2^-8 of it. Past that budget its warp adds pair B to every
+        // iteration that holds small weights. Typical rows (keys within 10
+        // binades of their max, bar a few) never pay for pair B; long rows far
+        // below one dominant key do.
+        const int small = pmin < 0.25f ? 1 : 0;
+        const bool need_b = __any_sync(0xFFFFFFFFu, n_small + small > kSmallBudget);
+        if (!need_b) n_small += small;
+
+        // This key's column of P^T: term k of row r at byte k * NR + r (k: A hi,
+        // A lo, B hi, B lo) of 16-column block (byte / 16), the key's 16-byte
+        // chunk in it. Pair A is hi = e4m3(p), lo = e4m3(p - hi); pair B the
+        // same split of (p - hi - lo) * 2^10 where p < 1/4, else 0. (One body,
+        // instantiated with and without pair B.) With 8 or more rows pair B has
+        // blocks of its own: without pair B only pair A's blocks are stored,
+        // and pair B's are cleared only where this thread's chunk of the buffer
+        // may still hold nonzero codes (b_dirty).
+        auto make_p = [&](auto with_b) {
+          constexpr bool WB = decltype(with_b)::value;
+#pragma unroll
+          for (int a = 0; a < TP; ++a) {
+            if (a >= nt) break;
+            uint32_t words[NPV / 4];
+#pragma unroll
+            for (int w2 = 0; w2 < NPV / 4; ++w2) words[w2] = 0u;
+#pragma unroll
+            for (int r = 0; r < NR; r += 2) {
+              const float x0 = s[a][r], x1 = s[a][r + 1];
+              const __nv_fp8x2_storage_t hi2 = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+              const float2 hf = e4m3x2_to_float2(hi2);
+              const float d0 = x0 - hf.x, d1 = x1 - hf.y;  // exact
+              const __nv_fp8x2_storage_t lo2 = __nv_cvt_float2_to_fp8x2(make_float2(d0, d1), __NV_SATFINITE, __NV_E4M3);
+              const int sh = (r % 4) * 8;  // the pair's two bytes in their word
+              words[r / 4] |= uint32_t(hi2) << sh;
+              words[(NR + r) / 4] |= uint32_t(lo2) << sh;
+              if constexpr (WB) {
+                // pair B: what pair A left of p (exact), times 2^10, where p < 1/4
+                const float2 lf = e4m3x2_to_float2(lo2);
+                const float y0 = x0 < 0.25f ? (d0 - lf.x) * 1024.f : 0.f;
+                const float y1 = x1 < 0.25f ? (d1 - lf.y) * 1024.f : 0.f;
+                const __nv_fp8x2_storage_t bh2 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+                const float2 bhf = e4m3x2_to_float2(bh2);
+                const __nv_fp8x2_storage_t bl2 =
+                    __nv_cvt_float2_to_fp8x2(make_float2(y0 - bhf.x, y1 - bhf.y), __NV_SATFINITE, __NV_E4M3);
+                words[(2 * NR + r) / 4] |= uint32_t(bh2) << sh;
+                words[(3 * NR + r) / 4] |= uint32_t(bl2) << sh;
+              }
+              // l sums the weights themselves; O gets them to within
+              // max(2^-8 p, 2^-20) each
+              l_part[r] += x0;
+              l_part[r + 1] += x1;
+            }
+            uint8_t* pt = smem + lay.p0 + bs(i + a) * p_stride;
+            constexpr int kBlkA = NR >= 8 ? NPV / 32 : NPV / 16;  // blocks always stored
+#pragma unroll
+            for (int bk = 0; bk < kBlkA; ++bk)
+              *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
+                  make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
+            if constexpr (kBlkA < NPV / 16) {
+              const uint32_t bit = 1u << bs(i + a);
+              if (WB || (b_dirty & bit)) {
+#pragma unroll
+                for (int bk = kBlkA; bk < NPV / 16; ++bk)
+                  *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
+                      make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
+                b_dirty = WB ? (b_dirty | bit) : (b_dirty & ~bit);
+              }
+            }
+          }
+        };
+        if (need_b)
+          make_p(std::true_type{});
+        else
+          make_p(std::false_type{});
+        if (rescale) {
+          // O holds the PV sums up to tile i-1, scaled by the old references:
+          // wait for the last of them and rescale O in TMEM before PV_i (which
+          // waits for p_full, signalled below). Done after P is written, when
+          // S no longer occupies registers.
+          ok = tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(i - 1)]), bp(i - 1), abort, kWaitLimitNs);
+          if (!ok) break;
+          __syncwarp();  // lane 0's factors
+          tc::tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < DH * NPV; c += 16) {
-          float v[16];
-          tc::tmem_ld16(tO + lane_off + c, v);
-          tc::tmem_wait_ld();
+          for (int c = 0; c < DH * NPV; c += 16) {
+            float v[16];
+            tc::tmem_ld16(tO + lane_off + c, v);
+            tc::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] *= ctl.alpha[qd][((c + j) % NPV) % NR];  // column k * NR + r: row r
-          tc::tmem_st16(tO + lane_off + c, v);
-        }
-        tc::tmem_wait_st();
-      }
-
-      tc::fence_async_smem();
-      tc::tc_fence_before();
-#pragma unroll
-      for (int a = 0; a < TP; ++a)
-        if (a < nt) tc::mbar_arrive(tc::smem_u32(&ctl.p_full[bs(i + a)]));
-      if (!ok) break;
-    }
-    // the final O: wait for the last PV product; o_acc[dh][r] is channel
-    // 128 dh + x: pair A's two columns of row r plus 2^-10 times pair B's
-    float o_acc[DH][NR];
-#pragma unroll
-    for (int dh = 0; dh < DH; ++dh)
-#pragma unroll
-      for (int r = 0; r < NR; ++r) o_acc[dh][r] = 0.f;
-    ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(ntiles - 1)]), bp(ntiles - 1), abort, kWaitLimitNs);
-    if (ok) {
-      tc::tc_fence_after();
-#pragma unroll
-      for (int dh = 0; dh < DH; ++dh) {
-        float ob[NR];  // pair B's sum
-#pragma unroll
-        for (int r = 0; r < NR; ++r) ob[r] = 0.f;
-#pragma unroll
-        for (int c = 0; c < NPV; c += 16) {
-          float v[16];
-          tc::tmem_ld16(tO + lane_off + dh * NPV + c, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c + j;
-            if (col < 2 * NR)
-              o_acc[dh][col % NR] += v[j];
-            else
-              ob[col % NR] += v[j];
+            for (int j = 0; j < 16; ++j) v[j] *= ctl.alpha[qd][((c + j) % NPV) % NR];  // column k * NR + r: row r
+            tc::tmem_st16(tO + lane_off + c, v);
           }
+          tc::tmem_wait_st();
         }
-#pragma unroll
-        for (int r = 0; r < NR; ++r) o_acc[dh][r] = fmaf(ob[r], 1.f / 1024.f, o_acc[dh][r]);
-      }
-    }
 
-    // ---- epilogue --------------------------------------------------------
-    {
-      float tmp[NR];
+        tc::fence_async_smem();
+        tc::tc_fence_before();
 #pragma unroll
-      for (int r = 0; r < NR; ++r) tmp[r] = l_part[r];
-      const float wsum = rs_reduce<NR, false>(tmp, lane);
-      if (lane % kGroup == 0) ctl.lsum[qd][my_row] = wsum;
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.sum_bar));
-    ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.sum_bar), 0, abort, kWaitLimitNs);
-    if (ok) {
-      const bool direct = !p.with_reduction || p.n_splits[b] <= 1;
-      const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
+        for (int a = 0; a < TP; ++a)
+          if (a < nt) tc::mbar_arrive(tc::smem_u32(&ctl.p_full[bs(i + a)]));
+        if (!ok) break;
+      }
+      // the final O: wait for the last PV product; o_acc[dh][r] is channel
+      // 128 dh + x: pair A's two columns of row r plus 2^-10 times pair B's
+      float o_acc[DH][NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (r >= nr) break;
-        const float lr = ctl.lsum[0][r] + ctl.lsum[1][r] + ctl.lsum[2][r] + ctl.lsum[3][r];
-        const int row = r0 + r;
-        const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
-        const int64_t idx = direct ? 0 : part_index(p, b, w.w, g, row);
+      for (int dh = 0; dh < DH; ++dh)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) o_acc[dh][r] = 0.f;
+      ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(ntiles - 1)]), bp(ntiles - 1), abort, kWaitLimitNs);
+      if (ok) {
+        tc::tc_fence_after();
 #pragma unroll
         for (int dh = 0; dh < DH; ++dh) {
-          const int ch = 128 * dh + x;
-          const float on = lr > 0.f ? o_acc[dh][r] / lr : 0.f;
-          if (direct) {
-            float val = on * vd;
-            if (p.o_mul) val *= p.o_mul[int64_t(h) * D + ch];
-            p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + ch] = float_to_out_bits(val, p.out_f16);
-          } else {
-            p.o_part[idx * D + ch] = on;
+          float ob[NR];  // pair B's sum
+#pragma unroll
+          for (int r = 0; r < NR; ++r) ob[r] = 0.f;
+#pragma unroll
+          for (int c = 0; c < NPV; c += 16) {
+            float v[16];
+            tc::tmem_ld16(tO + lane_off + dh * NPV + c, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c + j;
+              if (col < 2 * NR)
+                o_acc[dh][col % NR] += v[j];
+              else
+                ob[col % NR] += v[j];
+            }
           }
+#pragma unroll
+          for (int r = 0; r < NR; ++r) o_acc[dh][r] = fmaf(ob[r], 1.f / 1024.f, o_acc[dh][r]);
         }
-        if (x == 0) {
-          if (direct) {
-            if (p.lse)
-              p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
-                  lr > 0.f ? (m_ref[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
-          } else {
-            p.m_part[idx] = lr > 0.f ? m_ref[r] : -INFINITY;
-            p.l_part[idx] = lr * (1.f / 256.f);
+      }
+
+      // ---- epilogue --------------------------------------------------------
+      {
+        float tmp[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) tmp[r] = l_part[r];
+        const float wsum = rs_reduce<NR, false>(tmp, lane);
+        if (lane % kGroup == 0) ctl.lsum[qd][my_row] = wsum;
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.sum_bar));
+      ok = ok && tc::mbar_wait(tc::smem_u32(&ctl.sum_bar), 0, abort, kWaitLimitNs);
+      if (ok) {
+        const bool direct = !p.with_reduction || p.n_splits[b] <= 1;
+        const float vd = kv_descale(p.v_descale, p.ds_seq, p.ds_head, b, g) * p.v_fmt;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          if (r >= nr) break;
+          const float lr = ctl.lsum[0][r] + ctl.lsum[1][r] + ctl.lsum[2][r] + ctl.lsum[3][r];
+          const int row = r0 + r;
+          const int tq = row / p.h_r, h = g * p.h_r + row % p.h_r;
+          const int64_t idx = direct ? 0 : part_index(p, b, w.w, g, row);
+#pragma unroll
+          for (int dh = 0; dh < DH; ++dh) {
+            const int ch = 128 * dh + x;
+            const float on = lr > 0.f ? o_acc[dh][r] / lr : 0.f;
+            if (direct) {
+              float val = on * vd;
+              if (p.o_mul) val *= p.o_mul[int64_t(h) * D + ch];
+              p.out[int64_t(b * p.q_len + tq) * p.out_ts + int64_t(h) * p.out_hs + ch] = float_to_out_bits(val, p.out_f16);
+            } else {
+              p.o_part[idx * D + ch] = on;
+            }
+          }
+          if (x == 0) {
+            if (direct) {
+              if (p.lse)
+                p.lse[(int64_t(b) * p.h_k + g) * p.n_q + row] =
+                    lr > 0.f ? (m_ref[r] + fast_log2(lr) - 8.f) * kLn2 : -INFINITY;
+            } else {
+              p.m_part[idx] = lr > 0.f ? m_ref[r] : -INFINITY;
+              p.l_part[idx] = lr * (1.f / 256.f);
+            }
           }
         }
       }
     }
-  }
   }  // active
 
   // ---- teardown ------------------------------------------------------------

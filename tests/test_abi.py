@@ -321,3 +321,28 @@ def test_plan_refuses_buffers_it_would_overrun(lib):
     got = mj.mj_plan_split_kv(lens, 8, 1, 32, 8, 152, 2, 16, 0, 64, work_out=np.zeros((64, 4), np.int32),
                               n_splits_out=np.zeros(8, np.int32))
     assert got["with_reduction"] and sum(got["n_splits"]) <= got["slots"]
+
+
+def test_plan_upload_validates_on_the_host(lib):
+    """mj_plan_upload copies nothing for an empty plan and refuses missing
+    or misaligned buffers before it enqueues anything."""
+    base = 1 << 40  # never dereferenced: every case below returns before a copy
+    f = lib.mj_plan_upload
+    assert f(None, None, None, None, 0, 0, None) == mj.MJ_OK
+    assert f(None, base, base, base, 64, 8, None) == mj.MJ_ERR_INVALID_ARG  # no host work buffer
+    assert f(base, None, base, base, 64, 8, None) == mj.MJ_ERR_INVALID_ARG  # no host n_splits
+    assert f(base, base, base, None, 64, 8, None) == mj.MJ_ERR_INVALID_ARG  # no device n_splits
+    assert f(base, base, base + 4, base, 64, 8, None) == mj.MJ_ERR_ALIGNMENT
+    assert f(base, base, base, base, -1, 8, None) == mj.MJ_ERR_INVALID_ARG
+
+
+def test_decode_kernel_query(lib):
+    """mj_decode_kernel validates like mj_decode_attention and reports the
+    CUDA-core kernel when asked for it, without touching a device."""
+    a = _valid_args()
+    a.impl = mj.MJ_IMPL_SIMT
+    v = ctypes.c_int(-1)
+    assert lib.mj_decode_kernel(ctypes.byref(a), ctypes.byref(v)) == mj.MJ_OK and v.value == mj.MJ_IMPL_SIMT
+    a.page_size = 24
+    assert lib.mj_decode_kernel(ctypes.byref(a), ctypes.byref(v)) == mj.MJ_ERR_UNSUPPORTED
+    assert lib.mj_decode_kernel(ctypes.byref(a), None) == mj.MJ_ERR_INVALID_ARG

@@ -18,6 +18,8 @@
 
 #include <algorithm>
 
+#include <atomic>
+
 #include "mj_device.cuh"
 #include "mj_internal.h"
 
@@ -274,16 +276,15 @@ cudaError_t launch_write_kv(const mj_write_kv_args& a, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  // SM count per device, looked up once
-  static int sm_count[64] = {};
-  if (dev >= 64) return cudaErrorInvalidDevice;
-  if (sm_count[dev] == 0) {
-    int sms = 0;
+  // SM count per device, looked up once (host threads may race)
+  static std::atomic<int> sm_count[64];
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int sms = sm_count[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    sm_count[dev] = sms;
+    sm_count[dev].store(sms, std::memory_order_relaxed);
   }
-  const int sms = sm_count[dev];
   // enough blocks to fill every SM (8 x 256 threads each), fewer for small writes
   const int64_t blocks = std::min<int64_t>((work + kThreads - 1) / kThreads, int64_t(sms) * 8);
   if (a.d == 256)

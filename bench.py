@@ -57,7 +57,7 @@ FALLBACK_HBM_GBS = 6800.0
 # knobs per workload: (ctas_per_sm, max_splits, kv_stages)
 DEFAULT_KNOBS = {
     "qwen3_8b_decode": (2, 64, 6),
-    "long_split": (2, 64, 6),
+    "long_split": (4, 64, 6),  # planned for four CTAs an SM, two resident: the hardware balances the second wave
     "long_single": (2, 64, 6),
     "spec_verify": (4, 64, 4),
     "spec_verify_noncausal": (4, 64, 4),

@@ -141,7 +141,7 @@ def test_repeated_steps_are_identical(impl):
 # ----------------------------------------------------------------------------
 FULL = {
     "qwen3_8b_decode": dict(ctas_per_sm=2, max_splits=64, kv_stages=6),
-    "long_split": dict(ctas_per_sm=2, max_splits=64),
+    "long_split": dict(ctas_per_sm=4, max_splits=64),
     "long_single": dict(ctas_per_sm=2, max_splits=64),
     "spec_verify": dict(ctas_per_sm=4, max_splits=64, kv_stages=4),
     "spec_verify_noncausal": dict(ctas_per_sm=4, max_splits=64, kv_stages=4),

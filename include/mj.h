@@ -311,7 +311,11 @@ MJ_API int mj_workspace_status(void* workspace, void* stream, uint32_t* device_s
  * preceding kernel on `stream` has finished (programmatic dependent launch:
  * only its Q reads wait for that kernel), so that kernel must be the
  * mj_quantize_q call that wrote q_codes, with nothing enqueued in between;
- * the other Q modes are plainly stream-ordered.
+ * the other Q modes are stream-ordered for everything the kernel reads: its
+ * CTAs may start early, but before the preceding kernel has finished they
+ * only ask L2 to prefetch their first KV tiles (aimed with the plan and
+ * block table as they stand; a prefetch returns no data), and without a split
+ * they let the next kernel on `stream` launch early in the same way.
  * ---------------------------------------------------------------------- */
 MJ_API int mj_decode_attention(const mj_decode_args* args, void* stream);
 

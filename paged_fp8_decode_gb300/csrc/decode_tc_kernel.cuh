@@ -73,6 +73,7 @@ constexpr int kConvThreads = kThreadsTcFp6 - 7 * 32;
 constexpr int kConvWarp0 = 7;
 constexpr int kSoftmaxWarp0 = 2;     // warps 2-5: softmax warpgroup
 constexpr int kVProducerWarp = 6;
+constexpr int kPrefetchTiles = 3;  // tiles a CTA asks L2 for before the programmatic-launch wait
 constexpr int kTileBytes = kKvTile * 128;  // 128 keys x 128 bytes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -301,7 +302,44 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   // every thread waits for it here. With fp8 codes the preceding kernel is
   // mj_quantize_q, which wrote only the Q codes and descales: only the
   // softmax warps wait, before they read them.
-  if constexpr (QM != 0) tc::grid_dependency_wait();
+  //
+  // Before that wait, the two TMA producer warps ask L2 for the first
+  // kPrefetchTiles tiles of the CTA's work row (its K and its V pages, one
+  // page per lane): HBM streams them while the preceding kernel finishes, and
+  // a CTA that starts later has them requested before it has read seq_lens.
+  // A prefetch hands nothing to the SM, and L2 is where the preceding
+  // kernel's writes land, so it cannot return stale data: the work row and
+  // block-table entries it is aimed with are only a guess (read before the
+  // wait, bounds-checked), and everything is read again after it.
+  if constexpr (QM != 0) {
+    if (warp == 0 || warp == kVProducerWarp) {
+      const int4 wp = reinterpret_cast<const int4*>(p.work)[blockIdx.x / unsigned(p.h_k)];
+      const int gp = int(blockIdx.x % unsigned(p.h_k));
+      if (blockIdx.y == 0 && wp.z > wp.y && wp.x >= 0 && wp.x < p.num_seqs) {
+        const int ppt = kKvTile / p.page_size;
+        const int64_t e = int64_t(wp.y) * ppt + lane;  // block-table entry of this lane's page
+        if (lane < min(kPrefetchTiles, wp.z - wp.y) * ppt && e < p.bt_stride) {
+          const int pg = p.block_table[int64_t(wp.x) * p.bt_stride + e];
+          if (pg >= 0 && int64_t(pg) < p.num_pages) {
+            const CUtensorMap* map = warp == 0 ? &tmap_k : &tmap_v;
+#pragma unroll
+            for (int dh = 0; dh < DH; ++dh) {
+              if (p.tma_head_inner)
+                tc::tma_prefetch_4d(map, 128 * dh, gp, 0, pg);
+              else
+                tc::tma_prefetch_4d(map, 128 * dh, 0, gp, pg);
+            }
+          }
+        }
+      }
+    }
+    // With no split (no merge kernel follows), the next kernel on the stream
+    // may launch now: its CTAs take the SMs this grid's last CTAs leave and
+    // run their set-up and prefetches meanwhile. (After a split the merge's
+    // CTAs would sit on those SMs instead, and the step is slower.)
+    if (!p.with_reduction) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    tc::grid_dependency_wait();
+  }
 
   // CTA x = (work row, KV head) with the head fastest: the CTAs that run
   // together stream the same requests' pages (with token-major layouts the

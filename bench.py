@@ -61,10 +61,10 @@ DEFAULT_KNOBS = {
     "long_single": (2, 64, 6),
     "spec_verify": (4, 64, 4),
     "spec_verify_noncausal": (4, 64, 4),
-    "fp6_decode": (2, 64, 4),
+    "fp6_decode": (2, 64, 6),
     "d256_decode": (2, 64, 2),
-    "fp6_e3m2_decode": (2, 64, 4),
-    "fp4_decode": (2, 64, 4),
+    "fp6_e3m2_decode": (2, 64, 6),
+    "fp4_decode": (2, 64, 6),
     "tiny": (2, 16, 0),
 }
 

@@ -206,7 +206,12 @@ __host__ __device__ constexpr uint32_t mma_kv_type(int kf) {
 // or four of them) and its D / 128 O accumulators (NPV columns each); and the
 // power of two it allocates. An instance that needs all 512 columns must run
 // alone on its SM (launch_tc sizes its shared memory so that it does).
-__host__ __device__ constexpr int tc_nsb(int /*nr*/) { return 4; }  // S / P buffers in flight
+__host__ __device__ constexpr int tc_nsb(int /*nr*/) { return 4; }  // S buffers in flight
+// P buffers in shared memory: one per S buffer, except at 8 rows, where two
+// (one tile pair) leave room for a 6-entry ring at two CTAs per SM; the
+// softmax then writes a pair's P only once the PV products of the pair
+// before it are complete.
+__host__ __device__ constexpr int tc_npb(int nr) { return nr == 8 ? 2 : tc_nsb(nr); }
 __host__ __device__ constexpr int tc_tmem_cols_used(int nqk, int npv, int nr, int d) {
   return tc_nsb(nr) * nqk + (d / 128) * npv;
 }
@@ -241,6 +246,8 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   constexpr int TP = (NR <= 8 || (NR == 16 && QM != 1 && !PK)) ? 2 : 1;
   constexpr int NSB = tc_nsb(NR);
   static_assert(NSB >= 2 * TP, "S / P buffers");
+  constexpr int NPB = tc_npb(NR);  // P buffers: P_j in buffer j % NPB
+  static_assert(NPB % TP == 0 && NPB >= TP && NPB <= NSB, "P buffers");
   // TMEM: NSB S buffers (NQK columns each), DH O accumulators (NPV columns each)
   constexpr int kCols = tc_tmem_cols_used(NQK, NPV, NR, D);
   constexpr uint32_t kTmemCols = tc_tmem_alloc_cols(kCols);
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
 
   const int stages = p.kv_stages;
 
-  const TcSmem lay = tc_smem_layout(stages, NQK, NPV, NSB, DH);
+  const TcSmem lay = tc_smem_layout(stages, NQK, NPV, NPB, DH);
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + lay.ctrl);
   const uint32_t ring_addr = tc::smem_u32(smem + lay.ring);
   const uint32_t q_addr = tc::smem_u32(smem + lay.q);
@@ -525,7 +532,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
               // P, MN-major without swizzle: 8-key core groups 128 B apart (LBO),
               // 16-column blocks 2 KB apart (SBO)
               const uint64_t pdesc =
-                  tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(bs(np)) * p_stride, 128, 2048, 0);
+                  tc::smem_desc(tc::smem_u32(smem + lay.p0) + uint32_t(np % NPB) * p_stride, 128, 2048, 0);
 #pragma unroll
               for (int dh = 0; dh < DH; ++dh) {
                 const uint64_t vdesc = tc::smem_desc(ring_addr + uint32_t(slot) * kEntry + uint32_t(dh) * kTileBytes,
@@ -742,7 +749,7 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
       // P buffers whose pair-B blocks may hold nonzero codes in this thread's
       // chunk (bit j: buffer j); at first every buffer (shared memory starts
       // with arbitrary contents)
-      uint32_t b_dirty = (1u << NSB) - 1u;
+      uint32_t b_dirty = (1u << NPB) - 1u;
       constexpr int kSmallBudget = 8 / TP;  // iterations whose weights below 1/4 went with pair A alone
       int n_small = 0;
 
@@ -958,14 +965,14 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
               l_part[r] += x0;
               l_part[r + 1] += x1;
             }
-            uint8_t* pt = smem + lay.p0 + bs(i + a) * p_stride;
+            uint8_t* pt = smem + lay.p0 + ((i + a) % NPB) * p_stride;
             constexpr int kBlkA = NR >= 8 ? NPV / 32 : NPV / 16;  // blocks always stored
 #pragma unroll
             for (int bk = 0; bk < kBlkA; ++bk)
               *reinterpret_cast<uint4*>(pt + bk * 2048 + x * 16) =
                   make_uint4(words[4 * bk], words[4 * bk + 1], words[4 * bk + 2], words[4 * bk + 3]);
             if constexpr (kBlkA < NPV / 16) {
-              const uint32_t bit = 1u << bs(i + a);
+              const uint32_t bit = 1u << ((i + a) % NPB);
               if (WB || (b_dirty & bit)) {
 #pragma unroll
                 for (int bk = kBlkA; bk < NPV / 16; ++bk)
@@ -976,6 +983,15 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
             }
           }
         };
+        if constexpr (NPB < NSB) {
+          // this pair's P buffers last held the pair before the previous one:
+          // wait until the MMAs have read them (the commit after PV_{i-1}
+          // covers every earlier product)
+          if (i >= NPB) {
+            ok = tc::mbar_wait(tc::smem_u32(&ctl.o_full[bs(i - 1)]), bp(i - 1), abort, kWaitLimitNs);
+            if (!ok) break;
+          }
+        }
         if (need_b)
           make_p(std::true_type{});
         else
@@ -1110,7 +1126,7 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
   DecodeParams p = p0;
   // the ring depth the shared memory holds (even, at least 2)
   auto smem_bytes = [&](int stages) {
-    return int(tc_smem_layout(stages, NQK, NPV, tc_nsb(NR), D / 128).total) + 1024;
+    return int(tc_smem_layout(stages, NQK, NPV, tc_npb(NR), D / 128).total) + 1024;
   };
   if (p.kv_stages <= 0) {
     // default: the deepest ring up to 6 entries that keeps two CTAs per SM

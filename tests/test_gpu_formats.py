@@ -119,7 +119,7 @@ def test_full_size(name):
     in e3m2 and e2m1, in the benchmark's launch settings: a seeded tenth of
     the (request, KV head) units plus the last one."""
     w = synth.WORKLOADS[name]()
-    got = run_gpu(w, impl=0, ctas_per_sm=2, max_splits=64, kv_stages=4, q_mode="fp8_fused")
+    got = run_gpu(w, impl=0, ctas_per_sm=2, max_splits=64, kv_stages=6, q_mode="fp8_fused")
     units = sorted(set(sample_units(w, -(-w.num_seqs * w.h_k // 10), seed=3)) | {(w.num_seqs - 1, w.h_k - 1)})
     assert 10 * len(units) >= w.num_seqs * w.h_k
     ref, _, _, _ = run_oracle(w, units=units)

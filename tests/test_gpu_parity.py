@@ -145,7 +145,7 @@ FULL = {
     "long_single": dict(ctas_per_sm=2, max_splits=64),
     "spec_verify": dict(ctas_per_sm=4, max_splits=64, kv_stages=4),
     "spec_verify_noncausal": dict(ctas_per_sm=4, max_splits=64, kv_stages=4),
-    "fp6_decode": dict(ctas_per_sm=2, max_splits=64, kv_stages=4),
+    "fp6_decode": dict(ctas_per_sm=2, max_splits=64, kv_stages=6),
 }
 
 

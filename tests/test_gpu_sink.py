@@ -28,6 +28,8 @@ IMPLS = [2, 1]  # MJ_IMPL_TCGEN05, MJ_IMPL_SIMT
 CASES = {
     "long_single_131072": ([131072], [0]),
     "four_rows_32768": ([32768, 32768, 32768, 32768], [0, 5000, -1, 20000]),
+    # 64/8 heads: 8-row tiles (tile pairs, two P buffers, the single-bound exchange)
+    "gqa8_two_rows_32768": ([32768, 32768], [7, -3], dict(h_q=64)),
 }
 # plans: unsplit, and split the way the long-context benchmark plans
 PLANS = {"unsplit": dict(ctas_per_sm=2, max_splits=1), "split": dict(ctas_per_sm=2, max_splits=64)}
@@ -48,8 +50,8 @@ _cache = {}
 
 def _workload(name):
     if name not in _cache:
-        lens, pos = CASES[name]
-        w = synth.sink_case(name=name, seq_lens=lens, sink_pos=pos, gap_binades=20.0)
+        lens, pos, *kw = CASES[name]
+        w = synth.sink_case(name=name, seq_lens=lens, sink_pos=pos, gap_binades=20.0, **(kw[0] if kw else {}))
         ref, lse, _, _ = run_oracle(w)
         _cache.clear()
         _cache[name] = (w, ref, lse)

@@ -73,7 +73,11 @@ constexpr int kConvThreads = kThreadsTcFp6 - 7 * 32;
 constexpr int kConvWarp0 = 7;
 constexpr int kSoftmaxWarp0 = 2;     // warps 2-5: softmax warpgroup
 constexpr int kVProducerWarp = 6;
-constexpr int kPrefetchTiles = 3;  // tiles a CTA asks L2 for before the programmatic-launch wait
+// tiles a CTA asks L2 for before the programmatic-launch wait: more in the
+// first wave, whose CTAs can start while the preceding kernel still runs,
+// unless a split grid runs in several waves (measured: the deeper prefetch
+// then costs the later waves more than it gives the first)
+constexpr int kPrefetchTiles = 4, kPrefetchTilesFirstWave = 8;
 constexpr int kTileBytes = kKvTile * 128;  // 128 keys x 128 bytes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -207,11 +211,12 @@ __host__ __device__ constexpr uint32_t mma_kv_type(int kf) {
 // power of two it allocates. An instance that needs all 512 columns must run
 // alone on its SM (launch_tc sizes its shared memory so that it does).
 __host__ __device__ constexpr int tc_nsb(int /*nr*/) { return 4; }  // S buffers in flight
-// P buffers in shared memory: one per S buffer, except at 8 rows, where two
-// (one tile pair) leave room for a 6-entry ring at two CTAs per SM; the
-// softmax then writes a pair's P only once the PV products of the pair
-// before it are complete.
-__host__ __device__ constexpr int tc_npb(int nr) { return nr == 8 ? 2 : tc_nsb(nr); }
+// P buffers in shared memory: one per S buffer, except at 8 and 16 rows
+// (tile pairs), where two (one pair) leave room for a 6-entry ring at two
+// CTAs per SM at 8 rows and shrink the footprint at 16; the softmax then
+// writes a pair's P only once the PV products of the pair before it are
+// complete.
+__host__ __device__ constexpr int tc_npb(int nr) { return (nr == 8 || nr == 16) ? 2 : tc_nsb(nr); }
 __host__ __device__ constexpr int tc_tmem_cols_used(int nqk, int npv, int nr, int d) {
   return tc_nsb(nr) * nqk + (d / 128) * npv;
 }
@@ -311,8 +316,9 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   // softmax warps wait, before they read them.
   //
   // Before that wait, the two TMA producer warps ask L2 for the first
-  // kPrefetchTiles tiles of the CTA's work row (its K and its V pages, one
-  // page per lane): HBM streams them while the preceding kernel finishes, and
+  // kPrefetchTiles tiles of the CTA's work row (its K and its V pages, the
+  // lanes taking every 32nd page; kPrefetchTilesFirstWave in the first wave
+  // of a grid without a split or of one wave): HBM streams them while the preceding kernel finishes, and
   // a CTA that starts later has them requested before it has read seq_lens.
   // A prefetch hands nothing to the SM, and L2 is where the preceding
   // kernel's writes land, so it cannot return stale data: the work row and
@@ -324,11 +330,17 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
       const int gp = int(blockIdx.x % unsigned(p.h_k));
       if (blockIdx.y == 0 && wp.z > wp.y && wp.x >= 0 && wp.x < p.num_seqs) {
         const int ppt = kKvTile / p.page_size;
-        const int64_t e = int64_t(wp.y) * ppt + lane;  // block-table entry of this lane's page
-        if (lane < min(kPrefetchTiles, wp.z - wp.y) * ppt && e < p.bt_stride) {
+        const int64_t grid = int64_t(gridDim.x) * gridDim.y;
+        const bool deep = int64_t(blockIdx.x) + int64_t(gridDim.x) * blockIdx.y < p.first_wave &&
+                          (!p.with_reduction || grid <= p.first_wave);
+        const int depth = deep ? kPrefetchTilesFirstWave : kPrefetchTiles;
+        const int n = min(depth, wp.z - wp.y) * ppt;  // pages
+        const CUtensorMap* map = warp == 0 ? &tmap_k : &tmap_v;
+        for (int k = lane; k < n; k += 32) {
+          const int64_t e = int64_t(wp.y) * ppt + k;  // block-table entry of the page
+          if (e >= p.bt_stride) break;
           const int pg = p.block_table[int64_t(wp.x) * p.bt_stride + e];
           if (pg >= 0 && int64_t(pg) < p.num_pages) {
-            const CUtensorMap* map = warp == 0 ? &tmap_k : &tmap_v;
 #pragma unroll
             for (int dh = 0; dh < DH; ++dh) {
               if (p.tma_head_inner)
@@ -1157,6 +1169,21 @@ cudaError_t launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const Decode
     while (bytes > have && !configured[dev].compare_exchange_weak(have, bytes, std::memory_order_acq_rel)) {
     }
   }
+  // CTAs resident at once (the first wave), looked up once per device and
+  // shared-memory size
+  static std::atomic<int64_t> first_wave[kMaxDevices];  // (bytes << 32) | CTAs
+  int64_t fw = first_wave[dev].load(std::memory_order_acquire);
+  if ((fw >> 32) != int64_t(bytes)) {
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_tc_kernel<NQK, NPV, NR, KF, QM, D>,
+                                                      KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc, size_t(bytes));
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    fw = (int64_t(bytes) << 32) | int64_t(per_sm) * sms;
+    first_wave[dev].store(fw, std::memory_order_release);
+  }
+  p.first_wave = int(fw & 0xFFFFFFFFll);
   cudaLaunchConfig_t cfg = {};
   if (int64_t(p.num_work) * p.h_k > INT32_MAX || p.n_row_tiles > 65535) return cudaErrorInvalidConfiguration;
   cfg.gridDim = dim3(unsigned(p.num_work) * unsigned(p.h_k), unsigned(p.n_row_tiles));

@@ -56,6 +56,7 @@ struct DecodeParams {
   int kv_format, page_size, row_bytes;
   int64_t num_pages;
   int tw, n_row_tiles;  // query rows per CTA, row tiles per (request, head)
+  int first_wave;       // tensor-core kernel: CTAs resident at once on the device
 
   const uint8_t* q_codes;
   const float* q_descale;

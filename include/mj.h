@@ -249,8 +249,8 @@ typedef struct mj_decode_args {
   int impl;          /* mj_impl */
   int kv_stages;     /* KV ring depth of the tensor-core kernel, in K or V tiles (made even,
                         at most 13, and lowered to what shared memory holds); 0 = the
-                        deepest even ring up to 6 that keeps two CTAs per SM (4 query rows
-                        per tile at d = 128: 6; 8 or 16 rows: 4; d = 256: 2) */
+                        deepest even ring up to 6 that keeps two CTAs per SM (4 or 8 query
+                        rows per tile at d = 128: 6; 16 rows: 4; d = 256: 2) */
   int evict_first;   /* 1 = L2 evict-first hint on KV loads (KV is read once) */
 
   int out_dtype;     /* mj_out_dtype of `out` (0 = bf16); rounding to nearest even */

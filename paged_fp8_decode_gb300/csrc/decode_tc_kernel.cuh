@@ -44,6 +44,11 @@
 //   request's last, partial tile the V producer warp also zeroes the V rows
 //   past the end before the PV product (page tails may hold NaN codes, and
 //   0 * NaN would reach O through the MMA).
+// * The launch may overlap the preceding kernel (programmatic dependent
+//   launch). Before its wait for that kernel, the producer warps ask L2 for
+//   the CTA's first KV tiles (a prefetch returns no data, so a guess made
+//   from inputs not yet final costs traffic, never correctness); a grid that
+//   does not split lets the next kernel launch early in turn.
 // * Every wait is bounded (2 s); a timeout raises a status bit and the CTA
 //   unwinds, frees its TMEM and returns.
 #include <cuda.h>

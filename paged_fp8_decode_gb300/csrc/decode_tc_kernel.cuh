@@ -79,10 +79,11 @@ constexpr int kConvWarp0 = 7;
 constexpr int kSoftmaxWarp0 = 2;     // warps 2-5: softmax warpgroup
 constexpr int kVProducerWarp = 6;
 // tiles a CTA asks L2 for before the programmatic-launch wait: more in the
-// first wave, whose CTAs can start while the preceding kernel still runs,
-// unless a split grid runs in several waves (measured: the deeper prefetch
-// then costs the later waves more than it gives the first)
-constexpr int kPrefetchTiles = 4, kPrefetchTilesFirstWave = 8;
+// first wave, whose CTAs can start while the preceding kernel still runs (16
+// when the grid is at most two waves, else 8), unless a split grid runs in
+// several waves (measured: a deeper prefetch then costs the later waves more
+// than it gives the first)
+constexpr int kPrefetchTiles = 4, kPrefetchTilesFirstWave = 8, kPrefetchTilesShortGrid = 16;
 constexpr int kTileBytes = kKvTile * 128;  // 128 keys x 128 bytes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -322,8 +323,8 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   //
   // Before that wait, the two TMA producer warps ask L2 for the first
   // kPrefetchTiles tiles of the CTA's work row (its K and its V pages, the
-  // lanes taking every 32nd page; kPrefetchTilesFirstWave in the first wave
-  // of a grid without a split or of one wave): HBM streams them while the preceding kernel finishes, and
+  // lanes taking every 32nd page; more in the first wave of a grid without a
+  // split or of one wave): HBM streams them while the preceding kernel finishes, and
   // a CTA that starts later has them requested before it has read seq_lens.
   // A prefetch hands nothing to the SM, and L2 is where the preceding
   // kernel's writes land, so it cannot return stale data: the work row and
@@ -338,7 +339,8 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
         const int64_t grid = int64_t(gridDim.x) * gridDim.y;
         const bool deep = int64_t(blockIdx.x) + int64_t(gridDim.x) * blockIdx.y < p.first_wave &&
                           (!p.with_reduction || grid <= p.first_wave);
-        const int depth = deep ? kPrefetchTilesFirstWave : kPrefetchTiles;
+        const int depth = !deep ? kPrefetchTiles
+                                : (grid <= 2 * int64_t(p.first_wave) ? kPrefetchTilesShortGrid : kPrefetchTilesFirstWave);
         const int n = min(depth, wp.z - wp.y) * ppt;  // pages
         const CUtensorMap* map = warp == 0 ? &tmap_k : &tmap_v;
         for (int k = lane; k < n; k += 32) {

@@ -34,7 +34,9 @@
  *    CUDA graph and replayed with new plans written into the same buffers
  *    (runner page, module docstring: the plan's buffers keep their
  *    addresses and the grid keeps its size per q_len, so a captured graph
- *    stays valid).
+ *    stays valid). The first launch of a kernel configuration on a device
+ *    raises its shared-memory limit and queries its occupancy (host calls,
+ *    cached): make one call of each configuration before capturing it.
  */
 #ifndef MJ_H
 #define MJ_H
@@ -356,8 +358,8 @@ MJ_API int mj_merge_lse(const mj_decode_args* args, void* stream);
  * partials need more (mj_workspace_size(part_seqs, max_splits, ...) above the
  * limit) is rejected with MJ_ERR_CAPACITY before anything is enqueued. The
  * first call on a device looks up the array's device address and zeroes its
- * status header (synchronously); make that first call before any stream
- * capture. All calls share the array and it keeps the last call's contents:
+ * status header on the caller's stream; make that first call before any
+ * stream capture. All calls share the array and it keeps the last call's contents:
  * calls whose kernels overlap on the GPU race on it, so issue them in order
  * on one stream. The kernels record anomalies (a page id out of range, a
  * bounded wait that timed out, a work row outside the partial area) in a

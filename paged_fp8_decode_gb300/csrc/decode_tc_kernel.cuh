@@ -323,9 +323,10 @@ __global__ void __launch_bounds__(KF != MJ_KV_E4M3 ? kThreadsTcFp6 : kThreadsTc,
   //
   // Before that wait, the two TMA producer warps ask L2 for the first
   // kPrefetchTiles tiles of the CTA's work row (its K and its V pages, the
-  // lanes taking every 32nd page; more in the first wave of a grid without a
-  // split or of one wave): HBM streams them while the preceding kernel finishes, and
-  // a CTA that starts later has them requested before it has read seq_lens.
+  // lanes taking every 32nd page; more in the first wave of a grid without
+  // a split or of one wave): HBM streams them while the preceding kernel
+  // finishes, and a CTA that starts later has them requested before it has
+  // read seq_lens.
   // A prefetch hands nothing to the SM, and L2 is where the preceding
   // kernel's writes land, so it cannot return stale data: the work row and
   // block-table entries it is aimed with are only a guess (read before the
